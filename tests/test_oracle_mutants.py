@@ -1,0 +1,55 @@
+"""Plant plausible mistakes in a copy of the oracle and check the pins catch
+each one.  The mistakes are planted in the oracle source, on the CPU only."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle_pins
+from oracle import build as obuild
+
+# (name, original text, planted text): a dropped term, a wrong sign or index,
+# a transposed operand, an off-by-one mask, a wrong normaliser.
+MUTANTS = [
+    ("drop_scale", "s[j] = scale * dot;", "s[j] = dot;"),
+    ("k_is_v", "qi[d] * K[(size_t)j * D + d]", "qi[d] * V[(size_t)j * D + d]"),
+    ("causal_off_by_one", "&& j > i) return 0;", "&& j >= i) return 0;"),
+    ("causal_flipped", "&& j > i) return 0;", "&& j < i) return 0;"),
+    ("padding_off_by_one", "if (j >= len) return 0;", "if (j > len) return 0;"),
+    ("no_max_shift", "s[j] = exp(s[j] - M);", "s[j] = exp(s[j]);"),
+    ("no_normalise", "double w = s[j] / Z;", "double w = s[j];"),
+    ("min_not_max", "if (!any || s[j] > M) M = s[j];", "if (!any || s[j] < M) M = s[j];"),
+    ("unbiased_var", "var /= N;", "var /= (N - 1);"),
+    ("eps_outside", "1.0 / sqrt(var + eps)", "1.0 / (sqrt(var) + eps)"),
+    ("gamma_beta_swapped", "* rstd * gamma[c] + beta[c]", "* rstd * beta[c] + gamma[c]"),
+    ("head_split_transposed",
+     "x[((size_t)b * Lq + i) * (size_t)H * D + (size_t)h * D + d];",
+     "x[((size_t)b * Lq + i) * (size_t)H * D + (size_t)d * H + h];"),
+    ("pv_uses_k", "o[d] += w * V[(size_t)j * D + d];", "o[d] += w * K[(size_t)j * D + d];"),
+    ("length_of_batch0", "int len = kv_lengths[b];", "int len = kv_lengths[0];"),
+    ("rows_api_head_index", "size_t bh = (size_t)b * H + (size_t)h;\n        attend_row",
+     "size_t bh = (size_t)h * B + (size_t)b;\n        attend_row"),
+]
+
+
+@pytest.fixture(scope="module")
+def workdir(tmp_path_factory):
+    return tmp_path_factory.mktemp("mutants")
+
+
+def test_unmutated_oracle_passes_all_pins():
+    assert oracle_pins.run_all() == []
+
+
+@pytest.mark.parametrize("name,orig,planted", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(workdir, name, orig, planted):
+    src = open(obuild.SRC).read()
+    assert src.count(orig) == 1, "mutation anchor not unique: %s" % name
+    path = os.path.join(str(workdir), name + ".c")
+    with open(path, "w") as f:
+        f.write(src.replace(orig, planted))
+    lib = os.path.join(str(workdir), "lib%s.so" % name)
+    obuild.build(force=True, src=path, out=lib)
+    fails = oracle_pins.run_all(path=lib)
+    assert fails, "mutant %s survived every pin" % name
