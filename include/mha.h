@@ -1,0 +1,152 @@
+/*
+ * mha.h -- C ABI of the GB300 (sm_103a) fused masked multi-head attention
+ * forward library (libmha.so).
+ *
+ * What is computed.  For every batch b, head h and query row i:
+ *     s_j = scale * sum_d Q[b,h,i,d] * K[b,h,j,d]
+ *     visible(i, j) = (j < len_b if MHA_MASK_KV_LEN) and (j <= i if MHA_MASK_CAUSAL)
+ *     O[b,h,i,:] = sum_j softmax_j(s over visible j) * V[b,h,j,:]
+ * with the softmax taken after subtracting the running row maximum (online
+ * softmax), masked keys contributing exactly zero, and a row with no visible
+ * key returning zeros.  Sources, cited by page title and section:
+ *  - "How to fuse cross-attention and layer-norm into a single CUDA kernel?"
+ *    (cms365.cn), knowledge points: S = QK^T -> P = softmax(S) -> O = PV;
+ *    answer steps two to five: Pre-LayerNorm on the query rows and the
+ *    extension signature (q, k, v, gamma, beta, eps).
+ *  - "masked multi head attention" CUDA article (2kiu.com/news/6063113),
+ *    sections 1, 3.1 and 6.1: causal and padding masks applied as -infinity
+ *    before the softmax; an extern "C" wrapper over raw device pointers.
+ *  - "Why attention must compute the max first" essay (gsyq.cn/news/340375),
+ *    sections 2.3-2.4 (online softmax fused with QK^T and PV), 3.1 (max
+ *    shift) and 5.2 (divide the logits by sqrt(d_k)).
+ *
+ * Conventions for every entry point.
+ *  - Pointers are DEVICE pointers owned by the caller; the library allocates
+ *    no device memory and keeps no per-call state.
+ *  - Layouts are dense and row-major: q, out [B,H,Lq,D]; k, v [B,H,Lk,D];
+ *    kv_lengths int32 [B].  Every tensor pointer must be 16-byte aligned.
+ *  - Work is enqueued on `stream` (0 = legacy default stream); no entry
+ *    point synchronises.  Results are valid once the stream reaches them.
+ *  - Host-detectable errors return a negative mha_status and launch nothing.
+ *    A launch failure returns MHA_ERR_CUDA.  Device-side waits are bounded:
+ *    if one ever expires the kernel records it in a status word (see
+ *    mha_device_status) and returns instead of hanging.
+ *  - Values at masked key positions must be finite: a masked key's weight
+ *    is exactly zero, and 0 * finite = 0.
+ */
+#ifndef MHA_GB300_H
+#define MHA_GB300_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MHA_API __attribute__((visibility("default")))
+#else
+#define MHA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MHA_OK = 0,
+    MHA_ERR_INVALID_ARG = -1,   /* null pointer, non-positive size, bad scale/eps, bad mask */
+    MHA_ERR_UNSUPPORTED = -2,   /* D not in {64, 128}, dtype not handled by this entry point */
+    MHA_ERR_MISALIGNED = -3,    /* a tensor pointer is not 16-byte aligned */
+    MHA_ERR_CUDA = -4,          /* the CUDA runtime or driver reported an error */
+    MHA_ERR_DEVICE = -5         /* a kernel's bounded wait expired (see mha_device_status) */
+} mha_status;
+
+/* Mask kinds: bit flags, combinable (MHA_MASK_CAUSAL | MHA_MASK_KV_LEN). */
+enum { MHA_MASK_NONE = 0, MHA_MASK_CAUSAL = 1, MHA_MASK_KV_LEN = 2 };
+
+/* Element types of q/k/v/out (and x_q).  MHA_F32 runs on CUDA-core FFMA;
+ * MHA_BF16 runs on tcgen05 tensor cores with fp32 accumulation in TMEM. */
+enum { MHA_F32 = 0, MHA_BF16 = 1 };
+
+/*
+ * mha_fwd -- fused masked multi-head attention forward.
+ *   q           [B,H,Lq,D] of `dtype`
+ *   k, v        [B,H,Lk,D] of `dtype`
+ *   mask_kind   MHA_MASK_* bits.  Causal alignment is top-left: key j is
+ *               visible to query i iff j <= i (also when Lq != Lk).
+ *   kv_lengths  device int32 [B]; read only when MHA_MASK_KV_LEN is set (it
+ *               must then be non-NULL).  Keys j >= kv_lengths[b] are hidden
+ *               for every query row of batch b.  Values are clamped to
+ *               [0, Lk] on the device; 0 gives all-zero output rows.
+ *   out         [B,H,Lq,D] of `dtype`, written once.  Must not alias inputs.
+ *   B, H, Lq    >= 0 (a zero extent is a no-op); Lk >= 0 (0 gives zeros).
+ *   D           64 or 128.
+ *   scale       logit multiplier, finite and > 0 (usually 1/sqrt(D)).
+ *   dtype       MHA_F32 or MHA_BF16.
+ *   stream      CUDA stream the kernel is enqueued on.
+ * Returns MHA_OK or a negative mha_status.
+ */
+MHA_API int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
+            const int32_t *kv_lengths, void *out, int B, int H, int Lq, int Lk,
+            int D, float scale, int dtype, cudaStream_t stream);
+
+/*
+ * prenorm_cross_attn_fwd -- Pre-LayerNorm cross-attention forward
+ * (cms365.cn answer, steps two and three).  For every (b, i):
+ *     xhat = (x_q[b,i,:] - mean) / sqrt(var + eps) * gamma + beta
+ * over the H*D features of the row (biased variance), Q[b,h,i,:] is the
+ * head-h slice xhat[h*D:(h+1)*D], and the attention above runs with the
+ * padding mask only (kv_lengths, or none when it is NULL).
+ *   x_q         [B,Lq,H*D] bf16 (query-side activations)
+ *   gamma, beta fp32 [H*D]
+ *   eps         finite, >= 0
+ *   k, v        [B,H,Lk,D] bf16 (encoder keys and values)
+ *   kv_lengths  device int32 [B] or NULL (all Lk keys visible)
+ *   out         [B,Lq,H*D] bf16 (heads merged back into the model dim)
+ *   dtype       must be MHA_BF16 (MHA_ERR_UNSUPPORTED otherwise)
+ * Other arguments as for mha_fwd.
+ */
+MHA_API int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const float *beta,
+                           float eps, const void *k, const void *v,
+                           const int32_t *kv_lengths, void *out, int B, int H,
+                           int Lq, int Lk, int D, float scale, int dtype,
+                           cudaStream_t stream);
+
+/* Static, human-readable text for an mha_status value. */
+MHA_API const char *mha_strerror(int status);
+
+/*
+ * mha_device_status -- read (and optionally clear) the device status word
+ * that kernels set when a bounded wait expires.  Bit k set means wait site
+ * k timed out (site numbers are listed in the kernel sources).  Synchronous:
+ * copies from the current device.  Returns MHA_OK or MHA_ERR_CUDA.
+ */
+MHA_API int mha_device_status(uint32_t *bits, int clear);
+
+/*
+ * mha_selftest_umma -- diagnostic: one 128-row tcgen05 GEMM tile built
+ * with exactly the shared-memory/TMEM descriptors the bf16 attention kernel
+ * uses, so the descriptor encoding can be checked against a host matmul.
+ *   variant 0: C[128,128] = A[128,K] * B[128,K]^T, both K-major in shared
+ *              memory (the S = Q K^T step); K = 64 or 128.
+ *   variant 1: C[128,N] = A[128,128] * B[128,N], A K-major and B N-major in
+ *              shared memory (the P V step with P staged in shared memory).
+ *   variant 2: as variant 1 but A is first written to tensor memory and the
+ *              MMA reads it from there (the P V step the kernel uses).
+ *   a, b bf16 row-major device buffers; c fp32 [128, N or 128] row-major.
+ * Returns MHA_OK or a negative mha_status.
+ */
+MHA_API int mha_selftest_umma(int variant, int K_or_N, const void *a, const void *b,
+                      float *c, cudaStream_t stream);
+
+/*
+ * mha_set_bf16_grid -- launch-shape hook for benchmarks: cap the bf16
+ * kernels' grid at `ctas` CTAs, each then loops over several work items
+ * (persistent scheduling); 0 restores one CTA per work item.  Affects later
+ * calls from any thread of the process.
+ */
+MHA_API void mha_set_bf16_grid(int ctas);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHA_GB300_H */

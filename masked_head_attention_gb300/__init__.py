@@ -1,0 +1,177 @@
+"""GB300 (sm_103a) fused masked multi-head attention forward.
+
+Thin ctypes binding over the C ABI of libmha.so (include/mha.h).  Every step
+of the computation runs in the library's CUDA kernels; this module only
+checks tensor metadata and passes device pointers, sizes and the current
+CUDA stream.  PyTorch provides device memory and streams, nothing else.
+
+There is no fallback: if libmha.so has not been built (see build.py, or
+``__graft_entry__.build()``), every call raises ``MhaError``.
+"""
+import ctypes
+import math
+import os
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_KV_LEN = 2
+F32 = 0
+BF16 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmha.so")
+_lib = None
+
+
+class MhaError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (what, _strerror_safe(status), status))
+
+
+def _strerror_safe(code):
+    try:
+        return lib().mha_strerror(code).decode()
+    except Exception:  # library itself unavailable
+        return "status %d" % code
+
+
+def lib():
+    """The loaded libmha.so (raises MhaError when it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MhaError(-4, "loading %s (not built)" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.mha_fwd.argtypes = [P, P, P, i, P, P, i, i, i, i, i, f, i, P]
+        L.mha_fwd.restype = i
+        L.prenorm_cross_attn_fwd.argtypes = [P, P, P, f, P, P, P, P, i, i, i, i, i, f, i, P]
+        L.prenorm_cross_attn_fwd.restype = i
+        L.mha_strerror.argtypes = [i]
+        L.mha_strerror.restype = ctypes.c_char_p
+        L.mha_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
+        L.mha_device_status.restype = i
+        L.mha_selftest_umma.argtypes = [i, i, P, P, P, P]
+        L.mha_selftest_umma.restype = i
+        L.mha_set_bf16_grid.argtypes = [i]
+        L.mha_set_bf16_grid.restype = None
+        _lib = L
+    return _lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, name, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("unsupported dtype %s (float32 or bfloat16)" % t.dtype)
+
+
+def _check(status, what):
+    if status != 0:
+        raise MhaError(status, what)
+
+
+def mha_fwd(q, k, v, mask_kind=MASK_NONE, kv_lengths=None, out=None, scale=None, stream=None):
+    """Fused masked MHA forward; q [B,H,Lq,D], k/v [B,H,Lk,D] (fp32 or bf16).
+
+    mask_kind: MASK_CAUSAL and/or MASK_KV_LEN bits; kv_lengths int32 [B] on
+    the device when MASK_KV_LEN is set.  Returns `out` [B,H,Lq,D]."""
+    torch = _torch()
+    _dev(q, "q")
+    _dev(k, "k", q.dtype)
+    _dev(v, "v", q.dtype)
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    if tuple(k.shape) != (B, H, Lk, D) or tuple(v.shape) != (B, H, Lk, D):
+        raise ValueError("k and v must be [B,H,Lk,D] matching q")
+    if kv_lengths is not None:
+        _dev(kv_lengths, "kv_lengths", torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _dev(out, "out", q.dtype)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(lib().mha_fwd(_ptr(q), _ptr(k), _ptr(v), int(mask_kind), _ptr(kv_lengths), _ptr(out),
+                         B, H, Lq, Lk, D, scale, _dtype_code(q), _stream(stream)), "mha_fwd")
+    return out
+
+
+def prenorm_cross_attn_fwd(x_q, gamma, beta, eps, k, v, kv_lengths=None, out=None, scale=None,
+                           stream=None):
+    """Pre-LayerNorm cross-attention; x_q [B,Lq,H*D] bf16, gamma/beta fp32
+    [H*D], k/v [B,H,Lk,D] bf16.  Returns `out` [B,Lq,H*D] bf16."""
+    torch = _torch()
+    _dev(x_q, "x_q", torch.bfloat16)
+    _dev(gamma, "gamma", torch.float32)
+    _dev(beta, "beta", torch.float32)
+    _dev(k, "k", torch.bfloat16)
+    _dev(v, "v", torch.bfloat16)
+    B, H, Lk, D = k.shape
+    Lq = x_q.shape[1]
+    if tuple(x_q.shape) != (B, Lq, H * D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("x_q must be [B,Lq,H*D] and v [B,H,Lk,D]")
+    if gamma.numel() != H * D or beta.numel() != H * D:
+        raise ValueError("gamma and beta must have H*D elements")
+    if kv_lengths is not None:
+        _dev(kv_lengths, "kv_lengths", torch.int32)
+    if out is None:
+        out = torch.empty_like(x_q)
+    else:
+        _dev(out, "out", torch.bfloat16)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(lib().prenorm_cross_attn_fwd(_ptr(x_q), _ptr(gamma), _ptr(beta), float(eps), _ptr(k),
+                                        _ptr(v), _ptr(kv_lengths), _ptr(out), B, H, Lq, Lk, D,
+                                        scale, BF16, _stream(stream)), "prenorm_cross_attn_fwd")
+    return out
+
+
+def mha_strerror(status):
+    return lib().mha_strerror(int(status)).decode()
+
+
+def device_status(clear=False):
+    """Bits of the device status word (nonzero: a bounded wait expired)."""
+    bits = ctypes.c_uint32(0)
+    _check(lib().mha_device_status(ctypes.byref(bits), 1 if clear else 0), "mha_device_status")
+    return bits.value
+
+
+def selftest_umma(variant, kn, a, b, c, stream=None):
+    """Diagnostic tcgen05 GEMM tile (see mha_selftest_umma in include/mha.h)."""
+    _check(lib().mha_selftest_umma(int(variant), int(kn), _ptr(a), _ptr(b), _ptr(c),
+                                   _stream(stream)), "mha_selftest_umma")
+    return c
+
+
+def set_bf16_grid(ctas):
+    lib().mha_set_bf16_grid(int(ctas))

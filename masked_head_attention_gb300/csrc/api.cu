@@ -1,0 +1,140 @@
+// api.cu -- the extern "C" boundary of libmha.so: argument validation,
+// dispatch by (entry point, dtype, D), and status reporting.  Host code only;
+// the kernels live in fwd_f32.cu and fwd_bf16.cu.
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mha.h"
+#include "internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA; }
+
+// Shared checks of the shape arguments; 1 means "nothing to do".
+int check_shape(int B, int H, int Lq, int Lk, int D, float scale, int *empty) {
+    *empty = 0;
+    if (B < 0 || H < 0 || Lq < 0 || Lk < 0) return MHA_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return MHA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return MHA_ERR_UNSUPPORTED;
+    if (B > 65535) return MHA_ERR_INVALID_ARG;                 // grid z of the fp32 path
+    const int64_t n_qt = ((int64_t)Lq + 127) / 128;
+    if ((int64_t)B * H * (n_qt > 0 ? n_qt : 1) > 0x7fffffffLL) return MHA_ERR_INVALID_ARG;
+    if (B == 0 || H == 0 || Lq == 0) *empty = 1;
+    return MHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
+            const int32_t *kv_lengths, void *out, int B, int H, int Lq, int Lk, int D,
+            float scale, int dtype, cudaStream_t stream) {
+    int empty = 0;
+    int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
+    if (st != MHA_OK) return st;
+    if (mask_kind < 0 || mask_kind > (MHA_MASK_CAUSAL | MHA_MASK_KV_LEN)) return MHA_ERR_INVALID_ARG;
+    if (dtype != MHA_F32 && dtype != MHA_BF16) return MHA_ERR_UNSUPPORTED;
+    if (empty) return MHA_OK;
+    if (!q || !out || (Lk > 0 && (!k || !v))) return MHA_ERR_INVALID_ARG;
+    if ((mask_kind & MHA_MASK_KV_LEN) && !kv_lengths) return MHA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || (Lk > 0 && (!aligned16(k) || !aligned16(v))))
+        return MHA_ERR_MISALIGNED;
+    if (dtype == MHA_F32)
+        return from_cuda(mha::launch_fwd_f32(
+            static_cast<const float *>(q), static_cast<const float *>(k),
+            static_cast<const float *>(v), kv_lengths, static_cast<float *>(out), B, H, Lq, Lk,
+            D, mask_kind, scale, stream));
+    mha::Bf16Call c{};
+    c.q = q;
+    c.k = k;
+    c.v = v;
+    c.kv_lengths = kv_lengths;
+    c.out = out;
+    c.B = B;
+    c.H = H;
+    c.Lq = Lq;
+    c.Lk = Lk;
+    c.D = D;
+    c.mask_kind = mask_kind;
+    c.scale = scale;
+    int drv = 0;
+    cudaError_t e = mha::launch_fwd_bf16(c, stream, &drv);
+    if (drv != 0) return MHA_ERR_CUDA;
+    return from_cuda(e);
+}
+
+int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const float *beta, float eps,
+                           const void *k, const void *v, const int32_t *kv_lengths, void *out,
+                           int B, int H, int Lq, int Lk, int D, float scale, int dtype,
+                           cudaStream_t stream) {
+    int empty = 0;
+    int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
+    if (st != MHA_OK) return st;
+    if (dtype != MHA_BF16) return MHA_ERR_UNSUPPORTED;
+    if (!(std::isfinite(eps) && eps >= 0.f)) return MHA_ERR_INVALID_ARG;
+    if ((int64_t)H * D > 65536) return MHA_ERR_INVALID_ARG;
+    if (empty) return MHA_OK;
+    if (!x_q || !gamma || !beta || !out || (Lk > 0 && (!k || !v))) return MHA_ERR_INVALID_ARG;
+    if (!aligned16(x_q) || !aligned16(out) || !aligned16(gamma) || !aligned16(beta) ||
+        (Lk > 0 && (!aligned16(k) || !aligned16(v))))
+        return MHA_ERR_MISALIGNED;
+    mha::Bf16Call c{};
+    c.x = x_q;
+    c.gamma = gamma;
+    c.beta = beta;
+    c.eps = eps;
+    c.k = k;
+    c.v = v;
+    c.kv_lengths = kv_lengths;
+    c.out = out;
+    c.B = B;
+    c.H = H;
+    c.Lq = Lq;
+    c.Lk = Lk;
+    c.D = D;
+    c.mask_kind = kv_lengths ? MHA_MASK_KV_LEN : MHA_MASK_NONE;
+    c.scale = scale;
+    int drv = 0;
+    cudaError_t e = mha::launch_fwd_bf16(c, stream, &drv);
+    if (drv != 0) return MHA_ERR_CUDA;
+    return from_cuda(e);
+}
+
+const char *mha_strerror(int status) {
+    switch (status) {
+        case MHA_OK: return "success";
+        case MHA_ERR_INVALID_ARG: return "invalid argument (null pointer, bad size, scale, eps or mask)";
+        case MHA_ERR_UNSUPPORTED: return "unsupported configuration (D must be 64 or 128; dtype not handled)";
+        case MHA_ERR_MISALIGNED: return "a tensor pointer is not 16-byte aligned";
+        case MHA_ERR_CUDA: return "CUDA runtime or driver error";
+        case MHA_ERR_DEVICE: return "a kernel's bounded wait expired (see mha_device_status)";
+        default: return "unknown status";
+    }
+}
+
+int mha_device_status(uint32_t *bits, int clear) {
+    return from_cuda(mha::read_device_status(bits, clear != 0));
+}
+
+int mha_selftest_umma(int variant, int K_or_N, const void *a, const void *b, float *c,
+                      cudaStream_t stream) {
+    if (variant < 0 || variant > 2) return MHA_ERR_INVALID_ARG;
+    if (K_or_N != 64 && K_or_N != 128) return MHA_ERR_UNSUPPORTED;
+    if (!a || !b || !c) return MHA_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return MHA_ERR_MISALIGNED;
+    int drv = 0;
+    cudaError_t e = mha::launch_selftest_umma(variant, K_or_N, a, b, c, stream, &drv);
+    if (drv != 0) return MHA_ERR_CUDA;
+    return from_cuda(e);
+}
+
+// Benchmark hook: cap the bf16 grid at `ctas` CTAs (persistent scheduling);
+// 0 restores one CTA per work item.
+void mha_set_bf16_grid(int ctas) { mha::set_bf16_grid_override(ctas); }
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+// fwd_f32.cu -- fused masked multi-head attention forward for fp32 inputs on
+// CUDA-core FFMA (sm_103a).
+//
+// One CTA of 256 threads owns a 64-row query tile of one (b, h).  K and V
+// tiles of 64 keys are staged in shared memory; each thread keeps a 4 x 4
+// block of logits and a 4 x (D/16) block of the output in registers.  The
+// softmax is the online form (running row max m, rescaled running sum l),
+// with the row reductions done by warp shuffles inside the 16 lanes that
+// share a row group, the mask computed from (row, col, length) in registers
+// and key tiles beyond the causal limit or the valid length never loaded.
+//
+// Page sections this follows ("masked multi head attention" CUDA article,
+// 2kiu.com): 2 (one fused kernel, skip masked work), 3.1 (mask computed in
+// the kernel, -infinity before the softmax), 3.2 (row max by warp shuffles);
+// "Why attention must compute the max first" (gsyq.cn): 2.3-2.4 (online
+// softmax fused between QK^T and PV, scores never written to memory).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kBM = 64;        // query rows per CTA
+constexpr int kBN = 64;        // keys per tile
+constexpr int kThreads = 256;  // 16 x 16 thread grid: ty owns 4 rows, tx 4 key columns
+
+template <int D>
+struct F32Cfg {
+    static constexpr int LD = D + 4;     // padded row stride of the Q/K/V tiles (floats)
+    static constexpr int LDP = kBN + 4;  // padded row stride of the P tile
+    static constexpr int OC = D / 16;    // output columns per thread
+    static constexpr size_t kSmem = sizeof(float) * (size_t)(kBM * LD + 2 * kBN * LD + kBM * LDP);
+};
+
+// Copy rows [row0, row0 + 64) of a [rows, D] fp32 matrix into a padded tile;
+// rows at or beyond `nrows` become zero.
+template <int D>
+__device__ __forceinline__ void load_tile(float *dst, const float *__restrict__ src, int row0,
+                                          int nrows, int tid) {
+    constexpr int V4 = D / 4;
+#pragma unroll
+    for (int idx = tid; idx < kBN * V4; idx += kThreads) {
+        const int r = idx / V4, c = idx % V4;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row0 + r < nrows)
+            val = __ldg(reinterpret_cast<const float4 *>(src + (size_t)(row0 + r) * D) + c);
+        *reinterpret_cast<float4 *>(dst + r * F32Cfg<D>::LD + 4 * c) = val;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+    mha_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
+                       const float *__restrict__ v, const int32_t *__restrict__ kv_lengths,
+                       float *__restrict__ out, int H, int Lq, int Lk, int mask_kind,
+                       float scale_log2) {
+    using C = F32Cfg<D>;
+    extern __shared__ float4 f32_smem[];
+    float *sQ = reinterpret_cast<float *>(f32_smem);
+    float *sK = sQ + kBM * C::LD;
+    float *sV = sK + kBN * C::LD;
+    float *sP = sV + kBN * C::LD;
+
+    // Heaviest causal query tiles are launched first.
+    const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int q0 = qt * kBM;
+    const size_t bh = (size_t)b * H + h;
+    const float *Qg = q + bh * (size_t)Lq * D;
+    const float *Kg = k + bh * (size_t)Lk * D;
+    const float *Vg = v + bh * (size_t)Lk * D;
+    float *Og = out + bh * (size_t)Lq * D;
+
+    const bool causal = (mask_kind & 1) != 0;
+    int len = Lk;
+    if (mask_kind & 2) len = max(0, min((int)kv_lengths[b], Lk));
+    int kend = len;                                   // keys at or past kend are hidden for all rows
+    if (causal) kend = min(kend, q0 + kBM);
+    const int n_kt = (kend + kBN - 1) / kBN;
+
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+
+    load_tile<D>(sQ, Qg, q0, Lq, tid);
+
+    float o[4][C::OC];
+    float m[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < C::OC; ++c) o[i][c] = 0.f;
+    }
+
+    for (int t = 0; t < n_kt; ++t) {
+        const int k0 = t * kBN;
+        __syncthreads();  // the previous tile's P.V is done with sK, sV, sP
+        load_tile<D>(sK, Kg, k0, Lk, tid);
+        load_tile<D>(sV, Vg, k0, Lk, tid);
+        __syncthreads();
+
+        // S = Q K^T for rows 4*ty + i and keys tx + 16*j.
+        float s[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+#pragma unroll 4
+        for (int d = 0; d < D; d += 4) {
+            float4 qa[4], kb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                qa[i] = *reinterpret_cast<const float4 *>(sQ + (ty * 4 + i) * C::LD + d);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                kb[j] = *reinterpret_cast<const float4 *>(sK + (tx + 16 * j) * C::LD + d);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    s[i][j] = fmaf(qa[i].x, kb[j].x, s[i][j]);
+                    s[i][j] = fmaf(qa[i].y, kb[j].y, s[i][j]);
+                    s[i][j] = fmaf(qa[i].z, kb[j].z, s[i][j]);
+                    s[i][j] = fmaf(qa[i].w, kb[j].w, s[i][j]);
+                }
+        }
+
+        // Scale into the base-2 domain and mask; only a tile that crosses the
+        // visible end of some row needs the element test.
+        const bool edge = (k0 + kBN > len) || (causal && k0 + kBN - 1 > q0);
+        float mt[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = q0 + ty * 4 + i;
+            const int vis_end = causal ? min(len, row + 1) : len;
+            mt[i] = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float x = s[i][j] * scale_log2;
+                if (edge && (k0 + tx + 16 * j >= vis_end)) x = -INFINITY;
+                s[i][j] = x;
+                mt[i] = fmaxf(mt[i], x);
+            }
+        }
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], off));
+
+        // Online softmax update (base 2): m_new = max(m, tile max),
+        // alpha = 2^(m - m_new), p = 2^(s - m_new), l = alpha * l + sum p.
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float m_new = fmaxf(m[i], mt[i]);
+            const float msub = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = ex2_approx(m[i] - msub);
+            m[i] = m_new;
+            float rs = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float pj = ex2_approx(s[i][j] - msub);
+                s[i][j] = pj;
+                rs += pj;
+            }
+            l[i] = fmaf(l[i], alpha, rs);
+#pragma unroll
+            for (int c = 0; c < C::OC; ++c) o[i][c] *= alpha;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sP[(ty * 4 + i) * C::LDP + tx + 16 * j] = s[i][j];
+        __syncthreads();
+
+        // O += P V for rows 4*ty + i and output columns 4*tx (+ 64).
+#pragma unroll 2
+        for (int j = 0; j < kBN; j += 4) {
+            float4 pa[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                pa[i] = *reinterpret_cast<const float4 *>(sP + (ty * 4 + i) * C::LDP + j);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const float *vrow = sV + (j + jj) * C::LD + tx * 4;
+                float4 vv[C::OC / 4];
+#pragma unroll
+                for (int hv = 0; hv < C::OC / 4; ++hv)
+                    vv[hv] = *reinterpret_cast<const float4 *>(vrow + 64 * hv);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float pv = jj == 0 ? pa[i].x : jj == 1 ? pa[i].y : jj == 2 ? pa[i].z : pa[i].w;
+#pragma unroll
+                    for (int hv = 0; hv < C::OC / 4; ++hv) {
+                        o[i][4 * hv + 0] = fmaf(pv, vv[hv].x, o[i][4 * hv + 0]);
+                        o[i][4 * hv + 1] = fmaf(pv, vv[hv].y, o[i][4 * hv + 1]);
+                        o[i][4 * hv + 2] = fmaf(pv, vv[hv].z, o[i][4 * hv + 2]);
+                        o[i][4 * hv + 3] = fmaf(pv, vv[hv].w, o[i][4 * hv + 3]);
+                    }
+                }
+            }
+        }
+    }
+
+    // O / l; a row that saw no visible key (l == 0) is written as zeros.
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float lt = l[i];
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const int row = q0 + ty * 4 + i;
+        if (row < Lq) {
+            float *dst = Og + (size_t)row * D + tx * 4;
+#pragma unroll
+            for (int hv = 0; hv < C::OC / 4; ++hv)
+                *reinterpret_cast<float4 *>(dst + 64 * hv) =
+                    make_float4(o[i][4 * hv] * inv, o[i][4 * hv + 1] * inv,
+                                o[i][4 * hv + 2] * inv, o[i][4 * hv + 3] * inv);
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch(const float *q, const float *k, const float *v, const int32_t *kv,
+                   float *out, int B, int H, int Lq, int Lk, int mask_kind, float scale,
+                   cudaStream_t stream) {
+    constexpr size_t smem = F32Cfg<D>::kSmem;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(mha_fwd_f32_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const dim3 grid((Lq + kBM - 1) / kBM, H, B);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    mha_fwd_f32_kernel<D><<<grid, kThreads, smem, stream>>>(q, k, v, kv, out, H, Lq, Lk,
+                                                            mask_kind, scale_log2);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v,
+                           const int32_t *kv_lengths, float *out, int B, int H, int Lq,
+                           int Lk, int D, int mask_kind, float scale, cudaStream_t stream) {
+    if (D == 64) return launch<64>(q, k, v, kv_lengths, out, B, H, Lq, Lk, mask_kind, scale, stream);
+    return launch<128>(q, k, v, kv_lengths, out, B, H, Lq, Lk, mask_kind, scale, stream);
+}
+
+}  // namespace mha

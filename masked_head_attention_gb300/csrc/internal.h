@@ -1,0 +1,46 @@
+// internal.h -- host-side declarations shared by the C-ABI layer (api.cu) and
+// the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mha {
+
+// fp32 CUDA-core path (fwd_f32.cu).  Arguments already validated.
+cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v,
+                           const int32_t *kv_lengths, float *out, int B, int H, int Lq,
+                           int Lk, int D, int mask_kind, float scale, cudaStream_t stream);
+
+// bf16 tensor-core path (fwd_bf16.cu).  x/gamma/beta are null for plain
+// self-attention; for the Pre-LN variant q is null and x/gamma/beta are set.
+struct Bf16Call {
+    const void *q;          // [B,H,Lq,D] (self-attention) or null
+    const void *x;          // [B,Lq,H*D] (Pre-LN) or null
+    const float *gamma;
+    const float *beta;
+    float eps;
+    const void *k;          // [B,H,Lk,D]
+    const void *v;
+    const int32_t *kv_lengths;
+    void *out;              // [B,H,Lq,D] or [B,Lq,H*D]
+    int B, H, Lq, Lk, D;
+    int mask_kind;
+    float scale;
+};
+
+// Returns cudaSuccess or the first CUDA error; *driver_err receives a
+// nonzero CUresult when tensor-map encoding failed.
+cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_err);
+
+// Diagnostic single-tile tcgen05 GEMM (fwd_bf16.cu).
+cudaError_t launch_selftest_umma(int variant, int K_or_N, const void *a, const void *b,
+                                 float *c, cudaStream_t stream, int *driver_err);
+
+// Device status word of the bf16 translation unit.
+cudaError_t read_device_status(uint32_t *bits, bool clear);
+
+// Launch-configuration overrides used by the benchmark sweeps (0 = default).
+void set_bf16_grid_override(int ctas);
+
+}  // namespace mha

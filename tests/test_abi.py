@@ -1,0 +1,108 @@
+"""The C-ABI library loads and exports every symbol include/mha.h declares,
+and rejects bad arguments on the host, before any CUDA call (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from masked_head_attention_gb300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mha.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA, DEVICE = 0, -1, -2, -3, -4, -5
+
+
+@pytest.fixture(scope="module")
+def L():
+    path = mbuild.build()
+    lib = ctypes.CDLL(path)
+    P, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.mha_fwd.argtypes = [P, P, P, i, P, P, i, i, i, i, i, f, i, P]
+    lib.prenorm_cross_attn_fwd.argtypes = [P, P, P, f, P, P, P, P, i, i, i, i, i, f, i, P]
+    lib.mha_strerror.restype = ctypes.c_char_p
+    lib.mha_selftest_umma.argtypes = [i, i, P, P, P, P]
+    return lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^MHA_API\s+[\w\s\*]*?\**\s*(\w+)\s*\(", text, re.M)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("mha_fwd", "prenorm_cross_attn_fwd", "mha_strerror", "mha_device_status"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_strerror_covers_every_status(L):
+    for code in (OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA, DEVICE):
+        s = L.mha_strerror(code).decode()
+        assert s and s != "unknown status"
+    assert L.mha_strerror(12345).decode() == "unknown status"
+
+
+# Fake, never-dereferenced addresses: every case below is rejected (or is a
+# no-op) on the host before the library touches CUDA.
+A = ctypes.c_void_p(0x10000)
+A2 = ctypes.c_void_p(0x20000)
+A3 = ctypes.c_void_p(0x30000)
+OUT = ctypes.c_void_p(0x40000)
+BAD = ctypes.c_void_p(0x40008)
+
+
+def fwd(L, q=A, k=A2, v=A3, mask=0, lens=None, out=OUT, B=2, H=2, Lq=8, Lk=8, D=64,
+        scale=0.125, dtype=1):
+    return L.mha_fwd(q, k, v, mask, lens, out, B, H, Lq, Lk, D, scale, dtype, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), INVALID), (dict(out=None), INVALID), (dict(k=None), INVALID),
+    (dict(B=-1), INVALID), (dict(Lk=-3), INVALID), (dict(scale=0.0), INVALID),
+    (dict(scale=float("nan")), INVALID), (dict(scale=-1.0), INVALID),
+    (dict(mask=4), INVALID), (dict(mask=2, lens=None), INVALID),
+    (dict(D=32), UNSUPPORTED), (dict(D=96), UNSUPPORTED), (dict(dtype=7), UNSUPPORTED),
+    (dict(out=BAD), MISALIGNED), (dict(q=ctypes.c_void_p(0x10004)), MISALIGNED),
+    (dict(B=0), OK), (dict(H=0), OK), (dict(Lq=0), OK),
+    (dict(B=70000), INVALID),
+])
+def test_mha_fwd_host_validation(L, kw, want):
+    assert fwd(L, **kw) == want
+
+
+def pre(L, x=A, g=A2, b=A3, eps=1e-5, k=A, v=A2, lens=None, out=OUT, B=2, H=2, Lq=8, Lk=8,
+        D=64, scale=0.125, dtype=1):
+    return L.prenorm_cross_attn_fwd(x, g, b, eps, k, v, lens, out, B, H, Lq, Lk, D, scale,
+                                    dtype, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(x=None), INVALID), (dict(g=None), INVALID), (dict(b=None), INVALID),
+    (dict(eps=-1.0), INVALID), (dict(eps=float("inf")), INVALID),
+    (dict(dtype=0), UNSUPPORTED), (dict(D=80), UNSUPPORTED),
+    (dict(g=ctypes.c_void_p(0x20004)), MISALIGNED), (dict(Lq=0), OK), (dict(B=0), OK),
+])
+def test_prenorm_host_validation(L, kw, want):
+    assert pre(L, **kw) == want
+
+
+def test_selftest_host_validation(L):
+    assert L.mha_selftest_umma(3, 64, A, A2, OUT, None) == INVALID
+    assert L.mha_selftest_umma(0, 96, A, A2, OUT, None) == UNSUPPORTED
+    assert L.mha_selftest_umma(0, 64, None, A2, OUT, None) == INVALID
+    assert L.mha_selftest_umma(0, 64, A, A2, BAD, None) == MISALIGNED
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import masked_head_attention_gb300 as mha
+    monkeypatch.setattr(mha, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(mha, "_lib", None)
+    with pytest.raises(mha.MhaError):
+        mha.lib()

@@ -1,0 +1,122 @@
+"""bf16 tensor-core path (TMA + tcgen05 + TMEM) against the fp64 oracle (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import masked_head_attention_gb300 as mha
+import oracle
+from masked_head_attention_gb300 import synthetic
+from parity_util import as_np, check_bf16, dev, lens_tensor, randn, sample_rows
+
+CASES = [
+    (1, 1, 1, 1, 64, 0, None),
+    (1, 1, 1, 1, 128, 1, None),
+    (2, 3, 7, 7, 64, 1, None),
+    (1, 2, 128, 128, 128, 1, None),
+    (2, 2, 129, 129, 64, 1, None),
+    (1, 2, 300, 300, 128, 1, None),
+    (2, 2, 65, 300, 64, 0, None),
+    (2, 2, 200, 77, 128, 1, None),
+    (2, 1, 77, 200, 64, 1, None),
+    (4, 2, 260, 260, 64, 2, [0, 1, 260, 130]),
+    (3, 2, 257, 257, 128, 2, [400, -3, 128]),
+    (4, 2, 390, 390, 128, 3, [1, 127, 128, 390]),
+    (2, 4, 512, 512, 64, 3, [300, 512]),
+]
+
+
+def _run(B, H, Lq, Lk, D, mask, lens, std=1.0, seed=0):
+    q = randn((B, H, Lq, D), seed, std, torch.bfloat16)
+    k = randn((B, H, Lk, D), seed + 1, std, torch.bfloat16)
+    v = randn((B, H, Lk, D), seed + 2, 1.0, torch.bfloat16)
+    out = mha.mha_fwd(dev(q), dev(k), dev(v), mask, dev(lens_tensor(lens)))
+    torch.cuda.synchronize()
+    want = oracle.mha_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), mask, lens)
+    return as_np(out), want
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dLq%dLk%dD%dm%d" % c[:6])
+def test_bf16_small(case):
+    got, want = _run(*case)
+    check_bf16(got, want, str(case))
+    assert mha.device_status() == 0
+
+
+@pytest.mark.gpu
+def test_bf16_peaky_logits_stress_max_shift():
+    # Logit std 2.5 (span about [-10, 10]) as in the long causal workload.
+    got, want = _run(1, 4, 600, 600, 128, 1, None, std=2.5 ** 0.5, seed=3)
+    check_bf16(got, want, "peaky")
+
+
+@pytest.mark.gpu
+def test_bf16_large_logits_finite():
+    # Logits around +-100: exp would overflow fp32 without the max shift.
+    got, want = _run(1, 2, 256, 256, 64, 1, None, std=4.0, seed=4)
+    assert np.all(np.isfinite(got))
+    check_bf16(got, want, "large logits")
+
+
+@pytest.mark.gpu
+def test_bf16_c3_full_workload():
+    w = synthetic.WORKLOADS["c3_causal_bf16"]
+    x = synthetic.make(w, seed=0)
+    out = mha.mha_fwd(dev(x["q"]), dev(x["k"]), dev(x["v"]), w.mask, None, scale=w.scale)
+    torch.cuda.synchronize()
+    want = oracle.mha_fwd(x["q"].float().numpy(), x["k"].float().numpy(), x["v"].float().numpy(),
+                          w.mask, None, w.scale)
+    r = check_bf16(as_np(out), want, w.name)
+    print(w.name, r)
+
+
+@pytest.mark.gpu
+def test_bf16_c5_sampled_rows():
+    w = synthetic.WORKLOADS["c5_long_causal_bf16"]
+    x = synthetic.make(w, seed=0)
+    out = mha.mha_fwd(dev(x["q"]), dev(x["k"]), dev(x["v"]), w.mask, None, scale=w.scale)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.B, w.H, w.Lq, 160, seed=5)
+    want = oracle.mha_rows(x["q"].float().numpy(), x["k"].float().numpy(),
+                           x["v"].float().numpy(), rows, w.mask, None, w.scale)
+    o = out.float().cpu()
+    got = np.stack([o[b, h, i].numpy() for b, h, i in rows]).astype(np.float64)
+    r = check_bf16(got, want, w.name)
+    print(w.name, r)
+
+
+@pytest.mark.gpu
+def test_bf16_masked_keys_contribute_exactly_zero():
+    B, H, L, D = 2, 2, 300, 128
+    q = randn((B, H, L, D), 5, dtype=torch.bfloat16)
+    k = randn((B, H, L, D), 6, dtype=torch.bfloat16)
+    v = randn((B, H, L, D), 7, dtype=torch.bfloat16)
+    lens = torch.tensor([140, 300], dtype=torch.int32)
+    a = mha.mha_fwd(dev(q), dev(k), dev(v), 3, dev(lens)).cpu()
+    k2, v2 = k.clone(), v.clone()
+    k2[0, :, 140:] = randn((H, L - 140, D), 8, 30.0, torch.bfloat16)
+    v2[0, :, 140:] = randn((H, L - 140, D), 9, 30.0, torch.bfloat16)
+    k2[1, :, 11] += 5.0
+    b = mha.mha_fwd(dev(q), dev(k2), dev(v2), 3, dev(lens)).cpu()
+    assert torch.equal(a[0], b[0])
+    assert torch.equal(a[1, :, :11], b[1, :, :11])
+
+
+@pytest.mark.gpu
+def test_bf16_zero_keys_and_persistent_grid():
+    q = randn((2, 2, 9, 64), 1, dtype=torch.bfloat16).cuda()
+    kv = torch.empty((2, 2, 0, 64), device="cuda", dtype=torch.bfloat16)
+    out = mha.mha_fwd(q, kv, kv, 0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out.float()).item() == 0
+    # The same problem on a capped (persistent) grid matches the default grid.
+    x = [randn((2, 3, 700, 128), s, dtype=torch.bfloat16).cuda() for s in (11, 12, 13)]
+    a = mha.mha_fwd(*x, 1)
+    try:
+        mha.set_bf16_grid(5)
+        b = mha.mha_fwd(*x, 1)
+    finally:
+        mha.set_bf16_grid(0)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert mha.device_status() == 0

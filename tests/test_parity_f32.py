@@ -1,0 +1,83 @@
+"""fp32 CUDA-core path against the fp64 oracle, element by element (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import masked_head_attention_gb300 as mha
+import oracle
+from masked_head_attention_gb300 import synthetic
+from parity_util import as_np, check_f32, dev, lens_tensor, randn
+
+# (B, H, Lq, Lk, D, mask, lengths): several tiles, ragged tails, Lq != Lk,
+# lengths at 0, 1, the end, beyond the end (clamped) and negative (clamped).
+CASES = [
+    (1, 1, 1, 1, 64, 0, None),
+    (1, 1, 1, 1, 64, 1, None),
+    (2, 3, 7, 7, 64, 1, None),
+    (2, 2, 130, 130, 64, 1, None),
+    (1, 2, 200, 200, 128, 1, None),
+    (2, 2, 65, 200, 64, 0, None),
+    (3, 2, 100, 37, 64, 1, None),
+    (2, 2, 37, 100, 128, 1, None),
+    (4, 2, 150, 150, 64, 2, [0, 1, 150, 77]),
+    (3, 1, 129, 129, 128, 2, [200, -5, 64]),
+    (4, 2, 190, 190, 64, 3, [1, 63, 64, 190]),
+    (2, 2, 256, 256, 128, 3, [129, 256]),
+]
+
+
+def _run(B, H, Lq, Lk, D, mask, lens, seed=0):
+    q = randn((B, H, Lq, D), seed)
+    k = randn((B, H, Lk, D), seed + 1)
+    v = randn((B, H, Lk, D), seed + 2)
+    lt = lens_tensor(lens)
+    out = mha.mha_fwd(dev(q), dev(k), dev(v), mask, dev(lt))
+    torch.cuda.synchronize()
+    want = oracle.mha_fwd(q.numpy(), k.numpy(), v.numpy(), mask, lens)
+    return as_np(out), want
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dLq%dLk%dD%dm%d" % c[:6])
+def test_f32_small(case):
+    got, want = _run(*case)
+    check_f32(got, want, str(case))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["c1_causal_f32", "c2_padding_f32"])
+def test_f32_full_workload(name):
+    w = synthetic.WORKLOADS[name]
+    x = synthetic.make(w, seed=0)
+    out = mha.mha_fwd(dev(x["q"]), dev(x["k"]), dev(x["v"]), w.mask, dev(x["kv_lengths"]),
+                      scale=w.scale)
+    torch.cuda.synchronize()
+    lens = None if x["kv_lengths"] is None else x["kv_lengths"].numpy()
+    want = oracle.mha_fwd(x["q"].numpy(), x["k"].numpy(), x["v"].numpy(), w.mask, lens, w.scale)
+    check_f32(as_np(out), want, name)
+
+
+@pytest.mark.gpu
+def test_f32_masked_keys_contribute_exactly_zero():
+    B, H, L, D = 2, 2, 160, 64
+    q, k, v = randn((B, H, L, D), 5), randn((B, H, L, D), 6), randn((B, H, L, D), 7)
+    lens = torch.tensor([70, 160], dtype=torch.int32)
+    a = mha.mha_fwd(dev(q), dev(k), dev(v), 3, dev(lens)).cpu()
+    k2, v2 = k.clone(), v.clone()
+    k2[0, :, 70:] = randn((H, L - 70, D), 8, std=30.0)
+    v2[0, :, 70:] = randn((H, L - 70, D), 9, std=30.0)
+    for i in (10, 100):        # causal: keys after row i never matter for row i
+        k2[1, :, i + 1:i + 2] += 5.0
+    b = mha.mha_fwd(dev(q), dev(k2), dev(v2), 3, dev(lens)).cpu()
+    assert torch.equal(a[0], b[0])
+    assert torch.equal(a[1, :, :11], b[1, :, :11])
+    assert not torch.equal(a[1, :, 11:101], b[1, :, 11:101])
+
+
+@pytest.mark.gpu
+def test_f32_zero_keys_gives_zeros():
+    q = randn((2, 2, 9, 64), 1).cuda()
+    kv = torch.empty((2, 2, 0, 64), device="cuda")
+    out = mha.mha_fwd(q, kv, kv, 0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0
