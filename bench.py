@@ -1,0 +1,499 @@
+#!/usr/bin/env python
+"""Benchmark of the fused masked multi-head attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-extra] [--no-cpu-baseline]
+
+A step is one call of the hot path (one kernel launch) on one batch of
+synthetic inputs already resident in HBM.  Input sets rotate so the data read
+per step is not served from L2 (their total exceeds twice the L2 size).  The
+metric is mask-aware attention TFLOP/s (4*B*H*Lq*Lk*D, halved for causal; for
+the padding mask the valid keys 4*H*D*Lq*sum_b len_b), with us per call and
+the fraction of the roofline of the dominant kernel.
+
+Rank 0 prints one JSON line.  Under torchrun each rank runs its own replica
+of the workload (weak scaling, no collective on the data path); the time is
+the max over ranks.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from masked_head_attention_gb300 import synthetic  # noqa: E402
+
+METRIC = "mask-aware attention TFLOP/s and µs/call at 1 GB300; % of roofline"
+DEFAULT_WORKLOAD = "c2_padding_f32"
+DEFAULT_L2 = 129 * 1024 * 1024
+KERNEL_OF = {  # dominant (only) kernel of each workload
+    "mha:f32": "mha_fwd_f32_kernel",
+    "mha:bf16": "attn_fwd_bf16_kernel",
+    "prenorm:bf16": "attn_fwd_bf16_kernel<prenorm>",
+}
+
+
+# ------------------------------------------------------------------ helpers --
+def visible_lengths(w, lens):
+    if lens is None:
+        return [w.Lk] * w.B
+    return [max(0, min(int(x), w.Lk)) for x in lens]
+
+
+def mask_aware_flops(w, lens):
+    """4*B*H*Lq*Lk*D halved for causal; for kv lengths 4*H*D*Lq*sum(len)."""
+    if w.mask & synthetic.MASK_KV_LEN:
+        f = 4.0 * w.H * w.D * w.Lq * sum(visible_lengths(w, lens))
+        return f / 2 if w.mask & synthetic.MASK_CAUSAL else f
+    f = 4.0 * w.B * w.H * w.Lq * w.Lk * w.D
+    return f / 2 if w.mask & synthetic.MASK_CAUSAL else f
+
+
+def nominal_flops(w):
+    return 4.0 * w.B * w.H * w.Lq * w.Lk * w.D
+
+
+def algorithmic_bytes(w, lens):
+    """Bytes a perfect kernel moves: Q (or x) and O once, K/V of visible keys once."""
+    e = 4 if w.dtype == "f32" else 2
+    kv_rows = sum(visible_lengths(w, lens)) * w.H
+    qo = 2 * w.B * w.H * w.Lq * w.D * e
+    extra = 2 * 4 * w.H * w.D if w.kind == "prenorm" else 0   # gamma, beta
+    return qo + 2 * kv_rows * w.D * e + extra
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["_source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "_source": "fallback"}
+
+
+def fp32_alu_peak_tflops(n_sm, mhz):
+    """FFMA ceiling: SMs x 128 fp32 lanes x 2 FLOP x clock."""
+    return n_sm * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def traffic_record(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path)).get(kernel_key)
+        if not rec:
+            return None
+        src = os.path.join(ROOT, rec["source"])
+        import hashlib
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return rec if h == rec["source_sha256_16"] else None
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the GPU is busy."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [r for r in rows if r["sm"] > 0.5 * r["smax"]] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(busy)}
+
+
+# ------------------------------------------------------------- GPU workload --
+class GpuWorkload:
+    """Device-resident rotating input sets and the launch of one step."""
+
+    def __init__(self, w, seed, device, l2_bytes, max_bytes=6 << 30):
+        import masked_head_attention_gb300 as mha
+        self.mha = mha
+        self.w = w
+        self.host = synthetic.make(w, seed)
+        self.lens = None if self.host["kv_lengths"] is None else self.host["kv_lengths"].tolist()
+        self.device = device
+        keys = ["q", "k", "v"] if w.kind == "mha" else ["x", "gamma", "beta", "k", "v"]
+        self.in_keys = keys
+        set_bytes = sum(self.host[k].numel() * self.host[k].element_size() for k in keys)
+        out_like = self.host["q"] if w.kind == "mha" else self.host["x"]
+        set_bytes += out_like.numel() * out_like.element_size()
+        self.set_bytes = set_bytes
+        n = max(1, math.ceil(2 * l2_bytes / set_bytes))
+        n = max(1, min(n, max_bytes // set_bytes))
+        self.sets = []
+        for _ in range(n):
+            s = {k: self.host[k].to(device) for k in keys}
+            s["out"] = torch.empty_like(out_like, device=device)
+            self.sets.append(s)
+        self.kv = None if self.host["kv_lengths"] is None else self.host["kv_lengths"].to(device)
+        self.i = 0
+
+    def step(self, s=None):
+        w = self.w
+        if s is None:
+            s = self.sets[self.i % len(self.sets)]
+            self.i += 1
+        if w.kind == "mha":
+            self.mha.mha_fwd(s["q"], s["k"], s["v"], w.mask, self.kv, out=s["out"], scale=w.scale)
+        else:
+            self.mha.prenorm_cross_attn_fwd(s["x"], s["gamma"], s["beta"], w.eps, s["k"], s["v"],
+                                            self.kv, out=s["out"], scale=w.scale)
+
+    def input_bytes(self):
+        b = sum(self.host[k].numel() * self.host[k].element_size() for k in self.in_keys)
+        if self.host["kv_lengths"] is not None:
+            b += self.host["kv_lengths"].numel() * 4
+        return b
+
+    def output_bytes(self):
+        o = self.sets[0]["out"]
+        return o.numel() * o.element_size()
+
+
+def time_steps(wl, steps, warmup, sync_ranks=None):
+    """Warm up, then time exactly `steps` back-to-back steps with CUDA events on
+    the launching stream; also per-launch event pairs for the kernel time."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    if sync_ranks:
+        sync_ranks()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        wl.step()
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if sync_ranks:
+        sync_ranks()
+    total_ms = t0.elapsed_time(t1)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    return total_ms, per_launch
+
+
+def time_e2e(wl, steps, warmup):
+    """Same metric through the public API with pinned host buffers: each step
+    copies its inputs host->device, runs the call and reads the output back."""
+    w = wl.w
+    host = {k: wl.host[k].pin_memory() for k in wl.in_keys}
+    kv_host = None if wl.host["kv_lengths"] is None else wl.host["kv_lengths"].pin_memory()
+    s = wl.sets[0]
+    out_host = torch.empty(s["out"].shape, dtype=s["out"].dtype).pin_memory()
+
+    def one():
+        for k in wl.in_keys:
+            s[k].copy_(host[k], non_blocking=True)
+        if kv_host is not None:
+            wl.kv.copy_(kv_host, non_blocking=True)
+        wl.step(s)
+        out_host.copy_(s["out"], non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def roofline_for(w, lens, kernel_ms, peaks, n_sm):
+    flops = mask_aware_flops(w, lens)
+    kkey = KERNEL_OF["%s:%s" % (w.kind, w.dtype)]
+    if w.dtype == "f32":
+        peak = fp32_alu_peak_tflops(n_sm, peaks.get("sm_max_mhz", 2070.0))
+        bound = "alu"
+    else:
+        peak = peaks["bf16_tflops"]
+        bound = "tensor"
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    rec = traffic_record("%s/%s" % (kkey, w.name))
+    return {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "traffic": None if rec is None else rec["dram_bytes_per_launch"],
+            "algorithmic_bytes": int(algorithmic_bytes(w, lens)),
+            "kernel": kkey, "peak_source": peaks["_source"] +
+            (" (SMs x 128 lanes x 2 x max SM clock)" if w.dtype == "f32" else " bf16 burst")}
+
+
+# --------------------------------------------------------------- CPU oracle --
+def oracle_sample(w, host, budget_s, max_problems=None):
+    """Time the fp64 oracle on whole (b, h) problems of the workload until the
+    budget is spent; returns (mask-aware TFLOP/s, seconds, problems, threads)."""
+    import oracle
+    lens = None if host["kv_lengths"] is None else host["kv_lengths"].numpy()
+    if w.kind == "mha":
+        q, k, v = (host[n].float().numpy() for n in ("q", "k", "v"))
+    else:
+        x = host["x"].float().numpy()
+        k, v = host["k"].float().numpy(), host["v"].float().numpy()
+    order = [(b, h) for h in range(w.H) for b in range(w.B)]
+    done, flops, t_total = 0, 0.0, 0.0
+    for b, h in order:
+        if max_problems is not None and done >= max_problems:
+            break
+        lb = None if lens is None else lens[b:b + 1]
+        t0 = time.perf_counter()
+        if w.kind == "mha":
+            oracle.mha_fwd(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1],
+                           w.mask, lb, w.scale)
+        else:
+            rows = np.array([(0, h, i) for i in range(w.Lq)], np.int64)
+            oracle.prenorm_rows(x[b:b + 1], host["gamma"].numpy(), host["beta"].numpy(), w.eps,
+                                k[b:b + 1], v[b:b + 1], rows, lb, w.scale)
+        t_total += time.perf_counter() - t0
+        sub = synthetic.Workload(w.name, w.kind, w.dtype, 1, 1, w.Lq, w.Lk, w.D, w.mask)
+        flops += mask_aware_flops(sub, None if lb is None else lb.tolist())
+        done += 1
+        if t_total >= budget_s:
+            break
+    return flops / t_total / 1e12, t_total, done, oracle.num_threads()
+
+
+# -------------------------------------------------------------------- main --
+def combine_ranks(total_ms, flops_per_step, steps, world, reduce_max=None):
+    """Whole-job throughput of `world` replicas: every rank ran `steps` steps of
+    `flops_per_step`; the job time is the slowest rank's.  `reduce_max` turns a
+    local float into the max over ranks (identity for one rank).
+    Returns (ms_per_step, TFLOP/s)."""
+    t = reduce_max(total_ms) if reduce_max is not None else total_ms
+    ms = t / steps
+    return ms, world * flops_per_step / (ms * 1e-3) / 1e12
+
+
+def torch_reduce_max(device):
+    import torch.distributed as dist
+
+    def f(x):
+        t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return f
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = synthetic.WORKLOADS[args.workload]
+    host = synthetic.make(w, seed=0)
+    per_step = max(1, (w.B * w.H) // 8)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        tf, secs, n, thr = oracle_sample(w, host, budget_s=1e9, max_problems=per_step)
+        if i >= args.warmup:
+            vals.append((tf, secs, n, thr))
+    tf = statistics.median(v[0] for v in vals)
+    secs = statistics.median(v[1] for v in vals)
+    line = {"metric": METRIC, "impl": "reference", "value": round(tf, 6), "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "D": w.D,
+                       "note": w.note},
+            "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": vals[0][3],
+                             "kind": "oracle",
+                             "sample": "%d of %d (b,h) problems per step, all rows" % (
+                                 per_step, w.B * w.H)},
+            "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def measure_config(w, args, device, peaks, n_sm, l2):
+    wl = GpuWorkload(w, 0, device, l2)
+    probe_ms, _ = time_steps(wl, 3, 2)
+    steps = max(5, min(2000, int(300.0 / max(probe_ms / 3, 1e-3))))
+    total_ms, per_launch = time_steps(wl, steps, max(3, args.warmup))
+    call_ms = total_ms / steps
+    flops = mask_aware_flops(w, wl.lens)
+    r = roofline_for(w, wl.lens, statistics.mean(per_launch), peaks, n_sm)
+    out = {"us_per_call": round(call_ms * 1e3, 3), "tflops": round(flops / call_ms / 1e9, 3),
+           "nominal_tflops": round(nominal_flops(w) / call_ms / 1e9, 3), "steps": steps,
+           "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "frac", "traffic")},
+           "hbm_gbs": round(algorithmic_bytes(w, wl.lens) / call_ms / 1e6, 1),
+           "input_sets": len(wl.sets)}
+    del wl
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--no-extra", action="store_true", help="skip the other four workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--settle-s", type=float, default=1.0,
+                    help="untimed back-to-back steps before the timed region (clock settling)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import masked_head_attention_gb300 as mha
+    mha.lib()   # fails loudly when the extension is missing
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    props = torch.cuda.get_device_properties(device)
+    n_sm = props.multi_processor_count
+    l2 = getattr(props, "L2_cache_size", 0) or DEFAULT_L2
+    peaks = load_peaks()
+    w = synthetic.WORKLOADS[args.workload]
+
+    sync = None
+    if world > 1:
+        import torch.distributed as dist
+        sync = dist.barrier
+
+    wl = GpuWorkload(w, seed=rank, device=device, l2_bytes=l2)
+    # Settle clocks under this load, then the timed region, with clock samples.
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        t_end = time.time() + args.settle_s
+        while time.time() < t_end:
+            for _ in range(20):
+                wl.step()
+            torch.cuda.synchronize()
+        total_ms, per_launch = time_steps(wl, args.steps, args.warmup, sync)
+    flops = mask_aware_flops(w, wl.lens)
+    ms_per_step, value = combine_ranks(total_ms, flops, args.steps, world,
+                                       torch_reduce_max(device) if world > 1 else None)
+    kernel_ms = statistics.mean(per_launch)
+    roof = roofline_for(w, wl.lens, kernel_ms, peaks, n_sm)
+
+    e2e_ms = time_e2e(wl, max(3, min(args.steps, 50)), 3)
+    e2e = {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(wl.input_bytes()),
+           "d2h_bytes_per_step": int(wl.output_bytes()), "ms_per_step": round(e2e_ms, 4)}
+    status = mha.device_status()
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+                "us_per_call": round(ms_per_step * 1e3, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32" if w.dtype == "f32" else "bf16 (fp32 accumulate)",
+                "data": "synthetic",
+                "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk,
+                           "D": w.D, "mask": w.mask, "note": w.note,
+                           "nominal_tflops": round(world * nominal_flops(w) / ms_per_step / 1e9, 3),
+                           "l2_policy": "%d rotating input sets of %.1f MB (> 2x L2 %.0f MB)" % (
+                               len(wl.sets), wl.set_bytes / 1e6, l2 / 1e6),
+                           "parallelism": "replicas x%d (weak scaling, no collective)" % world},
+                "roofline": roof, "e2e": e2e, "gpu_launches": args.steps,
+                "clocks": clk.summary(), "device_status": status}
+        del wl
+        torch.cuda.empty_cache()
+        if not args.no_cpu_baseline and world == 1:
+            host = synthetic.make(w, seed=0)
+            tf, secs, n, thr = oracle_sample(w, host, args.cpu_budget)
+            line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": thr,
+                                    "kind": "oracle",
+                                    "sample": "%d of %d (b,h) problems, all rows, %.1f s" % (
+                                        n, w.B * w.H, secs)}
+        if not args.no_extra and world == 1:
+            extra = {}
+            for name, ow in synthetic.WORKLOADS.items():
+                if name == w.name:
+                    continue
+                extra[name] = measure_config(ow, args, device, peaks, n_sm, l2)
+            line["other_workloads"] = extra
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
