@@ -289,36 +289,49 @@ def roofline_for(w, lens, kernel_ms, peaks, n_sm):
 
 # --------------------------------------------------------------- CPU oracle --
 def oracle_sample(w, host, budget_s, max_problems=None):
-    """Time the fp64 oracle on whole (b, h) problems of the workload until the
-    budget is spent; returns (mask-aware TFLOP/s, seconds, problems, threads)."""
+    """Time the fp64 oracle on whole (b, h) problems of the workload, a chunk of
+    problems per call so its OpenMP loop over problems uses every thread, until
+    the budget is spent.  Returns (mask-aware TFLOP/s, seconds, problems,
+    threads)."""
     import oracle
+    threads = oracle.num_threads()
     lens = None if host["kv_lengths"] is None else host["kv_lengths"].numpy()
+    BH = w.B * w.H
+    # (b, h) problems as a flat batch of single-head problems.
+    plens = None if lens is None else np.repeat(lens, w.H).astype(np.int32)
     if w.kind == "mha":
-        q, k, v = (host[n].float().numpy() for n in ("q", "k", "v"))
+        q = host["q"].float().numpy().reshape(BH, 1, w.Lq, w.D)
+        k = host["k"].float().numpy().reshape(BH, 1, w.Lk, w.D)
+        v = host["v"].float().numpy().reshape(BH, 1, w.Lk, w.D)
     else:
         x = host["x"].float().numpy()
         k, v = host["k"].float().numpy(), host["v"].float().numpy()
-    order = [(b, h) for h in range(w.H) for b in range(w.B)]
+    chunk = max(1, threads)
+    if max_problems is not None:
+        chunk = min(chunk, max_problems)
     done, flops, t_total = 0, 0.0, 0.0
-    for b, h in order:
+    for p0 in range(0, BH, chunk):
         if max_problems is not None and done >= max_problems:
             break
-        lb = None if lens is None else lens[b:b + 1]
+        p1 = min(BH, p0 + chunk)
+        if max_problems is not None:
+            p1 = min(p1, p0 + max_problems - done)
+        lb = None if plens is None else plens[p0:p1]
         t0 = time.perf_counter()
         if w.kind == "mha":
-            oracle.mha_fwd(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1],
-                           w.mask, lb, w.scale)
+            oracle.mha_fwd(q[p0:p1], k[p0:p1], v[p0:p1], w.mask, lb, w.scale)
         else:
-            rows = np.array([(0, h, i) for i in range(w.Lq)], np.int64)
-            oracle.prenorm_rows(x[b:b + 1], host["gamma"].numpy(), host["beta"].numpy(), w.eps,
-                                k[b:b + 1], v[b:b + 1], rows, lb, w.scale)
+            rows = np.array([(pp // w.H, pp % w.H, i) for pp in range(p0, p1)
+                             for i in range(w.Lq)], np.int64)
+            oracle.prenorm_rows(x, host["gamma"].numpy(), host["beta"].numpy(), w.eps, k, v,
+                                rows, lens, w.scale)
         t_total += time.perf_counter() - t0
-        sub = synthetic.Workload(w.name, w.kind, w.dtype, 1, 1, w.Lq, w.Lk, w.D, w.mask)
+        sub = synthetic.Workload(w.name, w.kind, w.dtype, p1 - p0, 1, w.Lq, w.Lk, w.D, w.mask)
         flops += mask_aware_flops(sub, None if lb is None else lb.tolist())
-        done += 1
+        done += p1 - p0
         if t_total >= budget_s:
             break
-    return flops / t_total / 1e12, t_total, done, oracle.num_threads()
+    return flops / t_total / 1e12, t_total, done, threads
 
 
 # -------------------------------------------------------------------- main --
@@ -384,8 +397,11 @@ def run_reference(args, world, rank):
 
 def measure_config(w, args, device, peaks, n_sm, l2):
     wl = GpuWorkload(w, 0, device, l2)
-    probe_ms, _ = time_steps(wl, 3, 2)
-    steps = max(5, min(2000, int(300.0 / max(probe_ms / 3, 1e-3))))
+    if args.extra_steps > 0:
+        steps = args.extra_steps
+    else:
+        probe_ms, _ = time_steps(wl, 3, 2)
+        steps = max(5, min(2000, int(300.0 / max(probe_ms / 3, 1e-3))))
     total_ms, per_launch = time_steps(wl, steps, max(3, args.warmup))
     call_ms = total_ms / steps
     flops = mask_aware_flops(w, wl.lens)
@@ -410,6 +426,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other four workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--extra-steps", type=int, default=0,
+                    help="fixed timed steps for the other workloads (0 = about 0.3 s each)")
     ap.add_argument("--settle-s", type=float, default=1.0,
                     help="untimed back-to-back steps before the timed region (clock settling)")
     args = ap.parse_args()
