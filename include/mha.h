@@ -21,8 +21,10 @@
  *    shift) and 5.2 (divide the logits by sqrt(d_k)).
  *
  * Conventions for every entry point.
- *  - Pointers are DEVICE pointers owned by the caller; the library allocates
- *    no device memory and keeps no per-call state.
+ *  - Pointers are DEVICE pointers owned by the caller; the library keeps no
+ *    per-call state.  mha_fwd allocates no device memory;
+ *    prenorm_cross_attn_fwd takes a stream-ordered workspace of 8*B*Lq bytes
+ *    (cudaMallocAsync / cudaFreeAsync on `stream`) for the row statistics.
  *  - Layouts are dense and row-major: q, out [B,H,Lq,D]; k, v [B,H,Lk,D];
  *    kv_lengths int32 [B].  Every tensor pointer must be 16-byte aligned.
  *  - Work is enqueued on `stream` (0 = legacy default stream); no entry
@@ -94,7 +96,10 @@ MHA_API int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
  *     xhat = (x_q[b,i,:] - mean) / sqrt(var + eps) * gamma + beta
  * over the H*D features of the row (biased variance), Q[b,h,i,:] is the
  * head-h slice xhat[h*D:(h+1)*D], and the attention above runs with the
- * padding mask only (kv_lengths, or none when it is NULL).
+ * padding mask only (kv_lengths, or none when it is NULL).  Two kernels run
+ * on `stream`: one pass computes each row's mean and 1/sqrt(var + eps) into
+ * the workspace; the attention kernel loads each head's slice of x with TMA
+ * and normalises it in shared memory before the first QK^T product.
  *   x_q         [B,Lq,H*D] bf16 (query-side activations)
  *   gamma, beta fp32 [H*D]
  *   eps         finite, >= 0

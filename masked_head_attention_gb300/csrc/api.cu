@@ -63,7 +63,7 @@ int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
     c.mask_kind = mask_kind;
     c.scale = scale;
     int drv = 0;
-    cudaError_t e = mha::launch_fwd_bf16(c, stream, &drv);
+    cudaError_t e = mha::launch_fwd_bf16(c, stream, &drv, nullptr);
     if (drv != 0) return MHA_ERR_CUDA;
     return from_cuda(e);
 }
@@ -99,9 +99,16 @@ int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const float *bet
     c.D = D;
     c.mask_kind = kv_lengths ? MHA_MASK_KV_LEN : MHA_MASK_NONE;
     c.scale = scale;
+    // Row statistics of x live in a stream-ordered workspace for this call.
+    float2 *stats = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&stats), sizeof(float2) * (size_t)B * Lq,
+                        stream) != cudaSuccess)
+        return MHA_ERR_CUDA;
     int drv = 0;
-    cudaError_t e = mha::launch_fwd_bf16(c, stream, &drv);
+    cudaError_t e = mha::launch_fwd_bf16(c, stream, &drv, stats);
+    const cudaError_t ef = cudaFreeAsync(stats, stream);
     if (drv != 0) return MHA_ERR_CUDA;
+    if (e == cudaSuccess) e = ef;
     return from_cuda(e);
 }
 

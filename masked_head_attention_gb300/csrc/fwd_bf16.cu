@@ -2,23 +2,33 @@
 // the sm_103a tensor cores (tcgen05 MMAs accumulating in TMEM, operands
 // staged by TMA), and the Pre-LayerNorm cross-attention variant.
 //
-// Work item = one 128-row query tile of one (b, h).  CTA = 6 warps:
-//   warps 0-3  softmax warpgroup: thread t owns query row t of the tile (TMEM
-//              lane t).  Reads a 128 x 128 fp32 logit tile S from TMEM, masks
-//              it from (row, col, length), runs the online softmax (running
-//              max and rescaled running sum in registers), writes P as bf16
-//              back into TMEM and rescales the O accumulator when the max
-//              grows; finally divides O by the row sum and stores it through
-//              shared memory with TMA.  In the Pre-LN variant it also
-//              normalises the query rows and writes the Q tile to shared memory.
-//   warp 4     TMA producer: Q tile once per item, then K and V tiles of 128
-//              keys into a two-stage ring; key tiles past the causal limit or
-//              the valid length are never loaded.
-//   warp 5     MMA issuer: S_j = Q K_j^T (shared x shared -> TMEM) and
-//              O += P_j V_j (P read from TMEM, V from shared memory).  Owns the
-//              TMEM allocation.
-// S is double-buffered in TMEM so S_{j+1} runs on the tensor cores while the
-// softmax works on S_j.  All hand-offs are mbarriers; every wait is bounded.
+// Work item = two 128-row query tiles (256 rows) of one (b, h).  CTA = 12 warps:
+//   warps 0-3 / 4-7  softmax warpgroups WG0 / WG1, one per query tile: thread
+//              t owns query row t of its tile (TMEM lane t).  It loads its S
+//              row (128 keys, fp32) from TMEM, masks it from (row, col,
+//              length), runs the online softmax (running max and rescaled
+//              running sum in registers), writes P as bf16 into TMEM (over
+//              the first 64 columns of its S buffer when D = 128, in columns
+//              of its own when D = 64), and rescales its O row in TMEM
+//              when the max grows.  At the end it divides O by the row sum and
+//              stores the tile through shared memory with TMA.  In the Pre-LN
+//              variant it first normalises its rows of the Q tile in place.
+//   warp 8     TMA producer: both Q tiles per item (the head's slice of x for
+//              Pre-LN), K and V tiles of 128 keys through a ring of stages;
+//              key tiles past the causal limit or the valid length are never
+//              loaded.  The first K/V tiles of an item are issued before its
+//              Q tiles, overlapping the previous item's epilogue.
+//   warp 9     MMA issuer (one thread) and TMEM owner (S0, S1, O0, O1 = 512
+//              columns).  Issue order per key tile j:
+//                  PV0(j), S0(j+1), PV1(j), S1(j+1)
+//              so while one warpgroup runs its softmax the tensor cores work
+//              on the other query tile.
+//   warps 10-11 idle.  Warpgroup 2 (warps 8-11) hands registers to the two
+//              softmax warpgroups: 384 threads launch with 168 registers each
+//              (64512); after the split 2 x 128 x 200 + 128 x 104 = 64512,
+//              i.e. 504 per lane on each SM sub-partition (limit 512).
+// All hand-offs are mbarriers (TMA transaction counts, tcgen05.commit, thread
+// arrivals); every wait is bounded.
 //
 // Page sections this follows: "Why attention must compute the max first"
 // (gsyq.cn) 2.3-2.4 and 3.1 (online softmax with the max shift, fused between
@@ -26,7 +36,7 @@
 // article (2kiu.com) 2 and 3.1 (skip fully masked tiles, mask in-kernel as
 // -infinity before the softmax); "How to fuse cross-attention and
 // layer-norm into a single CUDA kernel?" (cms365.cn) answer steps one to
-// four (Pre-LN fused into the Q load, cross-attention with online softmax,
+// four (Pre-LN applied in the Q load, cross-attention with online softmax,
 // one write of O).
 #include <cstdint>
 #include <cstring>
@@ -43,81 +53,93 @@
 namespace mha {
 namespace {
 
-constexpr int kTileRows = 128;        // query rows per tile = keys per tile
+constexpr int kTileRows = 128;         // query rows per tile = keys per key tile
 constexpr int kHalfBytes = 128 * 128;  // one 128-row x 64-column bf16 box (16 KB)
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 384;
+constexpr uint32_t kSoftmaxRegs = 200;   // per thread after the split
+constexpr uint32_t kControlRegs = 104;
+constexpr int kWgThreads = 128;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
-// TMEM column map (lane = query row): two S buffers, O, two P buffers.
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
+constexpr int kMaxStages = 3;
 // Conditional rescale: O and l keep a stale max until the tile max exceeds
-// it by more than this many powers of two.  Exact after the final O / l.
+// it by more than this many powers of two (P stays <= 256).  Exact after the
+// final O / l.
 constexpr float kRescaleThreshold = 8.0f;
 
 struct AttnParams {
-    CUtensorMap tm_q;     // Q [B*H][Lq][D], box {64, 128, 1}
+    CUtensorMap tm_q;     // Q [B*H][Lq][D]; Pre-LN: x [B][Lq][H*D]; box {64, 128, 1}
     CUtensorMap tm_k;     // K [B*H][Lk][D]
     CUtensorMap tm_v;     // V [B*H][Lk][D]
     CUtensorMap tm_o;     // out: [B*H][Lq][D], or [B][Lq][H*D] for Pre-LN
-    const __nv_bfloat16 *x;   // Pre-LN input [B][Lq][H*D]
+    const float2 *ln_stats;      // Pre-LN: (mean, 1/sqrt(var + eps)) per row of x, [B*Lq]
     const float *gamma;
     const float *beta;
-    float eps;
     const int32_t *kv_lengths;   // null unless the kv-length mask is on
     int B, H, Lq, Lk;
     int causal;
     float scale_log2;     // scale * log2(e)
-    int n_qt;             // query tiles per (b, h)
-    int n_items;          // B * H * n_qt
+    int n_pairs;          // 256-row query blocks per (b, h)
+    int n_items;          // B * H * n_pairs
 };
 
 struct __align__(8) Bars {
-    uint64_t q_full, q_empty;
-    uint64_t k_full[2], v_full[2], kv_empty[2];
-    uint64_t s_full[2], p_full[2], pv_done[2];
-    uint64_t o_free;
-    uint64_t wg_bar;     // bounded barrier of the 128 softmax threads
-    uint64_t drain;      // teardown after an abort: in-flight MMAs done
+    uint64_t q_raw[2];    // producer -> Q tile (or x slice) landed
+    uint64_t q_full[2];   // Pre-LN: tile normalised -> MMA
+    uint64_t qfree[2];    // staging store has read the Q region -> producer
+    uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
+    uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+    uint64_t wg_bar[2];   // bounded barrier of each softmax warpgroup
+    uint64_t drain;       // teardown after an abort
     uint32_t tmem_base;
     int abort;
-    float ln_mean[kTileRows];
-    float ln_rstd[kTileRows];
 };
 
 template <int D>
-struct Layout {
+struct Cfg {
     static constexpr int NH = D / 64;                      // 64-column halves per tile
     static constexpr uint32_t kTile = NH * kHalfBytes;     // one 128 x D bf16 tile
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kQ + kTile;             // two stages
-    static constexpr uint32_t kV = kK + 2 * kTile;         // two stages
-    static constexpr uint32_t kO = kV + 2 * kTile;         // epilogue staging
-    static constexpr uint32_t kBars = kO + kTile;
+    static constexpr int kStages = D == 64 ? 3 : 2;        // K/V ring depth
+    static constexpr uint32_t kQ = 0;                      // two Q tiles; also O staging
+    static constexpr uint32_t kK = 2 * kTile;
+    static constexpr uint32_t kV = kK + kStages * kTile;
+    static constexpr uint32_t kBars = kV + kStages * kTile;
     static constexpr size_t kSmem = 1024 + kBars + sizeof(Bars);
+    static constexpr uint32_t kColO0 = 256;                // O_i at 256 + i * D; S_i at i * 128
+    // P_i (bf16 pairs, 64 columns): in its own columns when D = 64 leaves
+    // room (384 + 64 i); for D = 128 over the first half of S_i, where the
+    // in-order tensor pipe runs PV_i(j) before S_i(j + 1) overwrites it.
+    static constexpr uint32_t kColP0 = D == 64 ? 384 : 0;
+    static constexpr uint32_t kColPStep = D == 64 ? 64 : 128;
 };
 
 struct Item {
     int b, h, bh, q0;
     int len;      // visible keys of batch b (clamped)
-    int n_kv;     // key tiles to visit
+    int n[2];     // key tiles each query tile visits
+    int J;        // key tiles loaded = max(n[0], n[1])
 };
 
 __device__ __forceinline__ Item decode_item(const AttnParams &p, int item) {
     Item it;
     const int BH = p.B * p.H;
-    const int qt = p.n_qt - 1 - item / BH;     // heaviest (latest) query tiles first
+    const int pr = p.n_pairs - 1 - item / BH;     // heaviest (latest) query blocks first
     it.bh = item % BH;
     it.b = it.bh / p.H;
     it.h = it.bh % p.H;
-    it.q0 = qt * kTileRows;
+    it.q0 = pr * 2 * kTileRows;
     int len = p.Lk;
     if (p.kv_lengths) len = max(0, min((int)p.kv_lengths[it.b], p.Lk));
     it.len = len;
-    int kend = len;
-    if (p.causal) kend = min(kend, it.q0 + kTileRows);
-    it.n_kv = (kend + kTileRows - 1) / kTileRows;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int qi0 = it.q0 + i * kTileRows;
+        int kend = len;
+        if (p.causal) kend = min(kend, qi0 + kTileRows);
+        it.n[i] = qi0 < p.Lq ? (kend + kTileRows - 1) / kTileRows : 0;
+    }
+    it.J = max(it.n[0], it.n[1]);
     return it;
 }
 
@@ -141,80 +163,95 @@ __device__ __forceinline__ uint32_t swz_off(int r, int c) {
 
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------------------
-// Pre-LN prologue: per-row mean and 1/sqrt(var + eps) of x[b, q0 + r, :] over
-// the H*D features (fp32, shifted sums), then the head-h slice normalised,
-// scaled by gamma, shifted by beta and written as bf16 into the Q tile.
-// Thread t handles row t.
+// Pre-LN, step 1: per-row statistics of x [rows, N] (cms365.cn answer, step
+// two): mean and 1/sqrt(biased variance + eps), one warp per row, two passes
+// over the row (the second re-reads it from L1), fp32.
 // ---------------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ void prenorm_q_tile(const AttnParams &p, const Item &it, uint8_t *sQ,
-                                               int t) {
-    const int N = p.H * D;
-    const int row = it.q0 + t;
-    uint8_t *dst_row_base = sQ;
-    if (row < p.Lq) {
-        const __nv_bfloat16 *xr = p.x + ((size_t)it.b * p.Lq + row) * (size_t)N;
-        const uint4 *xv = reinterpret_cast<const uint4 *>(xr);
-        const float shift = __bfloat162float(xr[0]);
-        float s1 = 0.f, s2 = 0.f;
-        const int nchunk = N / 8;
-#pragma unroll 4
-        for (int c = 0; c < nchunk; ++c) {
-            const uint4 u = __ldg(xv + c);
+__global__ void __launch_bounds__(256) ln_row_stats_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                           float2 *__restrict__ stats,
+                                                           int64_t rows, int N, float eps) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int nchunk = N / 8;
+    for (int64_t r = warp; r < rows; r += nwarps) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + r * (int64_t)N);
+        float s = 0.f;
+        for (int c = lane; c < nchunk; c += 32) {
+            const uint4 u = __ldg(xr + c);
+            s += (bf_lo(u.x) + bf_hi(u.x)) + (bf_lo(u.y) + bf_hi(u.y)) +
+                 (bf_lo(u.z) + bf_hi(u.z)) + (bf_lo(u.w) + bf_hi(u.w));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        const float mean = s / (float)N;
+        float q = 0.f;
+        for (int c = lane; c < nchunk; c += 32) {
+            const uint4 u = __ldg(xr + c);
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float a = __uint_as_float(w[e] << 16) - shift;
-                const float bb = __uint_as_float(w[e] & 0xFFFF0000u) - shift;
-                s1 += a + bb;
-                s2 = fmaf(a, a, fmaf(bb, bb, s2));
+                const float a = bf_lo(w[e]) - mean, b = bf_hi(w[e]) - mean;
+                q = fmaf(a, a, fmaf(b, b, q));
             }
         }
-        const float inv_n = 1.f / (float)N;
-        const float dm = s1 * inv_n;
-        const float var = fmaxf(s2 * inv_n - dm * dm, 0.f);
-        const float mean = shift + dm;
-        const float rstd = rsqrtf(var + p.eps);
-        const uint4 *xs = xv + (it.h * D) / 8;
-        const float *g = p.gamma + it.h * D;
-        const float *bt = p.beta + it.h * D;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
+        if (lane == 0) stats[r] = make_float2(mean, rsqrtf(q / (float)N + eps));
+    }
+}
+
+// Pre-LN, step 2: thread t normalises row t of a Q tile in place.  The tile
+// holds the head's D-column slice of x (loaded by TMA in the swizzled layout
+// the MMA reads); y = (x - mean) * rstd * gamma + beta, rounded to bf16.
+template <int D>
+__device__ __forceinline__ void prenorm_rows_in_place(const AttnParams &p, const Item &it,
+                                                      uint8_t *sQi, int row_in_tile, int row) {
+    if (row < p.Lq) {
+        const float2 st = p.ln_stats[(size_t)it.b * p.Lq + row];
+        const float4 *g4 = reinterpret_cast<const float4 *>(p.gamma + it.h * D);
+        const float4 *b4 = reinterpret_cast<const float4 *>(p.beta + it.h * D);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
-            const uint4 u = __ldg(xs + c);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-            uint32_t o4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = c * 8 + 2 * e;
-                const float a = __uint_as_float(w[e] << 16);
-                const float bb = __uint_as_float(w[e] & 0xFFFF0000u);
-                const float ya = fmaf((a - mean) * rstd, __ldg(g + col), __ldg(bt + col));
-                const float yb = fmaf((bb - mean) * rstd, __ldg(g + col + 1), __ldg(bt + col + 1));
-                o4[e] = pack_bf16x2(ya, yb);
-            }
-            *reinterpret_cast<uint4 *>(dst_row_base + swz_off(t, c)) =
-                make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            uint4 *ptr = reinterpret_cast<uint4 *>(sQi + swz_off(row_in_tile, c));
+            const uint4 u = *ptr;
+            const float4 ga = __ldg(g4 + 2 * c), gb = __ldg(g4 + 2 * c + 1);
+            const float4 ba = __ldg(b4 + 2 * c), bb = __ldg(b4 + 2 * c + 1);
+            uint4 o;
+            o.x = pack_bf16x2(fmaf((bf_lo(u.x) - st.x) * st.y, ga.x, ba.x),
+                              fmaf((bf_hi(u.x) - st.x) * st.y, ga.y, ba.y));
+            o.y = pack_bf16x2(fmaf((bf_lo(u.y) - st.x) * st.y, ga.z, ba.z),
+                              fmaf((bf_hi(u.y) - st.x) * st.y, ga.w, ba.w));
+            o.z = pack_bf16x2(fmaf((bf_lo(u.z) - st.x) * st.y, gb.x, bb.x),
+                              fmaf((bf_hi(u.z) - st.x) * st.y, gb.y, bb.y));
+            o.w = pack_bf16x2(fmaf((bf_lo(u.w) - st.x) * st.y, gb.z, bb.z),
+                              fmaf((bf_hi(u.w) - st.x) * st.y, gb.w, bb.w));
+            *ptr = o;
         }
     } else {
 #pragma unroll
         for (int c = 0; c < D / 8; ++c)
-            *reinterpret_cast<uint4 *>(dst_row_base + swz_off(t, c)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(sQi + swz_off(row_in_tile, c)) = make_uint4(0, 0, 0, 0);
     }
 }
 
 // ---------------------------------------------------------------------------
-// The attention kernel.  Persistent-capable: CTA c takes items c, c + grid,
-// c + 2*grid, ...; all barrier phases run on counters that continue across
-// items (g = key tiles so far, qi = items with work so far).
+// The attention kernel.  CTA c takes items c, c + grid, c + 2*grid, ...; every
+// barrier phase runs on counters that continue across items:
+//   k = items so far, g = key tiles loaded so far, c_i = key tiles visited by
+//   query tile i, e_i = items in which query tile i had work.
 // ---------------------------------------------------------------------------
 template <int D, bool PRENORM>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ AttnParams p) {
-    using L = Layout<D>;
-    constexpr int NH = L::NH;
-    constexpr uint32_t TILE = L::kTile;
+    using C = Cfg<D>;
+    constexpr int NH = C::NH;
+    constexpr uint32_t TILE = C::kTile;
+    constexpr int S = C::kStages;
 
     // A bounded wait that expired earlier leaves g_status set; later launches
     // then return at once instead of timing out again.
@@ -223,35 +260,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *base = smem_raw + pad;
-    uint8_t *sQ = base + L::kQ;
-    uint8_t *sK = base + L::kK;
-    uint8_t *sV = base + L::kV;
-    uint8_t *sO = base + L::kO;
-    Bars *bars = reinterpret_cast<Bars *>(base + L::kBars);
+    uint8_t *sQ = base + C::kQ;      // query tile i at sQ + i * TILE
+    uint8_t *sK = base + C::kK;      // stage s at sK + s * TILE
+    uint8_t *sV = base + C::kV;
+    Bars *bars = reinterpret_cast<Bars *>(base + C::kBars);
     volatile int *abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars->q_full, 1);
-        mbar_init(&bars->q_empty, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->k_full[i], 1);
-            mbar_init(&bars->v_full[i], 1);
-            mbar_init(&bars->kv_empty[i], 1);
+            mbar_init(&bars->q_raw[i], 1);
+            mbar_init(&bars->q_full[i], 1);
+            mbar_init(&bars->qfree[i], 1);
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->p_full[i], kSoftmaxThreads);
-            mbar_init(&bars->pv_done[i], 1);
+            mbar_init(&bars->p_full[i], kWgThreads);
+            mbar_init(&bars->o_full[i], 1);
+            mbar_init(&bars->o_free[i], kWgThreads);
+            mbar_init(&bars->wg_bar[i], kWgThreads);
         }
-        mbar_init(&bars->o_free, kSoftmaxThreads);
-        mbar_init(&bars->wg_bar, kSoftmaxThreads);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+        }
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         mbar_fence_init();
     }
     if (warp == kProducerWarp && lane == 0) {
-        if (!PRENORM) tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
         tma_prefetch_desc(&p.tm_o);
@@ -265,52 +304,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
+    if (warp >= 8) {
+    setmaxnreg_dec<kControlRegs>();
     if (warp == kProducerWarp) {
         // ----------------------------- TMA producer -----------------------------
         if (lane == 0) {
-            uint32_t g = 0, qi = 0;
-            int q_issued = -1;          // phase of the last Q load issued
+            uint32_t g = 0, k = 0;
+            int q_pending[2] = {-1, -1};   // phase of a Q load not yet known to have landed
             bool ok = true;
+            auto load_kv = [&](const Item &it, int j) -> bool {
+                const uint32_t st = g % S;
+                if (g >= S &&
+                    !mbar_wait(&bars->kv_empty[st], ((g / S) - 1) & 1, kSiteKvEmpty, abort))
+                    return false;
+                mbar_arrive_expect_tx(&bars->k_full[st], TILE);
+#pragma unroll
+                for (int hh = 0; hh < NH; ++hh)
+                    tma_load_3d(sK + st * TILE + hh * kHalfBytes, &p.tm_k, &bars->k_full[st],
+                                hh * 64, j * kTileRows, it.bh);
+                mbar_arrive_expect_tx(&bars->v_full[st], TILE);
+#pragma unroll
+                for (int hh = 0; hh < NH; ++hh)
+                    tma_load_3d(sV + st * TILE + hh * kHalfBytes, &p.tm_v, &bars->v_full[st],
+                                hh * 64, j * kTileRows, it.bh);
+                ++g;
+                return true;
+            };
             for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
                 const Item it = decode_item(p, item);
-                if (it.n_kv == 0) continue;
-                if (!PRENORM) {
-                    if (qi > 0) ok = mbar_wait(&bars->q_empty, (qi - 1) & 1, kSiteQEmpty, abort);
+                // The first key tiles go out before this item's Q tiles, whose
+                // buffers are still being stored by the previous epilogue.
+                const int pre = min(it.J, S);
+                for (int j = 0; ok && j < pre; ++j) ok = load_kv(it, j);
+                for (int i = 0; ok && i < 2; ++i) {
+                    if (k > 0) ok = mbar_wait(&bars->qfree[i], (k - 1) & 1, kSiteQEmpty, abort);
                     if (!ok) break;
-                    q_issued = (int)(qi & 1);
-                    mbar_arrive_expect_tx(&bars->q_full, TILE);
+                    q_pending[i] = -1;
+                    if (it.n[i] > 0) {
+                        const int r0 = it.q0 + i * kTileRows;
+                        mbar_arrive_expect_tx(&bars->q_raw[i], TILE);
 #pragma unroll
-                    for (int hh = 0; hh < NH; ++hh)
-                        tma_load_3d(sQ + hh * kHalfBytes, &p.tm_q, &bars->q_full, hh * 64, it.q0,
-                                    it.bh);
-                }
-                for (int j = 0; j < it.n_kv; ++j, ++g) {
-                    const uint32_t st = g & 1;
-                    if (g >= 2) {
-                        ok = mbar_wait(&bars->kv_empty[st], ((g >> 1) - 1) & 1, kSiteKvEmpty, abort);
-                        if (!ok) break;
+                        for (int hh = 0; hh < NH; ++hh) {
+                            if (PRENORM)
+                                tma_load_3d(sQ + i * TILE + hh * kHalfBytes, &p.tm_q, &bars->q_raw[i],
+                                            it.h * D + hh * 64, r0, it.b);
+                            else
+                                tma_load_3d(sQ + i * TILE + hh * kHalfBytes, &p.tm_q, &bars->q_raw[i],
+                                            hh * 64, r0, it.bh);
+                        }
+                        q_pending[i] = (int)(k & 1);
+                    } else {
+                        mbar_arrive(&bars->q_raw[i]);   // keeps the warpgroup in step
                     }
-                    mbar_arrive_expect_tx(&bars->k_full[st], TILE);
-#pragma unroll
-                    for (int hh = 0; hh < NH; ++hh)
-                        tma_load_3d(sK + st * TILE + hh * kHalfBytes, &p.tm_k, &bars->k_full[st],
-                                    hh * 64, j * kTileRows, it.bh);
-                    mbar_arrive_expect_tx(&bars->v_full[st], TILE);
-#pragma unroll
-                    for (int hh = 0; hh < NH; ++hh)
-                        tma_load_3d(sV + st * TILE + hh * kHalfBytes, &p.tm_v, &bars->v_full[st],
-                                    hh * 64, j * kTileRows, it.bh);
                 }
-                ++qi;
+                for (int j = pre; ok && j < it.J; ++j) ok = load_kv(it, j);
+                ++k;
             }
             if (!ok) {
                 // Let the loads already issued land before shared memory is released.
                 volatile int no_abort = 0;
-                for (uint32_t gg = (g >= 2 ? g - 2 : 0); gg < g; ++gg) {
-                    mbar_wait(&bars->k_full[gg & 1], (gg >> 1) & 1, kSiteDrain, &no_abort);
-                    mbar_wait(&bars->v_full[gg & 1], (gg >> 1) & 1, kSiteDrain, &no_abort);
+                for (uint32_t gg = (g >= (uint32_t)S ? g - S : 0); gg < g; ++gg) {
+                    mbar_wait(&bars->k_full[gg % S], (gg / S) & 1, kSiteDrain, &no_abort);
+                    mbar_wait(&bars->v_full[gg % S], (gg / S) & 1, kSiteDrain, &no_abort);
                 }
-                if (q_issued >= 0) mbar_wait(&bars->q_full, (uint32_t)q_issued, kSiteDrain, &no_abort);
+                for (int i = 0; i < 2; ++i)
+                    if (q_pending[i] >= 0)
+                        mbar_wait(&bars->q_raw[i], (uint32_t)q_pending[i], kSiteDrain, &no_abort);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -319,231 +378,84 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);   // Q K-major, K K-major
             constexpr uint32_t idPV = idesc_bf16_f32(128, D, 0, 1);    // P (TMEM), V N-major
             const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
-            uint32_t g = 0, qi = 0;
+            uint32_t g = 0, k = 0, c[2] = {0, 0}, e[2] = {0, 0};
             bool ok = true;
             for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
                 const Item it = decode_item(p, item);
-                if (it.n_kv == 0) continue;
-                ok = mbar_wait(&bars->q_full, qi & 1, kSiteQFull, abort);
-                if (!ok) break;
-                // S_g = Q K_g^T into S buffer g & 1.
-                auto issue_s = [&](uint32_t gs) -> bool {
-                    const uint32_t st = gs & 1;
-                    if (!mbar_wait(&bars->k_full[st], (gs >> 1) & 1, kSiteKFull, abort)) return false;
-                    tc_fence_after();
-                    const uint32_t dS = tmem + (st ? kColS1 : kColS0);
+                if (it.J > 0) {
+                    for (int i = 0; ok && i < 2; ++i)
+                        if (it.n[i] > 0)
+                            ok = mbar_wait(PRENORM ? &bars->q_full[i] : &bars->q_raw[i], k & 1,
+                                           kSiteQFull, abort);
+                    const uint32_t g0 = g;
+                    int k_ready = -1;   // key tiles [0, k_ready] of this item have landed
+                    auto wait_k = [&](int j) -> bool {
+                        if (j <= k_ready) return true;
+                        const uint32_t gg = g0 + j;
+                        if (!mbar_wait(&bars->k_full[gg % S], (gg / S) & 1, kSiteKFull, abort))
+                            return false;
+                        k_ready = j;
+                        return true;
+                    };
+                    // S_i(j) = Q_i K_j^T into TMEM columns [128 i, 128 i + 128).
+                    auto issue_s = [&](int i, int j) {
+                        const uint32_t st = (g0 + j) % S;
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_ss(dS, desc_kmajor(sQa, kk), desc_kmajor(sKa + st * TILE, kk), idS,
-                                kk > 0 ? 1u : 0u);
-                    umma_commit(&bars->s_full[st]);
-                    return true;
-                };
-                const uint32_t g0 = g;
-                ok = issue_s(g0);
-                for (int j = 0; ok && j < it.n_kv; ++j) {
-                    const uint32_t gj = g0 + j;
-                    const uint32_t sb = gj & 1;
-                    if (j + 1 < it.n_kv) {
-                        ok = issue_s(gj + 1);
-                        if (!ok) break;
-                    } else {
-                        umma_commit(&bars->q_empty);      // Q tile no longer read
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            umma_ss(tmem + i * 128, desc_kmajor(sQa + i * TILE, kk),
+                                    desc_kmajor(sKa + st * TILE, kk), idS, kk > 0 ? 1u : 0u);
+                        umma_commit(&bars->s_full[i]);
+                    };
+                    for (int i = 0; ok && i < 2; ++i)
+                        if (it.n[i] > 0) {
+                            ok = wait_k(0);
+                            if (ok) issue_s(i, 0);
+                        }
+                    for (int j = 0; ok && j < it.J; ++j) {
+                        const uint32_t gj = g0 + j, st = gj % S;
+                        bool v_ready = false;
+                        for (int i = 0; ok && i < 2; ++i) {
+                            if (j >= it.n[i]) continue;
+                            ok = mbar_wait(&bars->p_full[i], (c[i] + j) & 1, kSitePFull, abort);
+                            if (ok && !v_ready)
+                                ok = v_ready =
+                                    mbar_wait(&bars->v_full[st], (gj / S) & 1, kSiteVFull, abort);
+                            if (ok && j == 0 && e[i] > 0)
+                                ok = mbar_wait(&bars->o_free[i], (e[i] - 1) & 1, kSiteOFree, abort);
+                            if (!ok) break;
+                            tc_fence_after();
+                            // O_i (+)= P_i V_j, P_i read from TMEM.
+                            const uint32_t dO = tmem + C::kColO0 + i * D;
+                            const uint32_t aP = tmem + C::kColP0 + i * C::kColPStep;
+#pragma unroll
+                            for (int kk = 0; kk < kTileRows / 16; ++kk)
+                                umma_ts(dO, aP + kk * 8, desc_mnmajor(sVa + st * TILE, kk), idPV,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+                            if (j + 1 < it.n[i]) {
+                                ok = wait_k(j + 1);
+                                if (ok) issue_s(i, j + 1);
+                            } else {
+                                umma_commit(&bars->o_full[i]);
+                            }
+                        }
+                        if (ok) umma_commit(&bars->kv_empty[st]);
                     }
-                    ok = mbar_wait(&bars->p_full[sb], (gj >> 1) & 1, kSitePFull, abort) &&
-                         mbar_wait(&bars->v_full[sb], (gj >> 1) & 1, kSiteVFull, abort);
-                    if (ok && j == 0 && qi > 0)
-                        ok = mbar_wait(&bars->o_free, (qi - 1) & 1, kSiteOFree, abort);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t aP = tmem + (sb ? kColP1 : kColP0);
-#pragma unroll
-                    for (int kk = 0; kk < kTileRows / 16; ++kk)
-                        umma_ts(tmem + kColO, aP + kk * 8, desc_mnmajor(sVa + sb * TILE, kk), idPV,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&bars->kv_empty[sb]);
-                    umma_commit(&bars->pv_done[sb]);
+                    g = g0 + it.J;
+                    for (int i = 0; i < 2; ++i) {
+                        c[i] += it.n[i];
+                        e[i] += it.n[i] > 0 ? 1 : 0;
+                    }
                 }
-                g = g0 + it.n_kv;
-                ++qi;
+                ++k;
             }
         }
-    } else {
-        // --------------------------- softmax warpgroup ---------------------------
-        const int t = threadIdx.x;                    // row within the tile, TMEM lane
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        uint32_t g = 0, qi = 0, wg_phase = 0;
-        bool ok = true;
-        // Waits whose outcome the whole warp shares, so warp-collective
-        // tcgen05 loads and stores never run with part of the warp gone.
-        auto wwait = [&](uint64_t *bar, uint32_t parity, uint32_t site) -> bool {
-            const bool r = mbar_wait(bar, parity, site, abort);
-            return __all_sync(0xffffffffu, r);
-        };
-        // Bounded barrier of the softmax warpgroup (an mbarrier, so an abort
-        // elsewhere cannot leave these warps blocked).
-        auto wg_sync = [&]() -> bool {
-            mbar_arrive(&bars->wg_bar);
-            const bool r = wwait(&bars->wg_bar, wg_phase & 1, kSiteWg);
-            ++wg_phase;
-            return r;
-        };
-        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
-            const Item it = decode_item(p, item);
-            const int row = it.q0 + t;
-            if (PRENORM && it.n_kv > 0) {
-                if (qi > 0) ok = wwait(&bars->q_empty, (qi - 1) & 1, kSiteQEmpty);
-                if (!ok) break;
-                prenorm_q_tile<D>(p, it, sQ, t);
-                fence_proxy_async_smem();
-                if (!(ok = wg_sync())) break;
-                if (t == 0) mbar_arrive(&bars->q_full);
-            }
-            const int vis_end = p.causal ? min(it.len, row + 1) : it.len;
-            float m_used = -INFINITY, l = 0.f;
-            for (int j = 0; j < it.n_kv; ++j) {
-                const uint32_t gj = g + j;
-                const uint32_t sb = gj & 1;
-                ok = wwait(&bars->s_full[sb], (gj >> 1) & 1, kSiteSFull);
-                if (!ok) break;
-                tc_fence_after();
-                float s[kTileRows];
-                {
-                    const uint32_t src = tmem + lane_off + (sb ? kColS1 : kColS0);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(src + c * 32, r);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) s[c * 32 + e] = u2f(r[e]);
-                    }
-                }
-                const int lim = vis_end - j * kTileRows;   // visible keys of this row in the tile
-                if (lim < kTileRows) {
-#pragma unroll
-                    for (int c = 0; c < kTileRows; ++c)
-                        if (c >= lim) s[c] = -INFINITY;
-                }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-                for (int c = 4; c < kTileRows; c += 4) {
-                    mx0 = fmaxf(mx0, s[c]);
-                    mx1 = fmaxf(mx1, s[c + 1]);
-                    mx2 = fmaxf(mx2, s[c + 2]);
-                    mx3 = fmaxf(mx3, s[c + 3]);
-                }
-                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
-                const bool need = m_tile > m_used + kRescaleThreshold;
-                float alpha = 1.f;
-                if (need) {
-                    alpha = ex2_approx(m_used - m_tile);
-                    m_used = m_tile;
-                }
-                const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-                float rs0 = 0.f, rs1 = 0.f;
-                uint32_t pk[kTileRows / 2];
-#pragma unroll
-                for (int c = 0; c < kTileRows; c += 2) {
-                    const float e0 = ex2_approx(fmaf(s[c], p.scale_log2, -msub));
-                    const float e1 = ex2_approx(fmaf(s[c + 1], p.scale_log2, -msub));
-                    rs0 += e0;
-                    rs1 += e1;
-                    pk[c >> 1] = pack_bf16x2(e0, e1);
-                }
-                l = fmaf(l, alpha, rs0 + rs1);
-                // P buffer sb was last read by the P.V MMA of tile gj - 2.
-                if (gj >= 2) {
-                    ok = wwait(&bars->pv_done[sb], ((gj - 2) >> 1) & 1, kSitePvDone);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                {
-                    const uint32_t dst = tmem + lane_off + (sb ? kColP1 : kColP0);
-                    uint32_t r[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = pk[e];
-                    tmem_st32(dst, r);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = pk[32 + e];
-                    tmem_st32(dst + 32, r);
-                    tmem_st_wait();
-                }
-                // Rescale O once the P.V of the previous tile has landed.
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
-                    const uint32_t gp = gj - 1;
-                    ok = wwait(&bars->pv_done[gp & 1], (gp >> 1) & 1, kSitePvDone);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t oa = tmem + lane_off + kColO;
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(oa + c * 32, r);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = f2u(u2f(r[e]) * alpha);
-                        tmem_st32(oa + c * 32, r);
-                    }
-                    tmem_st_wait();
-                }
-                tc_fence_before();
-                mbar_arrive(&bars->p_full[sb]);
-            }
-            if (!ok) break;
-
-            // ------------------------------- epilogue -------------------------------
-            // sO is reused per item: the previous item's TMA store must have read it.
-            if (t == 0) tma_store_wait_read();
-            if (!(ok = wg_sync())) break;
-            if (it.n_kv > 0) {
-                const uint32_t gl = g + it.n_kv - 1;
-                ok = wwait(&bars->pv_done[gl & 1], (gl >> 1) & 1, kSitePvDone);
-                if (!ok) break;
-                tc_fence_after();
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                const uint32_t oa = tmem + lane_off + kColO;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(oa + c * 32, r);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 w;
-                        w.x = pack_bf16x2(u2f(r[q4 * 8 + 0]) * inv, u2f(r[q4 * 8 + 1]) * inv);
-                        w.y = pack_bf16x2(u2f(r[q4 * 8 + 2]) * inv, u2f(r[q4 * 8 + 3]) * inv);
-                        w.z = pack_bf16x2(u2f(r[q4 * 8 + 4]) * inv, u2f(r[q4 * 8 + 5]) * inv);
-                        w.w = pack_bf16x2(u2f(r[q4 * 8 + 6]) * inv, u2f(r[q4 * 8 + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(sO + swz_off(t, c * 4 + q4)) = w;
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&bars->o_free);
-            } else {
-#pragma unroll
-                for (int c = 0; c < D / 8; ++c)
-                    *reinterpret_cast<uint4 *>(sO + swz_off(t, c)) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            if (!(ok = wg_sync())) break;
-            if (t == 0) {
-#pragma unroll
-                for (int hh = 0; hh < NH; ++hh) {
-                    if (PRENORM)
-                        tma_store_3d(&p.tm_o, sO + hh * kHalfBytes, it.h * D + hh * 64, it.q0, it.b);
-                    else
-                        tma_store_3d(&p.tm_o, sO + hh * kHalfBytes, hh * 64, it.q0, it.bh);
-                }
-                tma_store_commit();
-            }
-            g += it.n_kv;
-            if (it.n_kv > 0) ++qi;
-        }
-        if (t == 0) tma_store_wait_all();
     }
-
     // ------------------------------- teardown --------------------------------
+    // Every softmax thread has arrived on barrier 1 once it is done with TMEM.
     __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    named_barrier_sync(1, kThreads);
     if (warp == kMmaWarp) {
         tc_fence_after();
         if (*abort) {
@@ -556,6 +468,160 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         }
         tmem_dealloc(tmem, kTmemCols);
+    }
+    } else {
+        setmaxnreg_inc<kSoftmaxRegs>();
+        // --------------------------- softmax warpgroups ---------------------------
+        const int wg = warp >> 2;                       // query tile of this warpgroup
+        const int t = threadIdx.x & (kWgThreads - 1);   // row in the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_off + wg * 128;
+        const uint32_t tO = tmem + lane_off + C::kColO0 + wg * D;
+        const uint32_t tP = tmem + lane_off + C::kColP0 + wg * C::kColPStep;
+        uint8_t *sQi = sQ + wg * TILE;
+        uint32_t k = 0, c = 0, e = 0, wgp = 0;
+        bool ok = true;
+        // Waits whose outcome the whole warp shares, so warp-collective
+        // tcgen05 loads and stores never run with part of the warp gone.
+        auto wwait = [&](uint64_t *bar, uint32_t parity, uint32_t site) -> bool {
+            const bool r = mbar_wait(bar, parity, site, abort);
+            return __all_sync(0xffffffffu, r);
+        };
+        // Bounded barrier of this warpgroup (an mbarrier, so an abort elsewhere
+        // cannot leave these warps blocked).
+        auto wg_sync = [&]() -> bool {
+            mbar_arrive(&bars->wg_bar[wg]);
+            const bool r = wwait(&bars->wg_bar[wg], wgp & 1, kSiteWg);
+            ++wgp;
+            return r;
+        };
+        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+            const Item it = decode_item(p, item);
+            const int n = it.n[wg];
+            const int q0i = it.q0 + wg * kTileRows;
+            const int row = q0i + t;
+            ok = wwait(&bars->q_raw[wg], k & 1, kSiteQFull);
+            if (!ok) break;
+            if (PRENORM) {
+                if (n > 0) {
+                    prenorm_rows_in_place<D>(p, it, sQi, t, row);
+                    fence_proxy_async_smem();
+                }
+                if (!(ok = wg_sync())) break;
+                if (t == 0) mbar_arrive(&bars->q_full[wg]);
+            }
+            const int vis_end = p.causal ? min(it.len, row + 1) : it.len;
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < n; ++j) {
+                ok = wwait(&bars->s_full[wg], (c + j) & 1, kSiteSFull);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t s[kTileRows];
+                tmem_ld128(tS, s);
+                const int lim = vis_end - j * kTileRows;   // visible keys of this row in the tile
+                if (lim < kTileRows) {
+#pragma unroll
+                    for (int cc = 0; cc < kTileRows; ++cc)
+                        if (cc >= lim) s[cc] = f2u(-INFINITY);
+                }
+                float mx0 = u2f(s[0]), mx1 = u2f(s[1]), mx2 = u2f(s[2]), mx3 = u2f(s[3]);
+#pragma unroll
+                for (int cc = 4; cc < kTileRows; cc += 4) {
+                    mx0 = fmaxf(mx0, u2f(s[cc]));
+                    mx1 = fmaxf(mx1, u2f(s[cc + 1]));
+                    mx2 = fmaxf(mx2, u2f(s[cc + 2]));
+                    mx3 = fmaxf(mx3, u2f(s[cc + 3]));
+                }
+                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+                const bool need = m_tile > m_used + kRescaleThreshold;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2_approx(m_used - m_tile);
+                    m_used = m_tile;
+                }
+                const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+                float rs0 = 0.f, rs1 = 0.f;
+                // P overwrites the low half of s as packed bf16 pairs.
+#pragma unroll
+                for (int cc = 0; cc < kTileRows; cc += 2) {
+                    const float e0 = ex2_approx(fmaf(u2f(s[cc]), p.scale_log2, -msub));
+                    const float e1 = ex2_approx(fmaf(u2f(s[cc + 1]), p.scale_log2, -msub));
+                    rs0 += e0;
+                    rs1 += e1;
+                    s[cc >> 1] = pack_bf16x2(e0, e1);
+                }
+                l = fmaf(l, alpha, rs0 + rs1);
+                // The commit behind s_full covers the previous P.V, so O is at rest.
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + ch * 32, r);
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) r[q] = f2u(u2f(r[q]) * alpha);
+                        tmem_st32(tO + ch * 32, r);
+                    }
+                }
+                tmem_st64(tP, *reinterpret_cast<uint32_t(*)[64]>(s));
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars->p_full[wg]);
+            }
+            if (!ok) break;
+
+            // ------------------------------- epilogue -------------------------------
+            // O / l as bf16 into the Q region of this tile (free once o_full
+            // fired: its commit covers every MMA that read Q), then one TMA store.
+            if (n > 0) {
+                ok = wwait(&bars->o_full[wg], e & 1, kSitePvDone);
+                if (!ok) break;
+                tc_fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + ch * 32, r);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 w;
+                        w.x = pack_bf16x2(u2f(r[q4 * 8 + 0]) * inv, u2f(r[q4 * 8 + 1]) * inv);
+                        w.y = pack_bf16x2(u2f(r[q4 * 8 + 2]) * inv, u2f(r[q4 * 8 + 3]) * inv);
+                        w.z = pack_bf16x2(u2f(r[q4 * 8 + 4]) * inv, u2f(r[q4 * 8 + 5]) * inv);
+                        w.w = pack_bf16x2(u2f(r[q4 * 8 + 6]) * inv, u2f(r[q4 * 8 + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(sQi + swz_off(t, ch * 4 + q4)) = w;
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bars->o_free[wg]);
+            } else {
+#pragma unroll
+                for (int ch = 0; ch < D / 8; ++ch)
+                    *reinterpret_cast<uint4 *>(sQi + swz_off(t, ch)) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            if (!(ok = wg_sync())) break;
+            if (t == 0) {
+                if (q0i < p.Lq) {
+#pragma unroll
+                    for (int hh = 0; hh < NH; ++hh) {
+                        if (PRENORM)
+                            tma_store_3d(&p.tm_o, sQi + hh * kHalfBytes, it.h * D + hh * 64, q0i, it.b);
+                        else
+                            tma_store_3d(&p.tm_o, sQi + hh * kHalfBytes, hh * 64, q0i, it.bh);
+                    }
+                    tma_store_commit();
+                    tma_store_wait_read();
+                }
+                mbar_arrive(&bars->qfree[wg]);
+            }
+            c += n;
+            e += n > 0 ? 1 : 0;
+            ++k;
+        }
+        if (t == 0) tma_store_wait_all();
+        __syncwarp();
+        tc_fence_before();
+        named_barrier_arrive(1, kThreads);
     }
 }
 
@@ -700,7 +766,7 @@ int g_grid_override = 0;
 
 template <int D, bool PRENORM>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
-    constexpr size_t smem = Layout<D>::kSmem;
+    constexpr size_t smem = Cfg<D>::kSmem;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<D, PRENORM>,
@@ -730,14 +796,28 @@ cudaError_t read_device_status(uint32_t *bits, bool clear) {
     return e;
 }
 
-cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_err) {
+cudaError_t launch_ln_row_stats(const void *x, float2 *stats, int64_t rows, int N, float eps,
+                                cudaStream_t stream) {
+    const int64_t warps = (rows + 0) > 0 ? rows : 1;
+    int64_t blocks = (warps + 7) / 8;
+    if (blocks > 152 * 32) blocks = 152 * 32;
+    ln_row_stats_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16 *>(x), stats, rows, N, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_err,
+                            float2 *ln_stats) {
     *driver_err = 0;
     AttnParams p;
     std::memset(&p, 0, sizeof(p));
     const bool prenorm = c.x != nullptr;
     const uint64_t BH = (uint64_t)c.B * c.H;
-    CUresult r = CUDA_SUCCESS;
-    if (!prenorm) r = encode_bf16_3d(&p.tm_q, c.q, c.D, c.Lq, BH);
+    CUresult r;
+    if (prenorm)
+        r = encode_bf16_3d(&p.tm_q, c.x, (uint64_t)c.H * c.D, c.Lq, c.B);
+    else
+        r = encode_bf16_3d(&p.tm_q, c.q, c.D, c.Lq, BH);
     if (r == CUDA_SUCCESS) {
         // With no keys the K/V maps are never used; point them at a valid array.
         const bool has_k = c.Lk > 0;
@@ -755,10 +835,9 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
         *driver_err = (int)r;
         return cudaErrorInvalidValue;
     }
-    p.x = reinterpret_cast<const __nv_bfloat16 *>(c.x);
+    p.ln_stats = ln_stats;
     p.gamma = c.gamma;
     p.beta = c.beta;
-    p.eps = c.eps;
     p.kv_lengths = (c.mask_kind & 2) ? c.kv_lengths : nullptr;
     p.B = c.B;
     p.H = c.H;
@@ -766,9 +845,14 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     p.Lk = c.Lk;
     p.causal = (c.mask_kind & 1) ? 1 : 0;
     p.scale_log2 = c.scale * 1.4426950408889634f;
-    p.n_qt = (c.Lq + kTileRows - 1) / kTileRows;
-    p.n_items = (int)(BH * (uint64_t)p.n_qt);
-    if (prenorm) return c.D == 64 ? launch_attn<64, true>(p, stream) : launch_attn<128, true>(p, stream);
+    p.n_pairs = (c.Lq + 2 * kTileRows - 1) / (2 * kTileRows);
+    p.n_items = (int)(BH * (uint64_t)p.n_pairs);
+    if (prenorm) {
+        cudaError_t e = launch_ln_row_stats(c.x, ln_stats, (int64_t)c.B * c.Lq, c.H * c.D, c.eps,
+                                            stream);
+        if (e != cudaSuccess) return e;
+        return c.D == 64 ? launch_attn<64, true>(p, stream) : launch_attn<128, true>(p, stream);
+    }
     return c.D == 64 ? launch_attn<64, false>(p, stream) : launch_attn<128, false>(p, stream);
 }
 

@@ -30,8 +30,10 @@ struct Bf16Call {
 };
 
 // Returns cudaSuccess or the first CUDA error; *driver_err receives a
-// nonzero CUresult when tensor-map encoding failed.
-cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_err);
+// nonzero CUresult when tensor-map encoding failed.  For the Pre-LN variant
+// `ln_stats` is device scratch of B*Lq float2 (row mean, 1/sqrt(var + eps)).
+cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_err,
+                            float2 *ln_stats);
 
 // Diagnostic single-tile tcgen05 GEMM (fwd_bf16.cu).
 cudaError_t launch_selftest_umma(int variant, int K_or_N, const void *a, const void *b,
