@@ -58,7 +58,8 @@ typedef enum {
     MHA_ERR_UNSUPPORTED = -2,   /* D not in {64, 128}, dtype not handled by this entry point */
     MHA_ERR_MISALIGNED = -3,    /* a tensor pointer is not 16-byte aligned */
     MHA_ERR_CUDA = -4,          /* the CUDA runtime or driver reported an error */
-    MHA_ERR_DEVICE = -5         /* a kernel's bounded wait expired (see mha_device_status) */
+    MHA_ERR_DEVICE = -5,        /* a kernel's bounded wait expired (see mha_device_status) */
+    MHA_ERR_TOO_LARGE = -6      /* problem larger than a fixed-size scratch area allows */
 } mha_status;
 
 /* Mask kinds: bit flags, combinable (MHA_MASK_CAUSAL | MHA_MASK_KV_LEN). */
@@ -114,6 +115,32 @@ MHA_API int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const fl
                            const int32_t *kv_lengths, void *out, int B, int H,
                            int Lq, int Lk, int D, float scale, int dtype,
                            cudaStream_t stream);
+
+/*
+ * prenorm_cross_attn_fwd_noalloc -- the same computation as
+ * prenorm_cross_attn_fwd, for callers that cannot let a library allocate
+ * device memory: for example a serving runtime that reserves all GPU memory
+ * for its own pools at start-up and gives libraries only the buffers it
+ * planned, or a latency-critical loop in which an allocation could block or
+ * fail.  (No counterpart on the pages; this is an interface addition.)
+ *   Arguments, layouts and results are those of prenorm_cross_attn_fwd.
+ *   Memory: calls no allocator.  The per-row statistics go to a fixed array
+ *   of 262144 float2 (2 MiB) that is part of the library's device image and
+ *   stays resident on every GPU that loads the library until the process
+ *   exits.  B*Lq above 262144 returns MHA_ERR_TOO_LARGE without launching.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress) with that device current; make that first
+ *   call before any stream capture.
+ *   Sharing: every call uses the same array and it keeps the last call's
+ *   values (nothing needs clearing: each call writes every row it reads).
+ *   Calls whose kernels can overlap on the GPU (different streams, or
+ *   different host threads, on one device) race on it; order them.
+ */
+MHA_API int prenorm_cross_attn_fwd_noalloc(const void *x_q, const float *gamma,
+                                           const float *beta, float eps, const void *k,
+                                           const void *v, const int32_t *kv_lengths,
+                                           void *out, int B, int H, int Lq, int Lk, int D,
+                                           float scale, int dtype, cudaStream_t stream);
 
 /* Static, human-readable text for an mha_status value. */
 MHA_API const char *mha_strerror(int status);

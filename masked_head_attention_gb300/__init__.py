@@ -175,3 +175,41 @@ def selftest_umma(variant, kn, a, b, c, stream=None):
 
 def set_bf16_grid(ctas):
     lib().mha_set_bf16_grid(int(ctas))
+
+
+def prenorm_cross_attn_fwd_noalloc(x_q, gamma, beta, eps, k, v, kv_lengths=None, out=None,
+                                   scale=None, stream=None):
+    """prenorm_cross_attn_fwd without any allocation by the library: for
+    callers whose device memory is planned and owned elsewhere (e.g. a
+    serving runtime that reserves all GPU memory for its own pools).  The
+    row statistics use a fixed 2 MiB device array (B*Lq <= 262144); calls
+    that overlap on the GPU share that array and race.  `out` should be
+    passed in by such callers (it is created here only when omitted)."""
+    torch = _torch()
+    L = lib()
+    if not getattr(L, "_noalloc_bound", False):
+        P, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.prenorm_cross_attn_fwd_noalloc.argtypes = [P, P, P, f, P, P, P, P, i, i, i, i, i, f, i, P]
+        L.prenorm_cross_attn_fwd_noalloc.restype = i
+        L._noalloc_bound = True
+    _dev(x_q, "x_q", torch.bfloat16)
+    _dev(gamma, "gamma", torch.float32)
+    _dev(beta, "beta", torch.float32)
+    _dev(k, "k", torch.bfloat16)
+    _dev(v, "v", torch.bfloat16)
+    B, H, Lk, D = k.shape
+    Lq = x_q.shape[1]
+    if tuple(x_q.shape) != (B, Lq, H * D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("x_q must be [B,Lq,H*D] and v [B,H,Lk,D]")
+    if kv_lengths is not None:
+        _dev(kv_lengths, "kv_lengths", torch.int32)
+    if out is None:
+        out = torch.empty_like(x_q)
+    else:
+        _dev(out, "out", torch.bfloat16)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(L.prenorm_cross_attn_fwd_noalloc(_ptr(x_q), _ptr(gamma), _ptr(beta), float(eps),
+                                            _ptr(k), _ptr(v), _ptr(kv_lengths), _ptr(out), B, H,
+                                            Lq, Lk, D, scale, BF16, _stream(stream)),
+           "prenorm_cross_attn_fwd_noalloc")
+    return out

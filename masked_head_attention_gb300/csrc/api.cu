@@ -112,6 +112,46 @@ int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const float *bet
     return from_cuda(e);
 }
 
+int prenorm_cross_attn_fwd_noalloc(const void *x_q, const float *gamma, const float *beta,
+                                   float eps, const void *k, const void *v,
+                                   const int32_t *kv_lengths, void *out, int B, int H, int Lq,
+                                   int Lk, int D, float scale, int dtype, cudaStream_t stream) {
+    int empty = 0;
+    int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
+    if (st != MHA_OK) return st;
+    if (dtype != MHA_BF16) return MHA_ERR_UNSUPPORTED;
+    if (!(std::isfinite(eps) && eps >= 0.f)) return MHA_ERR_INVALID_ARG;
+    if ((int64_t)H * D > 65536) return MHA_ERR_INVALID_ARG;
+    if ((int64_t)B * Lq > mha::kNoAllocMaxRows) return MHA_ERR_TOO_LARGE;
+    if (empty) return MHA_OK;
+    if (!x_q || !gamma || !beta || !out || (Lk > 0 && (!k || !v))) return MHA_ERR_INVALID_ARG;
+    if (!aligned16(x_q) || !aligned16(out) || !aligned16(gamma) || !aligned16(beta) ||
+        (Lk > 0 && (!aligned16(k) || !aligned16(v))))
+        return MHA_ERR_MISALIGNED;
+    float2 *stats = nullptr;
+    if (mha::noalloc_ln_stats((int64_t)B * Lq, &stats) != cudaSuccess) return MHA_ERR_CUDA;
+    mha::Bf16Call c{};
+    c.x = x_q;
+    c.gamma = gamma;
+    c.beta = beta;
+    c.eps = eps;
+    c.k = k;
+    c.v = v;
+    c.kv_lengths = kv_lengths;
+    c.out = out;
+    c.B = B;
+    c.H = H;
+    c.Lq = Lq;
+    c.Lk = Lk;
+    c.D = D;
+    c.mask_kind = kv_lengths ? MHA_MASK_KV_LEN : MHA_MASK_NONE;
+    c.scale = scale;
+    int drv = 0;
+    cudaError_t e = mha::launch_fwd_bf16(c, stream, &drv, stats);
+    if (drv != 0) return MHA_ERR_CUDA;
+    return from_cuda(e);
+}
+
 const char *mha_strerror(int status) {
     switch (status) {
         case MHA_OK: return "success";
@@ -120,6 +160,7 @@ const char *mha_strerror(int status) {
         case MHA_ERR_MISALIGNED: return "a tensor pointer is not 16-byte aligned";
         case MHA_ERR_CUDA: return "CUDA runtime or driver error";
         case MHA_ERR_DEVICE: return "a kernel's bounded wait expired (see mha_device_status)";
+        case MHA_ERR_TOO_LARGE: return "B*Lq exceeds the fixed scratch of prenorm_cross_attn_fwd_noalloc (262144 rows)";
         default: return "unknown status";
     }
 }

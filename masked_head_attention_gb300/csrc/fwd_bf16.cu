@@ -796,6 +796,39 @@ cudaError_t read_device_status(uint32_t *bits, bool clear) {
     return e;
 }
 
+// ---------------------------------------------------------------------------
+// Fixed scratch for the no-allocation Pre-LN entry point: the per-row
+// statistics (mean, 1/sqrt(var + eps)) of up to kNoAllocMaxRows rows of x.
+// It is part of the module image, so every GPU that loads this library holds
+// these 2 MiB until the process exits.  Every call shares it; nothing in it
+// needs clearing, because the statistics pass writes every row the attention
+// kernel later reads.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) float2 g_noalloc_ln_stats[kNoAllocMaxRows];
+
+cudaError_t noalloc_ln_stats(int64_t rows, float2 **ptr) {
+    *ptr = nullptr;
+    if (rows > kNoAllocMaxRows) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    // The host-side name of the array is not a device address: look the
+    // address up once per device, with that device current, and reuse it.
+    constexpr int kMaxDevices = 64;
+    static void *addr[kMaxDevices] = {};
+    static std::mutex lock;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> guard(lock);
+    if (addr[dev] == nullptr) {
+        void *a = nullptr;
+        e = cudaGetSymbolAddress(&a, g_noalloc_ln_stats);
+        if (e != cudaSuccess) return e;
+        addr[dev] = a;
+    }
+    *ptr = static_cast<float2 *>(addr[dev]);
+    return cudaSuccess;
+}
+
 cudaError_t launch_ln_row_stats(const void *x, float2 *stats, int64_t rows, int N, float eps,
                                 cudaStream_t stream) {
     const int64_t warps = (rows + 0) > 0 ? rows : 1;

@@ -39,6 +39,12 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
 cudaError_t launch_selftest_umma(int variant, int K_or_N, const void *a, const void *b,
                                  float *c, cudaStream_t stream, int *driver_err);
 
+// No-allocation Pre-LN: device address of the fixed row-statistics array
+// (looked up once per device, with that device current).  Fails with
+// cudaErrorInvalidValue when `rows` exceeds kNoAllocMaxRows.
+constexpr int64_t kNoAllocMaxRows = 262144;
+cudaError_t noalloc_ln_stats(int64_t rows, float2 **ptr);
+
 // Device status word of the bf16 translation unit.
 cudaError_t read_device_status(uint32_t *bits, bool clear);
 

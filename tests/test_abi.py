@@ -11,7 +11,7 @@ from masked_head_attention_gb300 import build as mbuild
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "mha.h")
 
-OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA, DEVICE = 0, -1, -2, -3, -4, -5
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA, DEVICE, TOO_LARGE = 0, -1, -2, -3, -4, -5, -6
 
 
 @pytest.fixture(scope="module")
@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_strerror_covers_every_status(L):
-    for code in (OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA, DEVICE):
+    for code in (OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA, DEVICE, TOO_LARGE):
         s = L.mha_strerror(code).decode()
         assert s and s != "unknown status"
     assert L.mha_strerror(12345).decode() == "unknown status"
