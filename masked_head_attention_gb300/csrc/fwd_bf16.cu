@@ -11,13 +11,15 @@
 //              the first 64 columns of its S buffer when D = 128, in columns
 //              of its own when D = 64), and rescales its O row in TMEM
 //              when the max grows.  At the end it divides O by the row sum and
-//              stores the tile through shared memory with TMA.  In the Pre-LN
+//              writes its row of O once (16-byte stores).  In the Pre-LN
 //              variant it first normalises its rows of the Q tile in place.
 //   warp 8     TMA producer: both Q tiles per item (the head's slice of x for
 //              Pre-LN), K and V tiles of 128 keys through a ring of stages;
 //              key tiles past the causal limit or the valid length are never
 //              loaded.  The first K/V tiles of an item are issued before its
-//              Q tiles, overlapping the previous item's epilogue.
+//              Q tiles; a Q tile is reloaded as soon as the last QK^T product
+//              that reads it has completed, so the next item's loads overlap
+//              this item's last softmax, P.V and epilogue.
 //   warp 9     MMA issuer (one thread) and TMEM owner (S0, S1, O0, O1 = 512
 //              columns).  Issue order per key tile j:
 //                  PV0(j), S0(j+1), PV1(j), S1(j+1)
@@ -72,7 +74,7 @@ struct AttnParams {
     CUtensorMap tm_q;     // Q [B*H][Lq][D]; Pre-LN: x [B][Lq][H*D]; box {64, 128, 1}
     CUtensorMap tm_k;     // K [B*H][Lk][D]
     CUtensorMap tm_v;     // V [B*H][Lk][D]
-    CUtensorMap tm_o;     // out: [B*H][Lq][D], or [B][Lq][H*D] for Pre-LN
+    __nv_bfloat16 *out;   // [B*H][Lq][D], or [B][Lq][H*D] for Pre-LN
     const float2 *ln_stats;      // Pre-LN: (mean, 1/sqrt(var + eps)) per row of x, [B*Lq]
     const float *gamma;
     const float *beta;
@@ -82,12 +84,13 @@ struct AttnParams {
     float scale_log2;     // scale * log2(e)
     int n_pairs;          // 256-row query blocks per (b, h)
     int n_items;          // B * H * n_pairs
+    int group;            // (b, h) problems per scheduling group (their K/V fit in L2)
 };
 
 struct __align__(8) Bars {
     uint64_t q_raw[2];    // producer -> Q tile (or x slice) landed
     uint64_t q_full[2];   // Pre-LN: tile normalised -> MMA
-    uint64_t qfree[2];    // staging store has read the Q region -> producer
+    uint64_t qfree[2];    // Q tile i free: MMA issuer (last QK^T done) + each warp of WG i
     uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
     uint64_t wg_bar[2];   // bounded barrier of each softmax warpgroup
@@ -121,11 +124,19 @@ struct Item {
     int J;        // key tiles loaded = max(n[0], n[1])
 };
 
+// Item order: groups of `group` (b, h) problems whose K/V fit in L2 together;
+// inside a group the latest (for causal masks the heaviest) 256-row query
+// blocks come first and the (b, h) index varies fastest, so CTAs running at
+// the same time share K/V tiles through L2.
 __device__ __forceinline__ Item decode_item(const AttnParams &p, int item) {
     Item it;
     const int BH = p.B * p.H;
-    const int pr = p.n_pairs - 1 - item / BH;     // heaviest (latest) query blocks first
-    it.bh = item % BH;
+    const int per_group = p.group * p.n_pairs;
+    const int grp = item / per_group;
+    const int within = item - grp * per_group;
+    const int gsize = min(p.group, BH - grp * p.group);
+    const int pr = p.n_pairs - 1 - within / gsize;
+    it.bh = grp * p.group + within % gsize;
     it.b = it.bh / p.H;
     it.h = it.bh % p.H;
     it.q0 = pr * 2 * kTileRows;
@@ -245,6 +256,23 @@ __device__ __forceinline__ void prenorm_rows_in_place(const AttnParams &p, const
 //   k = items so far, g = key tiles loaded so far, c_i = key tiles visited by
 //   query tile i, e_i = items in which query tile i had work.
 // ---------------------------------------------------------------------------
+// Item sequence of a CTA: a persistent grid walks the ordered item list in
+// rounds of gridDim.x, forward in even rounds and backward in odd ones, so a
+// CTA that drew a heavy item early draws a light one next (a static
+// approximation of longest-processing-time-first).
+struct ItemIter {
+    int r = 0, idx = -1;
+    __device__ __forceinline__ bool next(int n_items) {
+        const int G = gridDim.x, c = blockIdx.x;
+        for (;;) {
+            if ((long long)r * G >= n_items) return false;
+            idx = (r & 1) ? (r + 1) * G - 1 - c : r * G + c;
+            ++r;
+            if (idx < n_items) return true;
+        }
+    }
+};
+
 template <int D, bool PRENORM>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ AttnParams p) {
@@ -273,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->q_raw[i], 1);
             mbar_init(&bars->q_full[i], 1);
-            mbar_init(&bars->qfree[i], 1);
+            mbar_init(&bars->qfree[i], 1 + kWgThreads / 32);   // issuer + each softmax warp
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->p_full[i], kWgThreads);
             mbar_init(&bars->o_full[i], 1);
@@ -293,7 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
-        tma_prefetch_desc(&p.tm_o);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -330,10 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++g;
                 return true;
             };
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
-                const Item it = decode_item(p, item);
+            ItemIter iter;
+            while (ok && iter.next(p.n_items)) {
+                const Item it = decode_item(p, iter.idx);
                 // The first key tiles go out before this item's Q tiles, whose
-                // buffers are still being stored by the previous epilogue.
+                // buffers the previous item may still be reading.
                 const int pre = min(it.J, S);
                 for (int j = 0; ok && j < pre; ++j) ok = load_kv(it, j);
                 for (int i = 0; ok && i < 2; ++i) {
@@ -377,16 +405,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);   // Q K-major, K K-major
             constexpr uint32_t idPV = idesc_bf16_f32(128, D, 0, 1);    // P (TMEM), V N-major
-            const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+            // Base descriptors, built once.  A K-step, a tile or a stage moves only
+            // the start-address field in the low word (addresses < 256 KB: no carry).
+            const uint64_t dq = desc_kmajor(smem_u32(sQ), 0);
+            const uint64_t dk = desc_kmajor(smem_u32(sK), 0);
+            const uint64_t dv = desc_mnmajor(smem_u32(sV), 0);
+            const uint32_t q_lo = (uint32_t)dq, q_hi = (uint32_t)(dq >> 32);
+            const uint32_t k_lo = (uint32_t)dk, k_hi = (uint32_t)(dk >> 32);
+            const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
+            constexpr uint32_t kTileUnits = TILE >> 4;           // one tile, in 16-byte units
             uint32_t g = 0, k = 0, c[2] = {0, 0}, e[2] = {0, 0};
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
-                const Item it = decode_item(p, item);
-                if (it.J > 0) {
-                    for (int i = 0; ok && i < 2; ++i)
-                        if (it.n[i] > 0)
-                            ok = mbar_wait(PRENORM ? &bars->q_full[i] : &bars->q_raw[i], k & 1,
-                                           kSiteQFull, abort);
+            ItemIter iter;
+            while (ok && iter.next(p.n_items)) {
+                const Item it = decode_item(p, iter.idx);
+                // Every item passes through both Q barriers, with or without work
+                // for the tile, so no role can run two phases ahead of another.
+                for (int i = 0; ok && i < 2; ++i) {
+                    ok = mbar_wait(PRENORM ? &bars->q_full[i] : &bars->q_raw[i], k & 1, kSiteQFull,
+                                   abort);
+                    if (ok && it.n[i] == 0) mbar_arrive(&bars->qfree[i]);   // tile never read
+                }
+                if (ok && it.J > 0) {
                     const uint32_t g0 = g;
                     int k_ready = -1;   // key tiles [0, k_ready] of this item have landed
                     auto wait_k = [&](int j) -> bool {
@@ -397,15 +437,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         k_ready = j;
                         return true;
                     };
-                    // S_i(j) = Q_i K_j^T into TMEM columns [128 i, 128 i + 128).
+                    // S_i(j) = Q_i K_j^T into TMEM columns [128 i, 128 i + 128).  After
+                    // the last QK^T of the item, the Q tile is released (qfree).
                     auto issue_s = [&](int i, int j) {
                         const uint32_t st = (g0 + j) % S;
+                        const uint32_t a0 = q_lo + i * kTileUnits, b0 = k_lo + st * kTileUnits;
                         tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            umma_ss(tmem + i * 128, desc_kmajor(sQa + i * TILE, kk),
-                                    desc_kmajor(sKa + st * TILE, kk), idS, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            // K-step kk: 64-column half kk/4, 32 bytes per step inside it.
+                            const uint32_t off =
+                                (uint32_t)((kk >> 2) * (kHalfBytes >> 4) + (kk & 3) * 2);
+                            umma_ss_w(tmem + i * 128, a0 + off, q_hi, b0 + off, k_hi, idS,
+                                      kk > 0 ? 1u : 0u);
+                        }
                         umma_commit(&bars->s_full[i]);
+                        if (j + 1 == it.n[i]) umma_commit(&bars->qfree[i]);
                     };
                     for (int i = 0; ok && i < 2; ++i)
                         if (it.n[i] > 0) {
@@ -428,10 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // O_i (+)= P_i V_j, P_i read from TMEM.
                             const uint32_t dO = tmem + C::kColO0 + i * D;
                             const uint32_t aP = tmem + C::kColP0 + i * C::kColPStep;
+                            const uint32_t vb = v_lo + st * kTileUnits;
+                            const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-                            for (int kk = 0; kk < kTileRows / 16; ++kk)
-                                umma_ts(dO, aP + kk * 8, desc_mnmajor(sVa + st * TILE, kk), idPV,
-                                        (j > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < kTileRows / 16; ++kk)   // 16 keys = 2048 B of V
+                                umma_ts_w(dO, aP + kk * 8, vb + kk * (2048 >> 4), v_hi, idPV,
+                                          kk > 0 ? 1u : acc0);
                             if (j + 1 < it.n[i]) {
                                 ok = wait_k(j + 1);
                                 if (ok) issue_s(i, j + 1);
@@ -495,8 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++wgp;
             return r;
         };
-        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
-            const Item it = decode_item(p, item);
+        ItemIter iter;
+        while (ok && iter.next(p.n_items)) {
+            const Item it = decode_item(p, iter.idx);
             const int n = it.n[wg];
             const int q0i = it.q0 + wg * kTileRows;
             const int row = q0i + t;
@@ -510,6 +560,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wg_sync())) break;
                 if (t == 0) mbar_arrive(&bars->q_full[wg]);
             }
+            // This warp is done with the Q tile; the issuer's arrival on qfree
+            // says when the MMAs are.  Every warp arrives (not one thread per
+            // warpgroup): a warp that ran ahead through items without work
+            // must not let the producer move the Q barrier two phases past a
+            // slower warp of the same warpgroup.
+            if (lane == 0) mbar_arrive(&bars->qfree[wg]);
             const int vis_end = p.causal ? min(it.len, row + 1) : it.len;
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
@@ -570,55 +626,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             // ------------------------------- epilogue -------------------------------
-            // O / l as bf16 into the Q region of this tile (free once o_full
-            // fired: its commit covers every MMA that read Q), then one TMA store.
+            // O / l as bf16, written once: row t of the tile is one contiguous
+            // run of D values (16-byte stores); rows past Lq are not written.
             if (n > 0) {
                 ok = wwait(&bars->o_full[wg], e & 1, kSitePvDone);
                 if (!ok) break;
                 tc_fence_after();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
+                __nv_bfloat16 *dst =
+                    PRENORM ? p.out + ((size_t)it.b * p.Lq + row) * (size_t)(p.H * D) + it.h * D
+                            : p.out + ((size_t)it.bh * p.Lq + row) * (size_t)D;
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t r[32];
                     tmem_ld32(tO + ch * 32, r);
+                    if (ch == D / 32 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(&bars->o_free[wg]);   // O of this tile has been read
+                    }
+                    if (row < p.Lq) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 w;
-                        w.x = pack_bf16x2(u2f(r[q4 * 8 + 0]) * inv, u2f(r[q4 * 8 + 1]) * inv);
-                        w.y = pack_bf16x2(u2f(r[q4 * 8 + 2]) * inv, u2f(r[q4 * 8 + 3]) * inv);
-                        w.z = pack_bf16x2(u2f(r[q4 * 8 + 4]) * inv, u2f(r[q4 * 8 + 5]) * inv);
-                        w.w = pack_bf16x2(u2f(r[q4 * 8 + 6]) * inv, u2f(r[q4 * 8 + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(sQi + swz_off(t, ch * 4 + q4)) = w;
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(u2f(r[q4 * 8 + 0]) * inv, u2f(r[q4 * 8 + 1]) * inv);
+                            w.y = pack_bf16x2(u2f(r[q4 * 8 + 2]) * inv, u2f(r[q4 * 8 + 3]) * inv);
+                            w.z = pack_bf16x2(u2f(r[q4 * 8 + 4]) * inv, u2f(r[q4 * 8 + 5]) * inv);
+                            w.w = pack_bf16x2(u2f(r[q4 * 8 + 6]) * inv, u2f(r[q4 * 8 + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(dst + ch * 32 + q4 * 8) = w;
+                        }
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(&bars->o_free[wg]);
-            } else {
+            } else if (row < p.Lq) {
+                __nv_bfloat16 *dst =
+                    PRENORM ? p.out + ((size_t)it.b * p.Lq + row) * (size_t)(p.H * D) + it.h * D
+                            : p.out + ((size_t)it.bh * p.Lq + row) * (size_t)D;
 #pragma unroll
                 for (int ch = 0; ch < D / 8; ++ch)
-                    *reinterpret_cast<uint4 *>(sQi + swz_off(t, ch)) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            if (!(ok = wg_sync())) break;
-            if (t == 0) {
-                if (q0i < p.Lq) {
-#pragma unroll
-                    for (int hh = 0; hh < NH; ++hh) {
-                        if (PRENORM)
-                            tma_store_3d(&p.tm_o, sQi + hh * kHalfBytes, it.h * D + hh * 64, q0i, it.b);
-                        else
-                            tma_store_3d(&p.tm_o, sQi + hh * kHalfBytes, hh * 64, q0i, it.bh);
-                    }
-                    tma_store_commit();
-                    tma_store_wait_read();
-                }
-                mbar_arrive(&bars->qfree[wg]);
+                    *reinterpret_cast<uint4 *>(dst + ch * 8) = make_uint4(0, 0, 0, 0);
             }
             c += n;
             e += n > 0 ? 1 : 0;
             ++k;
         }
-        if (t == 0) tma_store_wait_all();
         __syncwarp();
         tc_fence_before();
         named_barrier_arrive(1, kThreads);
@@ -764,6 +813,28 @@ CUresult encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_
 
 int g_grid_override = 0;
 
+// SM count and L2 size of the current device (cached per device).
+struct DeviceInfo {
+    int sms = 0;
+    int l2 = 0;
+};
+DeviceInfo device_info() {
+    constexpr int kMaxDevices = 64;
+    static DeviceInfo info[kMaxDevices];
+    static std::mutex lock;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return {148, 64 << 20};
+    std::lock_guard<std::mutex> guard(lock);
+    if (info[dev].sms == 0) {
+        int sms = 0, l2 = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+        info[dev].sms = sms > 0 ? sms : 148;
+        info[dev].l2 = l2 > 0 ? l2 : (64 << 20);
+    }
+    return info[dev];
+}
+
 template <int D, bool PRENORM>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
     constexpr size_t smem = Cfg<D>::kSmem;
@@ -774,8 +845,9 @@ cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    int grid = p.n_items;
-    if (g_grid_override > 0 && g_grid_override < grid) grid = g_grid_override;
+    // Persistent grid: one CTA per SM (one fits per SM), unless overridden.
+    int grid = g_grid_override > 0 ? g_grid_override : device_info().sms;
+    if (grid > p.n_items) grid = p.n_items;
     attn_fwd_bf16_kernel<D, PRENORM><<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
@@ -858,16 +930,11 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
         if (r == CUDA_SUCCESS)
             r = encode_bf16_3d(&p.tm_v, has_k ? c.v : c.out, c.D, has_k ? c.Lk : 1, has_k ? BH : 1);
     }
-    if (r == CUDA_SUCCESS) {
-        if (prenorm)
-            r = encode_bf16_3d(&p.tm_o, c.out, (uint64_t)c.H * c.D, c.Lq, c.B);
-        else
-            r = encode_bf16_3d(&p.tm_o, c.out, c.D, c.Lq, BH);
-    }
     if (r != CUDA_SUCCESS) {
         *driver_err = (int)r;
         return cudaErrorInvalidValue;
     }
+    p.out = reinterpret_cast<__nv_bfloat16 *>(c.out);
     p.ln_stats = ln_stats;
     p.gamma = c.gamma;
     p.beta = c.beta;
@@ -880,6 +947,15 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     p.scale_log2 = c.scale * 1.4426950408889634f;
     p.n_pairs = (c.Lq + 2 * kTileRows - 1) / (2 * kTileRows);
     p.n_items = (int)(BH * (uint64_t)p.n_pairs);
+    {
+        // (b, h) problems per scheduling group: their K and V together take
+        // at most half of L2.
+        const uint64_t kv_bytes = 4ull * (uint64_t)(c.Lk > 0 ? c.Lk : 1) * c.D;
+        uint64_t grp = (uint64_t)device_info().l2 / 2 / kv_bytes;
+        if (grp < 1) grp = 1;
+        if (grp > BH) grp = BH;
+        p.group = (int)grp;
+    }
     if (prenorm) {
         cudaError_t e = launch_ln_row_stats(c.x, ln_stats, (int64_t)c.B * c.Lq, c.H * c.D, c.eps,
                                             stream);

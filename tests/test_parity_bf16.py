@@ -134,3 +134,33 @@ def test_bf16_repeat_runs_bit_identical(D):
         assert torch.equal(out, ref)
     torch.cuda.synchronize()
     assert mha.device_status() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("ctas", [1, 3])
+def test_bf16_many_items_per_cta_mixed_work(D, ctas):
+    # Few CTAs walk many items: runs of items with no key tile (length 0),
+    # query tiles past Lq (no work for the second tile), and more key tiles
+    # than ring stages.  Exercises every hand-off between the roles; repeated
+    # because a hand-off race would show up only now and then.
+    B, H, L = 5, 2, 300
+    q = randn((B, H, L, D), 41, 1.0, torch.bfloat16)
+    k = randn((B, H, L, D), 42, 1.0, torch.bfloat16)
+    v = randn((B, H, L, D), 43, 1.0, torch.bfloat16)
+    lens = [0, 0, 300, 1, 129]
+    lt = dev(lens_tensor(lens))
+    dq, dk, dv = dev(q), dev(k), dev(v)
+    try:
+        mha.set_bf16_grid(0)
+        ref = mha.mha_fwd(dq, dk, dv, 3, lt)
+        mha.set_bf16_grid(ctas)
+        for _ in range(10):
+            out = mha.mha_fwd(dq, dk, dv, 3, lt)
+            torch.cuda.synchronize()
+            assert mha.device_status() == 0
+            assert torch.equal(out, ref)
+    finally:
+        mha.set_bf16_grid(0)
+    want = oracle.mha_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), 3, lens)
+    check_bf16(as_np(out), want, "many items D=%d ctas=%d" % (D, ctas))
