@@ -92,7 +92,7 @@ struct __align__(8) Bars {
     uint64_t q_full[2];   // Pre-LN: tile normalised -> MMA
     uint64_t qfree[2];    // Q tile i free: MMA issuer (last QK^T done) + each warp of WG i
     uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
-    uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+    uint64_t s_full[2], p_full[2], o_full[2], o_free[2];   // p_full, o_free: one arrival per warp
     uint64_t wg_bar[2];   // bounded barrier of each softmax warpgroup
     uint64_t drain;       // teardown after an abort
     uint32_t tmem_base;
@@ -303,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->q_full[i], 1);
             mbar_init(&bars->qfree[i], 1 + kWgThreads / 32);   // issuer + each softmax warp
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->p_full[i], kWgThreads);
+            mbar_init(&bars->p_full[i], kWgThreads / 32);     // one arrival per warp
             mbar_init(&bars->o_full[i], 1);
-            mbar_init(&bars->o_free[i], kWgThreads);
+            mbar_init(&bars->o_free[i], kWgThreads / 32);
             mbar_init(&bars->wg_bar[i], kWgThreads);
         }
         for (int s = 0; s < S; ++s) {
@@ -364,7 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // buffers the previous item may still be reading.
                 const int pre = min(it.J, S);
                 for (int j = 0; ok && j < pre; ++j) ok = load_kv(it, j);
-                for (int i = 0; ok && i < 2; ++i) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    if (!ok) break;
                     if (k > 0) ok = mbar_wait(&bars->qfree[i], (k - 1) & 1, kSiteQEmpty, abort);
                     if (!ok) break;
                     q_pending[i] = -1;
@@ -402,47 +404,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);   // Q K-major, K K-major
-            constexpr uint32_t idPV = idesc_bf16_f32(128, D, 0, 1);    // P (TMEM), V N-major
-            // Base descriptors, built once.  A K-step, a tile or a stage moves only
-            // the start-address field in the low word (addresses < 256 KB: no carry).
-            const uint64_t dq = desc_kmajor(smem_u32(sQ), 0);
-            const uint64_t dk = desc_kmajor(smem_u32(sK), 0);
-            const uint64_t dv = desc_mnmajor(smem_u32(sV), 0);
-            const uint32_t q_lo = (uint32_t)dq, q_hi = (uint32_t)(dq >> 32);
-            const uint32_t k_lo = (uint32_t)dk, k_hi = (uint32_t)(dk >> 32);
-            const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
-            constexpr uint32_t kTileUnits = TILE >> 4;           // one tile, in 16-byte units
-            uint32_t g = 0, k = 0, c[2] = {0, 0}, e[2] = {0, 0};
-            bool ok = true;
-            ItemIter iter;
-            while (ok && iter.next(p.n_items)) {
-                const Item it = decode_item(p, iter.idx);
-                // Every item passes through both Q barriers, with or without work
-                // for the tile, so no role can run two phases ahead of another.
-                for (int i = 0; ok && i < 2; ++i) {
-                    ok = mbar_wait(PRENORM ? &bars->q_full[i] : &bars->q_raw[i], k & 1, kSiteQFull,
-                                   abort);
-                    if (ok && it.n[i] == 0) mbar_arrive(&bars->qfree[i]);   // tile never read
+        // The whole warp walks the schedule: every value is warp-uniform, every
+        // wait's outcome is shared by all lanes, and one elected lane (the same
+        // one each time, the warp being converged) issues each MMA and commit.
+        constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);   // Q K-major, K K-major
+        constexpr uint32_t idPV = idesc_bf16_f32(128, D, 0, 1);    // P (TMEM), V N-major
+        // Base descriptors, built once.  A K-step, a tile or a stage moves only
+        // the start-address field in the low word (addresses < 256 KB: no carry).
+        const uint64_t dq = desc_kmajor(smem_u32(sQ), 0);
+        const uint64_t dk = desc_kmajor(smem_u32(sK), 0);
+        const uint64_t dv = desc_mnmajor(smem_u32(sV), 0);
+        const uint32_t q_lo = (uint32_t)dq, q_hi = (uint32_t)(dq >> 32);
+        const uint32_t k_lo = (uint32_t)dk, k_hi = (uint32_t)(dk >> 32);
+        const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
+        constexpr uint32_t kTileUnits = TILE >> 4;           // one tile, in 16-byte units
+        uint32_t g = 0, k = 0, c[2] = {0, 0}, e[2] = {0, 0};
+        bool ok = true;
+        auto wwait = [&](uint64_t *bar, uint32_t parity, uint32_t site) -> bool {
+            const bool r = mbar_wait(bar, parity, site, abort);
+            return __all_sync(0xffffffffu, r);
+        };
+        ItemIter iter;
+        while (ok && iter.next(p.n_items)) {
+            const Item it = decode_item(p, iter.idx);
+            // Every item passes through both Q barriers, with or without work
+            // for the tile, so no role can run two phases ahead of another.
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                if (!ok) break;
+                ok = wwait(PRENORM ? &bars->q_full[i] : &bars->q_raw[i], k & 1, kSiteQFull);
+                if (ok && it.n[i] == 0) {
+                    if (elect_one()) mbar_arrive(&bars->qfree[i]);   // tile never read
+                    __syncwarp();
                 }
-                if (ok && it.J > 0) {
-                    const uint32_t g0 = g;
-                    int k_ready = -1;   // key tiles [0, k_ready] of this item have landed
-                    auto wait_k = [&](int j) -> bool {
-                        if (j <= k_ready) return true;
-                        const uint32_t gg = g0 + j;
-                        if (!mbar_wait(&bars->k_full[gg % S], (gg / S) & 1, kSiteKFull, abort))
-                            return false;
-                        k_ready = j;
-                        return true;
-                    };
-                    // S_i(j) = Q_i K_j^T into TMEM columns [128 i, 128 i + 128).  After
-                    // the last QK^T of the item, the Q tile is released (qfree).
-                    auto issue_s = [&](int i, int j) {
-                        const uint32_t st = (g0 + j) % S;
-                        const uint32_t a0 = q_lo + i * kTileUnits, b0 = k_lo + st * kTileUnits;
-                        tc_fence_after();
+            }
+            if (ok && it.J > 0) {
+                const uint32_t g0 = g;
+                int k_ready = -1;   // key tiles [0, k_ready] of this item have landed
+                auto wait_k = [&](int j) -> bool {
+                    if (j <= k_ready) return true;
+                    const uint32_t gg = g0 + j;
+                    if (!wwait(&bars->k_full[gg % S], (gg / S) & 1, kSiteKFull)) return false;
+                    k_ready = j;
+                    return true;
+                };
+                // S_i(j) = Q_i K_j^T into TMEM columns [128 i, 128 i + 128).  After
+                // the last QK^T of the item, the Q tile is released (qfree).
+                auto issue_s = [&](int i, int j) {
+                    const uint32_t st = (g0 + j) % S;
+                    const uint32_t a0 = q_lo + i * kTileUnits, b0 = k_lo + st * kTileUnits;
+                    tc_fence_after();
+                    if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             // K-step kk: 64-column half kk/4, 32 bytes per step inside it.
@@ -453,51 +465,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         umma_commit(&bars->s_full[i]);
                         if (j + 1 == it.n[i]) umma_commit(&bars->qfree[i]);
-                    };
-                    for (int i = 0; ok && i < 2; ++i)
-                        if (it.n[i] > 0) {
-                            ok = wait_k(0);
-                            if (ok) issue_s(i, 0);
-                        }
-                    for (int j = 0; ok && j < it.J; ++j) {
-                        const uint32_t gj = g0 + j, st = gj % S;
-                        bool v_ready = false;
-                        for (int i = 0; ok && i < 2; ++i) {
-                            if (j >= it.n[i]) continue;
-                            ok = mbar_wait(&bars->p_full[i], (c[i] + j) & 1, kSitePFull, abort);
-                            if (ok && !v_ready)
-                                ok = v_ready =
-                                    mbar_wait(&bars->v_full[st], (gj / S) & 1, kSiteVFull, abort);
-                            if (ok && j == 0 && e[i] > 0)
-                                ok = mbar_wait(&bars->o_free[i], (e[i] - 1) & 1, kSiteOFree, abort);
-                            if (!ok) break;
-                            tc_fence_after();
-                            // O_i (+)= P_i V_j, P_i read from TMEM.
-                            const uint32_t dO = tmem + C::kColO0 + i * D;
-                            const uint32_t aP = tmem + C::kColP0 + i * C::kColPStep;
-                            const uint32_t vb = v_lo + st * kTileUnits;
-                            const uint32_t acc0 = j > 0 ? 1u : 0u;
+                    }
+                    __syncwarp();
+                };
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    if (ok && it.n[i] > 0) {
+                        ok = wait_k(0);
+                        if (ok) issue_s(i, 0);
+                    }
+                for (int j = 0; ok && j < it.J; ++j) {
+                    const uint32_t gj = g0 + j, st = gj % S;
+                    bool v_ready = false;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        if (!ok) break;
+                        if (j >= it.n[i]) continue;
+                        ok = wwait(&bars->p_full[i], (c[i] + j) & 1, kSitePFull);
+                        if (ok && !v_ready)
+                            ok = v_ready = wwait(&bars->v_full[st], (gj / S) & 1, kSiteVFull);
+                        if (ok && j == 0 && e[i] > 0)
+                            ok = wwait(&bars->o_free[i], (e[i] - 1) & 1, kSiteOFree);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // O_i (+)= P_i V_j, P_i read from TMEM.
+                        const uint32_t dO = tmem + C::kColO0 + i * D;
+                        const uint32_t aP = tmem + C::kColP0 + i * C::kColPStep;
+                        const uint32_t vb = v_lo + st * kTileUnits;
+                        const uint32_t acc0 = j > 0 ? 1u : 0u;
+                        const bool last = j + 1 >= it.n[i];
+                        if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < kTileRows / 16; ++kk)   // 16 keys = 2048 B of V
                                 umma_ts_w(dO, aP + kk * 8, vb + kk * (2048 >> 4), v_hi, idPV,
                                           kk > 0 ? 1u : acc0);
-                            if (j + 1 < it.n[i]) {
-                                ok = wait_k(j + 1);
-                                if (ok) issue_s(i, j + 1);
-                            } else {
-                                umma_commit(&bars->o_full[i]);
-                            }
+                            if (last) umma_commit(&bars->o_full[i]);
                         }
-                        if (ok) umma_commit(&bars->kv_empty[st]);
+                        __syncwarp();
+                        if (!last) {
+                            ok = wait_k(j + 1);
+                            if (ok) issue_s(i, j + 1);
+                        }
                     }
-                    g = g0 + it.J;
-                    for (int i = 0; i < 2; ++i) {
-                        c[i] += it.n[i];
-                        e[i] += it.n[i] > 0 ? 1 : 0;
+                    if (ok) {
+                        if (elect_one()) umma_commit(&bars->kv_empty[st]);
+                        __syncwarp();
                     }
                 }
-                ++k;
+                g = g0 + it.J;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    c[i] += it.n[i];
+                    e[i] += it.n[i] > 0 ? 1 : 0;
+                }
             }
+            ++k;
         }
     }
     // ------------------------------- teardown --------------------------------
@@ -508,8 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) {
         tc_fence_after();
         if (*abort) {
-            // Let MMAs still in flight finish before the columns are released.
-            if (lane == 0) {
+            // Let MMAs still in flight finish before the columns are released
+            // (the commit comes from the lane that issued them).
+            if (elect_one()) {
                 volatile int no_abort = 0;
                 umma_commit(&bars->drain);
                 mbar_wait(&bars->drain, 0, kSiteDrain, &no_abort);
@@ -547,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ItemIter iter;
         while (ok && iter.next(p.n_items)) {
             const Item it = decode_item(p, iter.idx);
-            const int n = it.n[wg];
+            const int n = wg ? it.n[1] : it.n[0];
             const int q0i = it.q0 + wg * kTileRows;
             const int row = q0i + t;
             ok = wwait(&bars->q_raw[wg], k & 1, kSiteQFull);
@@ -567,6 +590,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // slower warp of the same warpgroup.
             if (lane == 0) mbar_arrive(&bars->qfree[wg]);
             const int vis_end = p.causal ? min(it.len, row + 1) : it.len;
+            // Key tiles from j_edge on may hide keys from some rows of this tile
+            // (the causal diagonal, the valid-length end); earlier ones hide none.
+            // The same for the whole warpgroup, so the test is a uniform branch.
+            const int j_edge = min(p.causal ? q0i / kTileRows : n, it.len / kTileRows);
+            const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
                 ok = wwait(&bars->s_full[wg], (c + j) & 1, kSiteSFull);
@@ -574,21 +602,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 uint32_t s[kTileRows];
                 tmem_ld128(tS, s);
-                const int lim = vis_end - j * kTileRows;   // visible keys of this row in the tile
-                if (lim < kTileRows) {
+                if (j >= j_edge) {
+                    const int lim = vis_end - j * kTileRows;   // visible keys of this row in the tile
 #pragma unroll
                     for (int cc = 0; cc < kTileRows; ++cc)
                         if (cc >= lim) s[cc] = f2u(-INFINITY);
                 }
-                float mx0 = u2f(s[0]), mx1 = u2f(s[1]), mx2 = u2f(s[2]), mx3 = u2f(s[3]);
+                // Row max: eight independent chains of three-input max.
+                float mx[8];
 #pragma unroll
-                for (int cc = 4; cc < kTileRows; cc += 4) {
-                    mx0 = fmaxf(mx0, u2f(s[cc]));
-                    mx1 = fmaxf(mx1, u2f(s[cc + 1]));
-                    mx2 = fmaxf(mx2, u2f(s[cc + 2]));
-                    mx3 = fmaxf(mx3, u2f(s[cc + 3]));
-                }
-                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+                for (int q = 0; q < 8; ++q) mx[q] = u2f(s[q]);
+#pragma unroll
+                for (int cc = 8; cc < kTileRows; cc += 16)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) mx[q] = max3f(mx[q], u2f(s[cc + q]), u2f(s[cc + 8 + q]));
+                const float m_tile = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
+                                           fmaxf(mx[6], mx[7])) * p.scale_log2;
                 const bool need = m_tile > m_used + kRescaleThreshold;
                 float alpha = 1.f;
                 if (need) {
@@ -596,17 +625,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_used = m_tile;
                 }
                 const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-                float rs0 = 0.f, rs1 = 0.f;
+                // p = 2^(s * scale_log2 - m): paired fp32 FMA and adds (two lanes per
+                // instruction) around the hardware exponential; four partial sums.
                 // P overwrites the low half of s as packed bf16 pairs.
+                const float2 nm2 = make_float2(-msub, -msub);
+                float2 acc[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int cc = 0; cc < kTileRows; cc += 2) {
-                    const float e0 = ex2_approx(fmaf(u2f(s[cc]), p.scale_log2, -msub));
-                    const float e1 = ex2_approx(fmaf(u2f(s[cc + 1]), p.scale_log2, -msub));
-                    rs0 += e0;
-                    rs1 += e1;
-                    s[cc >> 1] = pack_bf16x2(e0, e1);
+                    float2 x = __ffma2_rn(make_float2(u2f(s[cc]), u2f(s[cc + 1])), scale2, nm2);
+                    x.x = ex2_approx(x.x);
+                    x.y = ex2_approx(x.y);
+                    acc[(cc >> 1) & 3] = __fadd2_rn(acc[(cc >> 1) & 3], x);
+                    s[cc >> 1] = pack_bf16x2(x.x, x.y);
                 }
-                l = fmaf(l, alpha, rs0 + rs1);
+                const float2 rs = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+                l = fmaf(l, alpha, rs.x + rs.y);
                 // The commit behind s_full covers the previous P.V, so O is at rest.
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -621,7 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st64(tP, *reinterpret_cast<uint32_t(*)[64]>(s));
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bars->p_full[wg]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->p_full[wg]);
             }
             if (!ok) break;
 
@@ -642,7 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tO + ch * 32, r);
                     if (ch == D / 32 - 1) {
                         tc_fence_before();
-                        mbar_arrive(&bars->o_free[wg]);   // O of this tile has been read
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->o_free[wg]);   // O of this tile has been read
                     }
                     if (row < p.Lq) {
 #pragma unroll

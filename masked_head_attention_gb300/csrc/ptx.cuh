@@ -340,6 +340,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction (sm_100+ three-input form).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// True in exactly one lane of a converged warp (the lowest lane of the full
+// mask, so the same lane every time the warp is converged).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Pack two floats to bf16x2 (round to nearest even): `lo` goes to bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
