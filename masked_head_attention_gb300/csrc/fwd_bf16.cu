@@ -74,6 +74,7 @@ struct AttnParams {
     CUtensorMap tm_q;     // Q [B*H][Lq][D]; Pre-LN: x [B][Lq][H*D]; box {64, 128, 1}
     CUtensorMap tm_k;     // K [B*H][Lk][D]
     CUtensorMap tm_v;     // V [B*H][Lk][D]
+    CUtensorMap tm_o;     // O, same layout as the output; box {64, 32, 1} (one warp's rows)
     __nv_bfloat16 *out;   // [B*H][Lq][D], or [B][Lq][H*D] for Pre-LN
     const float2 *ln_stats;      // Pre-LN: (mean, 1/sqrt(var + eps)) per row of x, [B*Lq]
     const float *gamma;
@@ -104,10 +105,14 @@ struct Cfg {
     static constexpr int NH = D / 64;                      // 64-column halves per tile
     static constexpr uint32_t kTile = NH * kHalfBytes;     // one 128 x D bf16 tile
     static constexpr int kStages = D == 64 ? 3 : 2;        // K/V ring depth
-    static constexpr uint32_t kQ = 0;                      // two Q tiles; also O staging
+    static constexpr uint32_t kQ = 0;                      // two Q tiles
     static constexpr uint32_t kK = 2 * kTile;
     static constexpr uint32_t kV = kK + kStages * kTile;
-    static constexpr uint32_t kBars = kV + kStages * kTile;
+    // O staging: one 32-row x 64-column bf16 slice (4 KB, 128-byte swizzle)
+    // per softmax warp, stored to global memory by TMA.
+    static constexpr uint32_t kStageWarp = 32 * 128;
+    static constexpr uint32_t kO = kV + kStages * kTile;
+    static constexpr uint32_t kBars = kO + 8 * kStageWarp;
     static constexpr size_t kSmem = 1024 + kBars + sizeof(Bars);
     static constexpr uint32_t kColO0 = 256;                // O_i at 256 + i * D; S_i at i * 128
     // P_i (bf16 pairs, 64 columns): in its own columns when D = 64 leaves
@@ -321,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_o);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -481,11 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 2; ++i) {
                         if (!ok) break;
                         if (j >= it.n[i]) continue;
-                        ok = wwait(&bars->p_full[i], (c[i] + j) & 1, kSitePFull);
-                        if (ok && !v_ready)
+                        // V_j and a free O_i normally arrived long ago; P_i(j) is the
+                        // wait that matters, so it comes last, right before the MMAs.
+                        if (!v_ready)
                             ok = v_ready = wwait(&bars->v_full[st], (gj / S) & 1, kSiteVFull);
                         if (ok && j == 0 && e[i] > 0)
                             ok = wwait(&bars->o_free[i], (e[i] - 1) & 1, kSiteOFree);
+                        if (ok) ok = wwait(&bars->p_full[i], (c[i] + j) & 1, kSitePFull);
                         if (!ok) break;
                         tc_fence_after();
                         // O_i (+)= P_i V_j, P_i read from TMEM.
@@ -551,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + C::kColO0 + wg * D;
         const uint32_t tP = tmem + lane_off + C::kColP0 + wg * C::kColPStep;
         uint8_t *sQi = sQ + wg * TILE;
+        uint8_t *sOw = base + C::kO + (warp & 7) * C::kStageWarp;   // this warp's O slice
         uint32_t k = 0, c = 0, e = 0, wgp = 0;
         bool ok = true;
         // Waits whose outcome the whole warp shares, so warp-collective
@@ -662,35 +671,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             // ------------------------------- epilogue -------------------------------
-            // O / l as bf16, written once: row t of the tile is one contiguous
-            // run of D values (16-byte stores); rows past Lq are not written.
+            // O / l as bf16, written once.  Each warp stages its 32 rows, 64
+            // columns at a time, in its own swizzled slice and stores the slice
+            // with one TMA store (rows past Lq are clipped by the unit).
             if (n > 0) {
                 ok = wwait(&bars->o_full[wg], e & 1, kSitePvDone);
                 if (!ok) break;
                 tc_fence_after();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                __nv_bfloat16 *dst =
-                    PRENORM ? p.out + ((size_t)it.b * p.Lq + row) * (size_t)(p.H * D) + it.h * D
-                            : p.out + ((size_t)it.bh * p.Lq + row) * (size_t)D;
+                const int row0 = q0i + 32 * (warp & 3);   // first row of this warp's slice
 #pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + ch * 32, r);
-                    if (ch == D / 32 - 1) {
+                for (int hh = 0; hh < NH; ++hh) {
+                    uint32_t r[64];
+                    tmem_ld32(tO + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    tmem_ld32(tO + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    if (hh == NH - 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars->o_free[wg]);   // O of this tile has been read
                     }
-                    if (row < p.Lq) {
+                    // The slice's previous store has finished reading it.
+                    if (lane == 0) tma_store_wait_read();
+                    __syncwarp();
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 w;
-                            w.x = pack_bf16x2(u2f(r[q4 * 8 + 0]) * inv, u2f(r[q4 * 8 + 1]) * inv);
-                            w.y = pack_bf16x2(u2f(r[q4 * 8 + 2]) * inv, u2f(r[q4 * 8 + 3]) * inv);
-                            w.z = pack_bf16x2(u2f(r[q4 * 8 + 4]) * inv, u2f(r[q4 * 8 + 5]) * inv);
-                            w.w = pack_bf16x2(u2f(r[q4 * 8 + 6]) * inv, u2f(r[q4 * 8 + 7]) * inv);
-                            *reinterpret_cast<uint4 *>(dst + ch * 32 + q4 * 8) = w;
-                        }
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        uint4 w;
+                        w.x = pack_bf16x2(u2f(r[c8 * 8 + 0]) * inv, u2f(r[c8 * 8 + 1]) * inv);
+                        w.y = pack_bf16x2(u2f(r[c8 * 8 + 2]) * inv, u2f(r[c8 * 8 + 3]) * inv);
+                        w.z = pack_bf16x2(u2f(r[c8 * 8 + 4]) * inv, u2f(r[c8 * 8 + 5]) * inv);
+                        w.w = pack_bf16x2(u2f(r[c8 * 8 + 6]) * inv, u2f(r[c8 * 8 + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(sOw + lane * 128 + ((c8 ^ (lane & 7)) << 4)) = w;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < p.Lq) {
+                        if (PRENORM)
+                            tma_store_3d(&p.tm_o, sOw, it.h * D + hh * 64, row0, it.b);
+                        else
+                            tma_store_3d(&p.tm_o, sOw, hh * 64, row0, it.bh);
+                        tma_store_commit();
                     }
                 }
             } else if (row < p.Lq) {
@@ -705,6 +724,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             e += n > 0 ? 1 : 0;
             ++k;
         }
+        // Output stores must finish before the CTA's shared memory is released.
+        if (lane == 0) tma_store_wait_all();
         __syncwarp();
         tc_fence_before();
         named_barrier_arrive(1, kThreads);
@@ -833,15 +854,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 3-D bf16 tensor map over a dense [d2][d1][d0] array with a {64, 128, 1} box
-// and the 128-byte swizzle; rows outside the array read as zero.
+// 3-D bf16 tensor map over a dense [d2][d1][d0] array with a {64, box_rows, 1}
+// box and the 128-byte swizzle; rows outside the array read as zero (loads)
+// or are not written (stores).
 CUresult encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
-                        uint64_t d2) {
+                        uint64_t d2, uint32_t box_rows = 128) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return CUDA_ERROR_NOT_SUPPORTED;
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -966,6 +988,12 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
         r = encode_bf16_3d(&p.tm_k, has_k ? c.k : c.out, c.D, has_k ? c.Lk : 1, has_k ? BH : 1);
         if (r == CUDA_SUCCESS)
             r = encode_bf16_3d(&p.tm_v, has_k ? c.v : c.out, c.D, has_k ? c.Lk : 1, has_k ? BH : 1);
+    }
+    if (r == CUDA_SUCCESS) {
+        if (prenorm)
+            r = encode_bf16_3d(&p.tm_o, c.out, (uint64_t)c.H * c.D, c.Lq, c.B, 32);
+        else
+            r = encode_bf16_3d(&p.tm_o, c.out, c.D, c.Lq, BH, 32);
     }
     if (r != CUDA_SUCCESS) {
         *driver_err = (int)r;
