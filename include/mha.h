@@ -170,12 +170,23 @@ MHA_API int mha_selftest_umma(int variant, int K_or_N, const void *a, const void
                       float *c, cudaStream_t stream);
 
 /*
- * mha_set_bf16_grid -- launch-shape hook for benchmarks: cap the bf16
- * kernels' grid at `ctas` CTAs, each then loops over several work items
- * (persistent scheduling); 0 restores one CTA per work item.  Affects later
+ * mha_set_bf16_grid -- launch-shape hook for tests and benchmarks: run the
+ * persistent bf16 kernels on `ctas` CTAs (each loops over its share of the
+ * work items); 0 restores the default of one CTA per SM.  Affects later
  * calls from any thread of the process.
  */
 MHA_API void mha_set_bf16_grid(int ctas);
+
+/*
+ * mha_set_f32_kernel -- kernel-choice hook for tests and benchmarks of the
+ * fp32 path.  0 = automatic: the short-key-range kernel (every visible K/V
+ * row of a 16-row query block staged in shared memory at once) when
+ * Lk * D <= 16384, else the tiled kernel (64-row query tiles, 64-key K/V
+ * tiles); 1 = always the tiled kernel; 2 = the short-key-range kernel
+ * whenever Lk * D <= 16384.  Other values act as 0.  Affects later calls
+ * from any thread of the process.
+ */
+MHA_API void mha_set_f32_kernel(int which);
 
 #ifdef __cplusplus
 }

@@ -56,24 +56,38 @@ def lib():
         L.mha_selftest_umma.restype = i
         L.mha_set_bf16_grid.argtypes = [i]
         L.mha_set_bf16_grid.restype = None
+        L.mha_set_f32_kernel.argtypes = [i]
+        L.mha_set_f32_kernel.restype = None
         _lib = L
     return _lib
 
 
+_torch_mod = None
+_raw_stream = None
+
+
 def _torch():
-    import torch
-    return torch
+    global _torch_mod, _raw_stream
+    if _torch_mod is None:
+        import torch
+        _torch_mod = torch
+        # The raw handle of the current stream without building a Stream object
+        # (a few microseconds per call otherwise).
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    return _torch_mod
 
 
-def _stream(stream):
+def _stream(stream, device_index=None):
     torch = _torch()
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device() if device_index is None else device_index)
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _dev(t, name, dtype=None):
@@ -122,7 +136,8 @@ def mha_fwd(q, k, v, mask_kind=MASK_NONE, kv_lengths=None, out=None, scale=None,
         _dev(out, "out", q.dtype)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     _check(lib().mha_fwd(_ptr(q), _ptr(k), _ptr(v), int(mask_kind), _ptr(kv_lengths), _ptr(out),
-                         B, H, Lq, Lk, D, scale, _dtype_code(q), _stream(stream)), "mha_fwd")
+                         B, H, Lq, Lk, D, scale, _dtype_code(q), _stream(stream, q.get_device())),
+           "mha_fwd")
     return out
 
 
@@ -151,7 +166,8 @@ def prenorm_cross_attn_fwd(x_q, gamma, beta, eps, k, v, kv_lengths=None, out=Non
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     _check(lib().prenorm_cross_attn_fwd(_ptr(x_q), _ptr(gamma), _ptr(beta), float(eps), _ptr(k),
                                         _ptr(v), _ptr(kv_lengths), _ptr(out), B, H, Lq, Lk, D,
-                                        scale, BF16, _stream(stream)), "prenorm_cross_attn_fwd")
+                                        scale, BF16, _stream(stream, x_q.get_device())),
+           "prenorm_cross_attn_fwd")
     return out
 
 
@@ -175,6 +191,11 @@ def selftest_umma(variant, kn, a, b, c, stream=None):
 
 def set_bf16_grid(ctas):
     lib().mha_set_bf16_grid(int(ctas))
+
+
+def set_f32_kernel(which):
+    """0 automatic, 1 tiled kernel only, 2 short-key-range kernel where it applies."""
+    lib().mha_set_f32_kernel(int(which))
 
 
 def prenorm_cross_attn_fwd_noalloc(x_q, gamma, beta, eps, k, v, kv_lengths=None, out=None,
@@ -210,6 +231,6 @@ def prenorm_cross_attn_fwd_noalloc(x_q, gamma, beta, eps, k, v, kv_lengths=None,
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     _check(L.prenorm_cross_attn_fwd_noalloc(_ptr(x_q), _ptr(gamma), _ptr(beta), float(eps),
                                             _ptr(k), _ptr(v), _ptr(kv_lengths), _ptr(out), B, H,
-                                            Lq, Lk, D, scale, BF16, _stream(stream)),
+                                            Lq, Lk, D, scale, BF16, _stream(stream, x_q.get_device())),
            "prenorm_cross_attn_fwd_noalloc")
     return out

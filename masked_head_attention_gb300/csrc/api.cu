@@ -185,4 +185,6 @@ int mha_selftest_umma(int variant, int K_or_N, const void *a, const void *b, flo
 // 0 restores one CTA per work item.
 void mha_set_bf16_grid(int ctas) { mha::set_bf16_grid_override(ctas); }
 
+void mha_set_f32_kernel(int which) { mha::set_f32_kernel_override(which); }
+
 }  // extern "C"

@@ -224,6 +224,286 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Short key ranges (Lk * D <= 16384): a CTA of 4 warps owns 16 query rows of
+// one (b, h) and stages every key row any of them can see, K and V, in shared
+// memory once (cp.async; S starts as soon as K has landed, while V is still
+// in flight).  There is no key-tile loop.  Warp w owns rows 4w..4w+3: for S
+// each lane takes keys lane, lane + 32, ... (every key block advances through
+// D together: 4 x blocks independent chains); for P.V each lane takes D/32
+// output columns, with even and odd keys in separate accumulators.  P goes
+// through shared memory as [key][4 rows], one broadcast 16-byte load per key.
+// Many small CTAs, latest (heaviest under a causal mask) query blocks first,
+// replace a few long serial ones when B * H * Lq is small.
+// ---------------------------------------------------------------------------
+constexpr int kSmallRows = 16;
+constexpr int kSmallR = 4;                               // query rows per warp (2 or 4)
+constexpr int kSmallWarps = kSmallRows / kSmallR;
+constexpr int kSmallThreads = 32 * kSmallWarps;
+constexpr int kSmallMaxKD = 16384;   // Lk * D limit (K and V: 2 x 64 KB + padding)
+
+template <int D>
+struct SmallCfg {
+    static constexpr int LDK = D + 4;                 // padded K row (conflict-free 16-byte loads)
+    static constexpr int kMaxKeys = kSmallMaxKD / D;  // 256 (D = 64) or 128 (D = 128)
+    static constexpr int KB = kMaxKeys / 32;          // key blocks of 32 per lane
+    static size_t smem(int keys) {
+        return sizeof(float) * ((size_t)keys * LDK + (size_t)keys * D + kSmallRows * D +
+                                (size_t)kSmallWarps * keys * kSmallR);
+    }
+};
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Q.K for the warp's R query rows against keys kb*32 + lane, kb < NKB.
+template <int D, int NKB, int KB>
+__device__ __forceinline__ void small_scores(const float *sK, const float *Qw, int lane,
+                                             float (&s)[kSmallR][KB]) {
+    constexpr int LDK = SmallCfg<D>::LDK;
+#pragma unroll 2
+    for (int d = 0; d < D; d += 4) {
+        float4 qq[kSmallR];
+#pragma unroll
+        for (int r = 0; r < kSmallR; ++r) qq[r] = *reinterpret_cast<const float4 *>(Qw + r * D + d);
+#pragma unroll
+        for (int kb = 0; kb < NKB; ++kb) {
+            const float4 kk = *reinterpret_cast<const float4 *>(sK + (kb * 32 + lane) * LDK + d);
+#pragma unroll
+            for (int r = 0; r < kSmallR; ++r) {
+                s[r][kb] = fmaf(qq[r].x, kk.x, s[r][kb]);
+                s[r][kb] = fmaf(qq[r].y, kk.y, s[r][kb]);
+                s[r][kb] = fmaf(qq[r].z, kk.z, s[r][kb]);
+                s[r][kb] = fmaf(qq[r].w, kk.w, s[r][kb]);
+            }
+        }
+    }
+}
+
+// acc[r][c] += P[key][r] * V[key][lane*DC + c] for the warp's rows.
+template <int D>
+__device__ __forceinline__ void small_pv_key(const float *Pw, const float *Vl, int key,
+                                             float (&acc)[kSmallR][D / 32]) {
+    constexpr int DC = D / 32;
+    static_assert(kSmallR == 2 || kSmallR == 4, "P is read as one float2 / float4 per key");
+    float pp[kSmallR];
+    if (kSmallR == 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(Pw + key * kSmallR);
+        pp[0] = t.x;
+        pp[1] = t.y;
+        pp[kSmallR - 2] = t.z;
+        pp[kSmallR - 1] = t.w;
+    } else {
+        const float2 t = *reinterpret_cast<const float2 *>(Pw + key * kSmallR);
+        pp[0] = t.x;
+        pp[1] = t.y;
+    }
+    float vv[DC];
+    if (DC == 2) {
+        const float2 t = *reinterpret_cast<const float2 *>(Vl + (size_t)key * D);
+        vv[0] = t.x;
+        vv[1] = t.y;
+    } else {
+        const float4 t = *reinterpret_cast<const float4 *>(Vl + (size_t)key * D);
+        vv[0] = t.x;
+        vv[1] = t.y;
+        vv[DC - 2] = t.z;
+        vv[DC - 1] = t.w;
+    }
+#pragma unroll
+    for (int c = 0; c < DC; ++c)
+#pragma unroll
+        for (int r = 0; r < kSmallR; ++r) acc[r][c] = fmaf(pp[r], vv[c], acc[r][c]);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kSmallThreads, 2)
+    mha_fwd_f32_small_kernel(const float *__restrict__ q, const float *__restrict__ k,
+                             const float *__restrict__ v, const int32_t *__restrict__ kv_lengths,
+                             float *__restrict__ out, int H, int Lq, int Lk, int mask_kind,
+                             float scale_log2, int keys_cap) {
+    using C = SmallCfg<D>;
+    constexpr int DC = D / 32;   // output columns per lane
+    constexpr int R = kSmallR;
+    extern __shared__ float4 small_smem[];
+    float *sK = reinterpret_cast<float *>(small_smem);   // [keys_cap][LDK]
+    float *sV = sK + (size_t)keys_cap * C::LDK;          // [keys_cap][D]
+    float *sQ = sV + (size_t)keys_cap * D;               // [16][D]
+    float *sP = sQ + kSmallRows * D;                     // [warps][keys_cap][R]
+
+    // Latest (for causal masks the heaviest) query blocks are launched first.
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int q0 = ((int)gridDim.x - 1 - (int)blockIdx.x) * kSmallRows;
+    const size_t bh = (size_t)b * H + h;
+    const float *Qg = q + bh * (size_t)Lq * D;
+    const float *Kg = k + bh * (size_t)Lk * D;
+    const float *Vg = v + bh * (size_t)Lk * D;
+    float *Og = out + bh * (size_t)Lq * D;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const bool causal = (mask_kind & 1) != 0;
+    int len = Lk;
+    if (mask_kind & 2) len = max(0, min((int)kv_lengths[b], Lk));
+    int kend = len;                                   // keys any row of the CTA can see
+    if (causal) kend = min(kend, q0 + kSmallRows);
+
+    constexpr int V4 = D / 4;
+    for (int idx = tid; idx < kend * V4; idx += kSmallThreads) {
+        const int r = idx / V4, c = idx % V4;
+        cp_async16(sK + r * C::LDK + 4 * c, Kg + (size_t)r * D + 4 * c);
+    }
+    cp_async_commit();
+    for (int idx = tid; idx < kend * V4; idx += kSmallThreads) {
+        const int r = idx / V4, c = idx % V4;
+        cp_async16(sV + r * D + 4 * c, Vg + (size_t)r * D + 4 * c);
+    }
+    cp_async_commit();
+    for (int idx = tid; idx < kSmallRows * V4; idx += kSmallThreads) {
+        const int r = idx / V4, c = idx % V4;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (q0 + r < Lq) val = __ldg(reinterpret_cast<const float4 *>(Qg + (size_t)(q0 + r) * D) + c);
+        *reinterpret_cast<float4 *>(sQ + r * D + 4 * c) = val;
+    }
+    cp_async_wait_group<1>();   // K has landed (V may still be in flight)
+    __syncthreads();
+
+    const int r0 = q0 + R * warp;                    // first row of this warp
+    int kw = len;                                    // keys any of the warp's rows can see
+    if (causal) kw = min(kw, r0 + R);
+    kw = max(kw, 0);
+    const int nkb = (kw + 31) / 32;
+    const float *Qw = sQ + R * warp * D;
+
+    // S for the warp's rows and keys kb*32 + lane.
+    float s[R][C::KB];
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+        for (int r = 0; r < R; ++r) s[r][kb] = 0.f;
+    switch (nkb) {
+#define MHA_SMALL_S_CASE(N)                                                              \
+    case N:                                                                              \
+        if (N <= C::KB) small_scores<D, (N <= C::KB ? N : 1), C::KB>(sK, Qw, lane, s);   \
+        break;
+        MHA_SMALL_S_CASE(1)
+        MHA_SMALL_S_CASE(2)
+        MHA_SMALL_S_CASE(3)
+        MHA_SMALL_S_CASE(4)
+        MHA_SMALL_S_CASE(5)
+        MHA_SMALL_S_CASE(6)
+        MHA_SMALL_S_CASE(7)
+        MHA_SMALL_S_CASE(8)
+#undef MHA_SMALL_S_CASE
+        default:
+            break;
+    }
+    // Mask, scale into base 2, row max / exp / row sum (warp shuffles).
+    float l[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int row = r0 + r;
+        const int vis_end = causal ? min(len, row + 1) : len;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb) {
+            const int key = kb * 32 + lane;
+            const float x = (kb < nkb && key < vis_end) ? s[r][kb] * scale_log2 : -INFINITY;
+            s[r][kb] = x;
+            mx = fmaxf(mx, x);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m = (mx == -INFINITY) ? 0.f : mx;
+        float sum = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb) {
+            const float pj = ex2_approx(s[r][kb] - m);
+            s[r][kb] = pj;
+            sum += pj;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        l[r] = sum;
+    }
+    float *Pw = sP + (size_t)warp * keys_cap * R;
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb)
+        if (kb < nkb)
+        {
+            float *dst = Pw + (kb * 32 + lane) * R;
+            if (R == 4)
+                *reinterpret_cast<float4 *>(dst) =
+                    make_float4(s[0][kb], s[1][kb], s[R - 2][kb], s[R - 1][kb]);
+            else
+                *reinterpret_cast<float2 *>(dst) = make_float2(s[0][kb], s[1][kb]);
+        }
+    cp_async_wait_group<0>();   // V has landed
+    __syncthreads();
+
+    // O = P V for the warp's rows, lane's columns lane*DC .. lane*DC + DC - 1;
+    // even and odd keys go to separate accumulators (two chains per output).
+    float o[2][R][DC];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < DC; ++c) o[h2][r][c] = 0.f;
+    const float *Vl = sV + lane * DC;
+    int key = 0;
+#pragma unroll 4
+    for (; key + 1 < kw; key += 2) {
+        small_pv_key<D>(Pw, Vl, key, o[0]);
+        small_pv_key<D>(Pw, Vl, key + 1, o[1]);
+    }
+    if (key < kw) small_pv_key<D>(Pw, Vl, key, o[0]);
+    // O / l; a row that saw no visible key (l == 0) is written as zeros.
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int row = r0 + r;
+        if (row >= Lq) continue;
+        const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
+        float *dst = Og + (size_t)row * D + lane * DC;
+        float res[DC];
+#pragma unroll
+        for (int c = 0; c < DC; ++c) res[c] = (o[0][r][c] + o[1][r][c]) * inv;
+        if (DC == 2)
+            *reinterpret_cast<float2 *>(dst) = make_float2(res[0], res[1]);
+        else
+            *reinterpret_cast<float4 *>(dst) = make_float4(res[0], res[1], res[DC - 2], res[DC - 1]);
+    }
+}
+
+template <int D>
+cudaError_t launch_small(const float *q, const float *k, const float *v, const int32_t *kv,
+                         float *out, int B, int H, int Lq, int Lk, int mask_kind, float scale,
+                         cudaStream_t stream) {
+    using C = SmallCfg<D>;
+    const int keys_cap = ((Lk + 31) / 32) * 32;
+    const size_t smem = C::smem(keys_cap);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(mha_fwd_f32_small_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::smem(C::kMaxKeys));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const dim3 grid((Lq + kSmallRows - 1) / kSmallRows, H, B);
+    mha_fwd_f32_small_kernel<D><<<grid, kSmallThreads, smem, stream>>>(
+        q, k, v, kv, out, H, Lq, Lk, mask_kind, scale * 1.4426950408889634f, keys_cap);
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch(const float *q, const float *k, const float *v, const int32_t *kv,
                    float *out, int B, int H, int Lq, int Lk, int mask_kind, float scale,
@@ -243,11 +523,20 @@ cudaError_t launch(const float *q, const float *k, const float *v, const int32_t
     return cudaGetLastError();
 }
 
+int g_f32_kernel = 0;   // 0 automatic, 1 tiled only, 2 short-key kernel where it applies
+
 }  // namespace
+
+void set_f32_kernel_override(int which) { g_f32_kernel = which; }
 
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v,
                            const int32_t *kv_lengths, float *out, int B, int H, int Lq,
                            int Lk, int D, int mask_kind, float scale, cudaStream_t stream) {
+    if ((int64_t)Lk * D <= kSmallMaxKD && g_f32_kernel != 1) {
+        if (D == 64)
+            return launch_small<64>(q, k, v, kv_lengths, out, B, H, Lq, Lk, mask_kind, scale, stream);
+        return launch_small<128>(q, k, v, kv_lengths, out, B, H, Lq, Lk, mask_kind, scale, stream);
+    }
     if (D == 64) return launch<64>(q, k, v, kv_lengths, out, B, H, Lq, Lk, mask_kind, scale, stream);
     return launch<128>(q, k, v, kv_lengths, out, B, H, Lq, Lk, mask_kind, scale, stream);
 }

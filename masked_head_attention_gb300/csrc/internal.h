@@ -48,7 +48,8 @@ cudaError_t noalloc_ln_stats(int64_t rows, float2 **ptr);
 // Device status word of the bf16 translation unit.
 cudaError_t read_device_status(uint32_t *bits, bool clear);
 
-// Launch-configuration overrides used by the benchmark sweeps (0 = default).
+// Launch-configuration overrides used by tests and benchmark sweeps (0 = default).
 void set_bf16_grid_override(int ctas);
+void set_f32_kernel_override(int which);
 
 }  // namespace mha

@@ -37,9 +37,17 @@ def _run(B, H, Lq, Lk, D, mask, lens, seed=0):
     return as_np(out), want
 
 
+@pytest.fixture
+def f32_kernel(request):
+    mha.set_f32_kernel(request.param)
+    yield request.param
+    mha.set_f32_kernel(0)
+
+
 @pytest.mark.gpu
+@pytest.mark.parametrize("f32_kernel", [0, 1, 2], indirect=True, ids=["auto", "tiled", "short"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dLq%dLk%dD%dm%d" % c[:6])
-def test_f32_small(case):
+def test_f32_small(case, f32_kernel):
     got, want = _run(*case)
     check_f32(got, want, str(case))
 
@@ -58,7 +66,8 @@ def test_f32_full_workload(name):
 
 
 @pytest.mark.gpu
-def test_f32_masked_keys_contribute_exactly_zero():
+@pytest.mark.parametrize("f32_kernel", [1, 2], indirect=True, ids=["tiled", "short"])
+def test_f32_masked_keys_contribute_exactly_zero(f32_kernel):
     B, H, L, D = 2, 2, 160, 64
     q, k, v = randn((B, H, L, D), 5), randn((B, H, L, D), 6), randn((B, H, L, D), 7)
     lens = torch.tensor([70, 160], dtype=torch.int32)
@@ -75,7 +84,8 @@ def test_f32_masked_keys_contribute_exactly_zero():
 
 
 @pytest.mark.gpu
-def test_f32_zero_keys_gives_zeros():
+@pytest.mark.parametrize("f32_kernel", [1, 2], indirect=True, ids=["tiled", "short"])
+def test_f32_zero_keys_gives_zeros(f32_kernel):
     q = randn((2, 2, 9, 64), 1).cuda()
     kv = torch.empty((2, 2, 0, 64), device="cuda")
     out = mha.mha_fwd(q, kv, kv, 0)
