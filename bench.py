@@ -37,11 +37,18 @@ from masked_head_attention_gb300 import synthetic  # noqa: E402
 METRIC = "mask-aware attention TFLOP/s and µs/call at 1 GB300; % of roofline"
 DEFAULT_WORKLOAD = "c2_padding_f32"
 DEFAULT_L2 = 129 * 1024 * 1024
-KERNEL_OF = {  # dominant (only) kernel of each workload
+KERNEL_OF = {  # dominant kernel of each workload
     "mha:f32": "mha_fwd_f32_kernel",
     "mha:bf16": "attn_fwd_bf16_kernel",
     "prenorm:bf16": "attn_fwd_bf16_kernel<prenorm>",
 }
+SMALL_F32_MAX_KD = 16384   # the fp32 path stages all keys at once when Lk * D is at most this
+
+
+def kernel_of(w):
+    if w.dtype == "f32" and w.Lk * w.D <= SMALL_F32_MAX_KD:
+        return "mha_fwd_f32_small_kernel"
+    return KERNEL_OF["%s:%s" % (w.kind, w.dtype)]
 
 
 # ------------------------------------------------------------------ helpers --
@@ -270,7 +277,7 @@ def time_e2e(wl, steps, warmup):
 
 def roofline_for(w, lens, kernel_ms, peaks, n_sm):
     flops = mask_aware_flops(w, lens)
-    kkey = KERNEL_OF["%s:%s" % (w.kind, w.dtype)]
+    kkey = kernel_of(w)
     if w.dtype == "f32":
         peak = fp32_alu_peak_tflops(n_sm, peaks.get("sm_max_mhz", 2070.0))
         bound = "alu"
