@@ -41,6 +41,7 @@ KERNEL_OF = {  # dominant kernel of each workload
     "mha:f32": "mha_fwd_f32_kernel",
     "mha:bf16": "attn_fwd_bf16_kernel",
     "prenorm:bf16": "attn_fwd_bf16_kernel<prenorm>",
+    "prenorm_residual:bf16": "attn_fwd_bf16_kernel<prenorm>",
 }
 SMALL_F32_MAX_KD = 16384   # the fp32 path stages all keys at once when Lk * D is at most this
 
@@ -76,7 +77,7 @@ def algorithmic_bytes(w, lens):
     e = 4 if w.dtype == "f32" else 2
     kv_rows = sum(visible_lengths(w, lens)) * w.H
     qo = 2 * w.B * w.H * w.Lq * w.D * e
-    extra = 2 * 4 * w.H * w.D if w.kind == "prenorm" else 0   # gamma, beta
+    extra = 2 * 4 * w.H * w.D if w.kind != "mha" else 0   # gamma, beta
     return qo + 2 * kv_rows * w.D * e + extra
 
 
@@ -204,9 +205,12 @@ class GpuWorkload:
             self.i += 1
         if w.kind == "mha":
             self.mha.mha_fwd(s["q"], s["k"], s["v"], w.mask, self.kv, out=s["out"], scale=w.scale)
-        else:
+        elif w.kind == "prenorm":
             self.mha.prenorm_cross_attn_fwd(s["x"], s["gamma"], s["beta"], w.eps, s["k"], s["v"],
                                             self.kv, out=s["out"], scale=w.scale)
+        else:
+            self.mha.prenorm_cross_attn_residual_fwd(s["x"], s["gamma"], s["beta"], w.eps, s["k"],
+                                                     s["v"], self.kv, out=s["out"], scale=w.scale)
 
     def input_bytes(self):
         b = sum(self.host[k].numel() * self.host[k].element_size() for k in self.in_keys)
@@ -330,8 +334,9 @@ def oracle_sample(w, host, budget_s, max_problems=None):
         else:
             rows = np.array([(pp // w.H, pp % w.H, i) for pp in range(p0, p1)
                              for i in range(w.Lq)], np.int64)
-            oracle.prenorm_rows(x, host["gamma"].numpy(), host["beta"].numpy(), w.eps, k, v,
-                                rows, lens, w.scale)
+            rows_fn = oracle.prenorm_rows if w.kind == "prenorm" else oracle.prenorm_residual_rows
+            rows_fn(x, host["gamma"].numpy(), host["beta"].numpy(), w.eps, k, v, rows, lens,
+                    w.scale)
         t_total += time.perf_counter() - t0
         sub = synthetic.Workload(w.name, w.kind, w.dtype, p1 - p0, 1, w.Lq, w.Lk, w.D, w.mask)
         flops += mask_aware_flops(sub, None if lb is None else lb.tolist())

@@ -117,6 +117,22 @@ MHA_API int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const fl
                            cudaStream_t stream);
 
 /*
+ * prenorm_cross_attn_residual_fwd -- Pre-LayerNorm cross-attention with the
+ * residual add (cms365.cn answer, step four: the attention output is added
+ * to the query-side input):
+ *     out[b,i,:] = x_q[b,i,:] + (prenorm_cross_attn_fwd output)[b,i,:]
+ * The sum is formed in fp32 inside the attention kernel's epilogue and
+ * rounded to bf16 once; a row with no visible key returns x_q's row.
+ *   Arguments, layouts, workspace and errors are those of
+ *   prenorm_cross_attn_fwd.  out must not overlap x_q.
+ */
+MHA_API int prenorm_cross_attn_residual_fwd(const void *x_q, const float *gamma,
+                            const float *beta, float eps, const void *k,
+                            const void *v, const int32_t *kv_lengths, void *out,
+                            int B, int H, int Lq, int Lk, int D, float scale,
+                            int dtype, cudaStream_t stream);
+
+/*
  * prenorm_cross_attn_fwd_noalloc -- the same computation as
  * prenorm_cross_attn_fwd, for callers that cannot let a library allocate
  * device memory: for example a serving runtime that reserves all GPU memory

@@ -48,6 +48,8 @@ def lib():
         L.mha_fwd.restype = i
         L.prenorm_cross_attn_fwd.argtypes = [P, P, P, f, P, P, P, P, i, i, i, i, i, f, i, P]
         L.prenorm_cross_attn_fwd.restype = i
+        L.prenorm_cross_attn_residual_fwd.argtypes = [P, P, P, f, P, P, P, P, i, i, i, i, i, f, i, P]
+        L.prenorm_cross_attn_residual_fwd.restype = i
         L.mha_strerror.argtypes = [i]
         L.mha_strerror.restype = ctypes.c_char_p
         L.mha_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
@@ -168,6 +170,38 @@ def prenorm_cross_attn_fwd(x_q, gamma, beta, eps, k, v, kv_lengths=None, out=Non
                                         _ptr(v), _ptr(kv_lengths), _ptr(out), B, H, Lq, Lk, D,
                                         scale, BF16, _stream(stream, x_q.get_device())),
            "prenorm_cross_attn_fwd")
+    return out
+
+
+def prenorm_cross_attn_residual_fwd(x_q, gamma, beta, eps, k, v, kv_lengths=None, out=None,
+                                    scale=None, stream=None):
+    """x_q + prenorm_cross_attn_fwd(x_q, ...), summed in fp32 and rounded once.
+    Same arguments and layouts as prenorm_cross_attn_fwd; `out` must not
+    overlap x_q."""
+    torch = _torch()
+    _dev(x_q, "x_q", torch.bfloat16)
+    _dev(gamma, "gamma", torch.float32)
+    _dev(beta, "beta", torch.float32)
+    _dev(k, "k", torch.bfloat16)
+    _dev(v, "v", torch.bfloat16)
+    B, H, Lk, D = k.shape
+    Lq = x_q.shape[1]
+    if tuple(x_q.shape) != (B, Lq, H * D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("x_q must be [B,Lq,H*D] and v [B,H,Lk,D]")
+    if gamma.numel() != H * D or beta.numel() != H * D:
+        raise ValueError("gamma and beta must have H*D elements")
+    if kv_lengths is not None:
+        _dev(kv_lengths, "kv_lengths", torch.int32)
+    if out is None:
+        out = torch.empty_like(x_q)
+    else:
+        _dev(out, "out", torch.bfloat16)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(lib().prenorm_cross_attn_residual_fwd(_ptr(x_q), _ptr(gamma), _ptr(beta), float(eps),
+                                                 _ptr(k), _ptr(v), _ptr(kv_lengths), _ptr(out),
+                                                 B, H, Lq, Lk, D, scale, BF16,
+                                                 _stream(stream, x_q.get_device())),
+           "prenorm_cross_attn_residual_fwd")
     return out
 
 

@@ -68,10 +68,16 @@ int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
     return from_cuda(e);
 }
 
-int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const float *beta, float eps,
+}  // extern "C"
+
+namespace {
+
+// Pre-LN cross-attention with a stream-ordered workspace for the row
+// statistics; `residual` is x_q for the residual variant, else null.
+int prenorm_with_workspace(const void *x_q, const float *gamma, const float *beta, float eps,
                            const void *k, const void *v, const int32_t *kv_lengths, void *out,
                            int B, int H, int Lq, int Lk, int D, float scale, int dtype,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const void *residual) {
     int empty = 0;
     int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
     if (st != MHA_OK) return st;
@@ -85,6 +91,7 @@ int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const float *bet
         return MHA_ERR_MISALIGNED;
     mha::Bf16Call c{};
     c.x = x_q;
+    c.residual = residual;
     c.gamma = gamma;
     c.beta = beta;
     c.eps = eps;
@@ -110,6 +117,26 @@ int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const float *bet
     if (drv != 0) return MHA_ERR_CUDA;
     if (e == cudaSuccess) e = ef;
     return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const float *beta, float eps,
+                           const void *k, const void *v, const int32_t *kv_lengths, void *out,
+                           int B, int H, int Lq, int Lk, int D, float scale, int dtype,
+                           cudaStream_t stream) {
+    return prenorm_with_workspace(x_q, gamma, beta, eps, k, v, kv_lengths, out, B, H, Lq, Lk, D,
+                                  scale, dtype, stream, nullptr);
+}
+
+int prenorm_cross_attn_residual_fwd(const void *x_q, const float *gamma, const float *beta,
+                                    float eps, const void *k, const void *v,
+                                    const int32_t *kv_lengths, void *out, int B, int H, int Lq,
+                                    int Lk, int D, float scale, int dtype, cudaStream_t stream) {
+    return prenorm_with_workspace(x_q, gamma, beta, eps, k, v, kv_lengths, out, B, H, Lq, Lk, D,
+                                  scale, dtype, stream, x_q);
 }
 
 int prenorm_cross_attn_fwd_noalloc(const void *x_q, const float *gamma, const float *beta,

@@ -80,6 +80,7 @@ struct AttnParams {
     const float *gamma;
     const float *beta;
     const int32_t *kv_lengths;   // null unless the kv-length mask is on
+    const __nv_bfloat16 *residual;   // Pre-LN with residual add: x [B][Lq][H*D]; else null
     int B, H, Lq, Lk;
     int causal;
     float scale_log2;     // scale * log2(e)
@@ -693,13 +694,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // The slice's previous store has finished reading it.
                     if (lane == 0) tma_store_wait_read();
                     __syncwarp();
+                    // Residual variant ("How to fuse cross-attention and layer-norm
+                    // into a single CUDA kernel?", answer step four): the row's slice
+                    // of x is added in fp32 before the one rounding to bf16.
+                    const bool add_res = PRENORM && p.residual != nullptr && row < p.Lq;
+                    const uint4 *res = reinterpret_cast<const uint4 *>(
+                        p.residual + ((size_t)it.b * p.Lq + (add_res ? row : 0)) * (size_t)(p.H * D) +
+                        it.h * D + hh * 64);
 #pragma unroll
                     for (int c8 = 0; c8 < 8; ++c8) {
+                        float f[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) f[q] = u2f(r[c8 * 8 + q]) * inv;
+                        if (add_res) {
+                            const uint4 u = __ldg(res + c8);
+                            f[0] += bf_lo(u.x);
+                            f[1] += bf_hi(u.x);
+                            f[2] += bf_lo(u.y);
+                            f[3] += bf_hi(u.y);
+                            f[4] += bf_lo(u.z);
+                            f[5] += bf_hi(u.z);
+                            f[6] += bf_lo(u.w);
+                            f[7] += bf_hi(u.w);
+                        }
                         uint4 w;
-                        w.x = pack_bf16x2(u2f(r[c8 * 8 + 0]) * inv, u2f(r[c8 * 8 + 1]) * inv);
-                        w.y = pack_bf16x2(u2f(r[c8 * 8 + 2]) * inv, u2f(r[c8 * 8 + 3]) * inv);
-                        w.z = pack_bf16x2(u2f(r[c8 * 8 + 4]) * inv, u2f(r[c8 * 8 + 5]) * inv);
-                        w.w = pack_bf16x2(u2f(r[c8 * 8 + 6]) * inv, u2f(r[c8 * 8 + 7]) * inv);
+                        w.x = pack_bf16x2(f[0], f[1]);
+                        w.y = pack_bf16x2(f[2], f[3]);
+                        w.z = pack_bf16x2(f[4], f[5]);
+                        w.w = pack_bf16x2(f[6], f[7]);
                         *reinterpret_cast<uint4 *>(sOw + lane * 128 + ((c8 ^ (lane & 7)) << 4)) = w;
                     }
                     fence_proxy_async_smem();
@@ -713,12 +735,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else if (row < p.Lq) {
+                // No visible key: the attention rows are zeros (the residual
+                // variant writes x's slice unchanged).
                 __nv_bfloat16 *dst =
                     PRENORM ? p.out + ((size_t)it.b * p.Lq + row) * (size_t)(p.H * D) + it.h * D
                             : p.out + ((size_t)it.bh * p.Lq + row) * (size_t)D;
+                const uint4 *res =
+                    (PRENORM && p.residual != nullptr)
+                        ? reinterpret_cast<const uint4 *>(
+                              p.residual + ((size_t)it.b * p.Lq + row) * (size_t)(p.H * D) + it.h * D)
+                        : nullptr;
 #pragma unroll
                 for (int ch = 0; ch < D / 8; ++ch)
-                    *reinterpret_cast<uint4 *>(dst + ch * 8) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(dst + ch * 8) =
+                        res ? __ldg(res + ch) : make_uint4(0, 0, 0, 0);
             }
             c += n;
             e += n > 0 ? 1 : 0;
@@ -1004,6 +1034,7 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     p.gamma = c.gamma;
     p.beta = c.beta;
     p.kv_lengths = (c.mask_kind & 2) ? c.kv_lengths : nullptr;
+    p.residual = prenorm ? reinterpret_cast<const __nv_bfloat16 *>(c.residual) : nullptr;
     p.B = c.B;
     p.H = c.H;
     p.Lq = c.Lq;

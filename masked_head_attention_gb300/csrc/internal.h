@@ -17,6 +17,7 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v,
 struct Bf16Call {
     const void *q;          // [B,H,Lq,D] (self-attention) or null
     const void *x;          // [B,Lq,H*D] (Pre-LN) or null
+    const void *residual;   // Pre-LN: added to the output ([B,Lq,H*D], i.e. x) or null
     const float *gamma;
     const float *beta;
     float eps;

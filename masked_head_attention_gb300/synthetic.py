@@ -23,7 +23,8 @@ DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 @dataclass(frozen=True)
 class Workload:
-    """One attention problem; `kind` is "mha" (self-attention) or "prenorm"."""
+    """One attention problem; `kind` is "mha" (self-attention), "prenorm"
+    (Pre-LN cross-attention) or "prenorm_residual" (the same plus x)."""
     name: str
     kind: str
     dtype: str
@@ -64,6 +65,10 @@ WORKLOADS = {
         "c4_prenorm_bf16", "prenorm", "bf16", B=32, H=16, Lq=2048, Lk=2048, D=64,
         mask=MASK_KV_LEN, len_range=(1024, 2048),
         note="Pre-LN cross-attention, bf16, d_model 1024, kv lengths U{1024..2048}"),
+    "c4r_prenorm_residual_bf16": Workload(
+        "c4r_prenorm_residual_bf16", "prenorm_residual", "bf16", B=32, H=16, Lq=2048, Lk=2048,
+        D=64, mask=MASK_KV_LEN, len_range=(1024, 2048),
+        note="Pre-LN cross-attention with the residual add (out = x + attention), shapes of c4"),
     "c5_long_causal_bf16": Workload(
         "c5_long_causal_bf16", "mha", "bf16", B=2, H=32, Lq=8192, Lk=8192, D=128,
         mask=MASK_CAUSAL, note="long causal self-attention, bf16, Q/K/V iid N(0,1)"),
@@ -98,7 +103,7 @@ def make(w: Workload, seed: int = 0):
         out["q"] = _normal(g, (w.B, w.H, w.Lq, w.D), w.qk_std, dt)
         out["k"] = _normal(g, (w.B, w.H, w.Lk, w.D), w.qk_std, dt)
         out["v"] = _normal(g, (w.B, w.H, w.Lk, w.D), w.v_std, dt)
-    elif w.kind == "prenorm":
+    elif w.kind in ("prenorm", "prenorm_residual"):
         N = w.H * w.D
         out["x"] = _normal(g, (w.B, w.Lq, N), w.qk_std, dt)
         out["gamma"] = (torch.randn((N,), generator=g, dtype=torch.float32) * w.gamma_std

@@ -41,9 +41,12 @@ def _bind(L):
     L.oracle_softmax_probs.argtypes = [P, P, i, P, P, i, i, i, i, i, d]
     L.oracle_layer_norm.argtypes = [P, P, P, d, P, i64, i]
     L.oracle_prenorm_cross_attn.argtypes = [P, P, P, d, P, P, P, P, i, i, i, i, i, d]
+    L.oracle_prenorm_cross_attn_residual.argtypes = [P, P, P, d, P, P, P, P, i, i, i, i, i, d]
     L.oracle_prenorm_rows.argtypes = [P, P, P, d, P, P, P, P, i64, P, i, i, i, i, i, d]
+    L.oracle_prenorm_residual_rows.argtypes = [P, P, P, d, P, P, P, P, i64, P, i, i, i, i, i, d]
     for f in ("oracle_mha_fwd", "oracle_mha_rows", "oracle_softmax_probs",
-              "oracle_layer_norm", "oracle_prenorm_cross_attn", "oracle_prenorm_rows"):
+              "oracle_layer_norm", "oracle_prenorm_cross_attn", "oracle_prenorm_rows",
+              "oracle_prenorm_cross_attn_residual", "oracle_prenorm_residual_rows"):
         getattr(L, f).restype = i
     return L
 
@@ -146,3 +149,34 @@ def prenorm_rows(x, gamma, beta, eps, k, v, rows, kv_lengths=None, scale=None, p
                                          _p(out), B, H, Lq, Lk, D, scale),
            "oracle_prenorm_rows")
     return out
+
+
+def prenorm_cross_attn_residual(x, gamma, beta, eps, k, v, kv_lengths=None, scale=None,
+                                path=None):
+    """out [B,Lq,H*D] = x + heads(LN(x)) attended over k/v [B,H,Lk,D]."""
+    x, g, b, k, v = _f64(x), _f64(gamma), _f64(beta), _f64(k), _f64(v)
+    B, Lq, N = x.shape
+    _, H, Lk, D = k.shape
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    out = np.zeros((B, Lq, N), np.float64)
+    _check(lib(path).oracle_prenorm_cross_attn_residual(
+        _p(x), _p(g), _p(b), float(eps), _p(k), _p(v), _p(_lens(kv_lengths)), _p(out),
+        B, H, Lq, Lk, D, scale), "oracle_prenorm_cross_attn_residual")
+    return out
+
+
+def prenorm_residual_rows(x, gamma, beta, eps, k, v, rows, kv_lengths=None, scale=None,
+                          path=None):
+    """Rows (b, h, i) of the residual variant, each the head-h slice -> [n, D]."""
+    x, g, b, k, v = _f64(x), _f64(gamma), _f64(beta), _f64(k), _f64(v)
+    B, Lq, N = x.shape
+    _, H, Lk, D = k.shape
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    out = np.zeros((rows.shape[0], D), np.float64)
+    _check(lib(path).oracle_prenorm_residual_rows(_p(x), _p(g), _p(b), float(eps), _p(k), _p(v),
+                                                  _p(_lens(kv_lengths)), _p(rows), rows.shape[0],
+                                                  _p(out), B, H, Lq, Lk, D, scale),
+           "oracle_prenorm_residual_rows")
+    return out
+

@@ -303,3 +303,45 @@ int oracle_prenorm_rows(const double *x, const double *gamma, const double *beta
     }
     return fail ? -1 : 0;
 }
+
+/*
+ * Pre-LN cross-attention with the residual add of the same page ("How to
+ * fuse cross-attention and layer-norm into a single CUDA kernel?", answer
+ * step four: the attention output is added to the query-side input src):
+ * out = x + prenorm_cross_attn(x).  Same shapes as oracle_prenorm_cross_attn.
+ */
+int oracle_prenorm_cross_attn_residual(const double *x, const double *gamma,
+                                       const double *beta, double eps,
+                                       const double *k, const double *v,
+                                       const int32_t *kv_lengths, double *out,
+                                       int B, int H, int Lq, int Lk, int D,
+                                       double scale) {
+    int rc = oracle_prenorm_cross_attn(x, gamma, beta, eps, k, v, kv_lengths, out,
+                                       B, H, Lq, Lk, D, scale);
+    if (rc != 0) return rc;
+    size_t n = (size_t)B * Lq * (size_t)H * D;
+    for (size_t e = 0; e < n; ++e) out[e] = x[e] + out[e];
+    return 0;
+}
+
+/*
+ * Selected rows of the residual variant: rows holds n triples (b, h, i);
+ * out_rows receives n x D values, x[b, i, h*D .. h*D + D) plus the head-h
+ * slice of the attention output of row (b, i).
+ */
+int oracle_prenorm_residual_rows(const double *x, const double *gamma,
+                                 const double *beta, double eps, const double *k,
+                                 const double *v, const int32_t *kv_lengths,
+                                 const int64_t *rows, int64_t n, double *out_rows,
+                                 int B, int H, int Lq, int Lk, int D, double scale) {
+    int rc = oracle_prenorm_rows(x, gamma, beta, eps, k, v, kv_lengths, rows, n, out_rows,
+                                 B, H, Lq, Lk, D, scale);
+    if (rc != 0) return rc;
+    for (int64_t r = 0; r < n; ++r) {
+        int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+        const double *src = x + ((size_t)b * Lq + (size_t)i) * (size_t)H * D + (size_t)h * D;
+        for (int d = 0; d < D; ++d) out_rows[(size_t)r * D + d] = src[d] + out_rows[(size_t)r * D + d];
+    }
+    return 0;
+}
+

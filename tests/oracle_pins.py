@@ -299,10 +299,44 @@ def check_prenorm(path=None):
     return None
 
 
+def check_prenorm_residual(path=None):
+    """Residual variant ("How to fuse cross-attention and layer-norm into a
+    single CUDA kernel?", answer step four: output + src).  gamma = beta = 0
+    makes every LN row zero, so Q = 0 and each head's attention is the mean of
+    its visible V rows: out = x + that mean (a closed form).  V = 0 leaves
+    exactly x.  The row API must agree with the full op."""
+    r = _rng(12)
+    B, H, Lq, Lk, D = 2, 3, 5, 7, 4
+    x = r.standard_normal((B, Lq, H * D)) * 1.5 - 0.25
+    k, v = r.standard_normal((B, H, Lk, D)), r.standard_normal((B, H, Lk, D))
+    lens = np.array([3, 7], np.int32)
+    z = np.zeros(H * D)
+    got = oracle.prenorm_cross_attn_residual(x, z, z, 1e-5, k, v, lens, 0.5, path=path)
+    want = x.copy()
+    for b in range(B):
+        for h in range(H):
+            want[b, :, h * D:(h + 1) * D] += v[b, h, :lens[b]].mean(axis=0)
+    if np.abs(got - want).max() > 1e-12:
+        return "gamma = beta = 0 is not x + mean of visible V: %g" % np.abs(got - want).max()
+    g = 1 + 0.1 * r.standard_normal(H * D)
+    be = 0.1 * r.standard_normal(H * D)
+    got0 = oracle.prenorm_cross_attn_residual(x, g, be, 1e-5, k, np.zeros_like(v), lens, 0.5,
+                                              path=path)
+    if np.abs(got0 - x).max() > 1e-15:
+        return "V = 0 does not return x"
+    full = oracle.prenorm_cross_attn_residual(x, g, be, 1e-5, k, v, lens, 0.5, path=path)
+    rows = [(0, 2, 4), (1, 0, 0), (1, 1, 3)]
+    pr = oracle.prenorm_residual_rows(x, g, be, 1e-5, k, v, rows, lens, 0.5, path=path)
+    for n, (b, h, i) in enumerate(rows):
+        if np.abs(pr[n] - full[b, i, h * D:(h + 1) * D]).max() > 1e-13:
+            return "residual row API differs from the full op"
+    return None
+
+
 ALL = [check_brute_force, check_sdpa, check_golden, check_shift_invariance,
        check_rows_sum_to_one, check_zero_query_is_mean, check_causal_rules,
        check_padding_rules, check_hard_max_and_overflow, check_rows_api,
-       check_layer_norm, check_prenorm]
+       check_layer_norm, check_prenorm, check_prenorm_residual]
 
 
 def run_all(path=None):

@@ -53,6 +53,25 @@ def check_bf16(got, want, what=""):
                 over_1e2=int((err > BF16_MAX_ABS).sum()))
 
 
+def check_bf16_sum(got, want, what=""):
+    """For outputs that add a bf16 input to an attention result and round the
+    sum once (the residual variant): the rounding alone costs up to half an
+    ulp of the result, on top of the attention's own error bounds (1e-2 per
+    element, 1e-3 on average).  So per element |gpu - oracle| <=
+    ulp_bf16(oracle) / 2 + 1e-2, and on average <= mean(ulp / 2) + 1e-3."""
+    got = np.asarray(got, np.float64)
+    err = np.abs(got - want)
+    assert np.all(np.isfinite(got)), "%s: non-finite output" % what
+    half = 0.5 * ulp_bf16(want)
+    bad = err > half + BF16_MAX_ABS
+    assert not bad.any(), "%s: %d elements over tolerance, worst %.3g at oracle %.3g" % (
+        what, bad.sum(), err.max(), want.ravel()[err.argmax()])
+    assert err.mean() <= half.mean() + BF16_MEAN_ABS, "%s: mean abs %.3g > %.3g" % (
+        what, err.mean(), half.mean() + BF16_MEAN_ABS)
+    return dict(max_abs=float(err.max()), mean_abs=float(err.mean()),
+                mean_half_ulp=float(half.mean()))
+
+
 def as_np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 

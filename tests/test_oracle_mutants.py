@@ -30,6 +30,11 @@ MUTANTS = [
     ("length_of_batch0", "int len = kv_lengths[b];", "int len = kv_lengths[0];"),
     ("rows_api_head_index", "size_t bh = (size_t)b * H + (size_t)h;\n        attend_row",
      "size_t bh = (size_t)h * B + (size_t)b;\n        attend_row"),
+    ("residual_dropped", "out[e] = x[e] + out[e];", "out[e] = out[e];"),
+    ("residual_doubled", "out[e] = x[e] + out[e];", "out[e] = x[e] + x[e] + out[e];"),
+    ("residual_rows_wrong_head",
+     "(size_t)i) * (size_t)H * D + (size_t)h * D;\n        for (int d = 0;",
+     "(size_t)i) * (size_t)H * D;\n        for (int d = 0;"),
 ]
 
 

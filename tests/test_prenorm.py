@@ -6,7 +6,7 @@ import torch
 import masked_head_attention_gb300 as mha
 import oracle
 from masked_head_attention_gb300 import synthetic
-from parity_util import as_np, check_bf16, dev, lens_tensor, randn, sample_rows
+from parity_util import as_np, check_bf16, check_bf16_sum, dev, lens_tensor, randn, sample_rows
 
 CASES = [
     (1, 1, 1, 1, 64, None),
@@ -57,3 +57,41 @@ def test_prenorm_c4_sampled_rows():
     got = np.stack([o[b, i, h * w.D:(h + 1) * w.D].numpy() for b, h, i in rows]).astype(np.float64)
     r = check_bf16(got, want, w.name)
     print(w.name, r)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dLq%dLk%dD%d" % c[:5])
+def test_prenorm_residual_small(case):
+    B, H, Lq, Lk, D, lens = case
+    x, g, b, k, v = _inputs(B, H, Lq, Lk, D, 23)
+    out = mha.prenorm_cross_attn_residual_fwd(dev(x), dev(g), dev(b), 1e-5, dev(k), dev(v),
+                                              dev(lens_tensor(lens)))
+    torch.cuda.synchronize()
+    want = oracle.prenorm_cross_attn_residual(x.float().numpy(), g.numpy(), b.numpy(), 1e-5,
+                                              k.float().numpy(), v.float().numpy(), lens)
+    check_bf16_sum(as_np(out), want, str(case))
+    assert mha.device_status() == 0
+    if lens is not None and 0 in lens:
+        # A batch with no visible key returns x unchanged, bit for bit.
+        z = lens.index(0)
+        assert torch.equal(out[z].cpu(), x[z])
+
+
+@pytest.mark.gpu
+def test_prenorm_residual_c4_sampled_rows():
+    w = synthetic.WORKLOADS["c4_prenorm_bf16"]
+    xs = synthetic.make(w, seed=0)
+    out = mha.prenorm_cross_attn_residual_fwd(dev(xs["x"]), dev(xs["gamma"]), dev(xs["beta"]),
+                                              w.eps, dev(xs["k"]), dev(xs["v"]),
+                                              dev(xs["kv_lengths"]), scale=w.scale)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.B, w.H, w.Lq, 160, seed=7)
+    want = oracle.prenorm_residual_rows(xs["x"].float().numpy(), xs["gamma"].numpy(),
+                                        xs["beta"].numpy(), w.eps, xs["k"].float().numpy(),
+                                        xs["v"].float().numpy(), rows, xs["kv_lengths"].numpy(),
+                                        w.scale)
+    o = out.float().cpu()
+    got = np.stack([o[b, i, h * w.D:(h + 1) * w.D].numpy() for b, h, i in rows]).astype(np.float64)
+    r = check_bf16_sum(got, want, w.name + " residual")
+    print(w.name, "residual", r)
+    assert mha.device_status() == 0
