@@ -44,11 +44,14 @@ KERNEL_OF = {  # dominant kernel of each workload
     "prenorm_residual:bf16": "attn_fwd_bf16_kernel<prenorm>",
 }
 SMALL_F32_MAX_KD = 16384   # the fp32 path stages all keys at once when Lk * D is at most this
+DECODE_MAX_ROWS = 8        # bf16 self-attention with at most this many query rows: decode kernel
 
 
 def kernel_of(w):
     if w.dtype == "f32" and w.Lk * w.D <= SMALL_F32_MAX_KD:
         return "mha_fwd_f32_small_kernel"
+    if w.kind == "mha" and w.dtype == "bf16" and w.Lq <= DECODE_MAX_ROWS:
+        return "attn_decode_bf16_kernel"
     return KERNEL_OF["%s:%s" % (w.kind, w.dtype)]
 
 
@@ -280,22 +283,33 @@ def time_e2e(wl, steps, warmup):
 
 
 def roofline_for(w, lens, kernel_ms, peaks, n_sm):
+    """The binding roofline of the workload's dominant kernel: compute (FFMA
+    for fp32 inputs, the tensor cores for bf16) or HBM, whichever takes
+    longer for the algorithmic work; achieved and peak in that roofline's
+    unit (TFLOP/s or GB/s)."""
     flops = mask_aware_flops(w, lens)
+    nbytes = algorithmic_bytes(w, lens)
     kkey = kernel_of(w)
     if w.dtype == "f32":
-        peak = fp32_alu_peak_tflops(n_sm, peaks.get("sm_max_mhz", 2070.0))
-        bound = "alu"
+        cpeak = fp32_alu_peak_tflops(n_sm, peaks.get("sm_max_mhz", 2070.0))
+        cbound, csrc = "alu", " (SMs x 128 lanes x 2 x max SM clock)"
     else:
-        peak = peaks["bf16_tflops"]
-        bound = "tensor"
-    achieved = flops / (kernel_ms * 1e-3) / 1e12
+        cpeak = peaks["bf16_tflops"]
+        cbound, csrc = "tensor", " bf16 burst"
     rec = traffic_record("%s/%s" % (kkey, w.name))
+    t_compute = flops / (cpeak * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    if t_hbm > t_compute:
+        achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+        bound, unit, peak, psrc = "hbm", "GB/s", peaks["hbm_gbs"], " HBM copy"
+    else:
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        bound, unit, peak, psrc = cbound, "TFLOP/s", cpeak, csrc
     return {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 1),
-            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "unit": unit, "frac": round(achieved / peak, 4),
             "traffic": None if rec is None else rec["dram_bytes_per_launch"],
-            "algorithmic_bytes": int(algorithmic_bytes(w, lens)),
-            "kernel": kkey, "peak_source": peaks["_source"] +
-            (" (SMs x 128 lanes x 2 x max SM clock)" if w.dtype == "f32" else " bf16 burst")}
+            "algorithmic_bytes": int(nbytes),
+            "kernel": kkey, "peak_source": peaks["_source"] + psrc}
 
 
 # --------------------------------------------------------------- CPU oracle --
@@ -448,7 +462,7 @@ def measure_config(w, args, device, peaks, n_sm, l2):
     r = roofline_for(w, wl.lens, statistics.mean(per_launch), peaks, n_sm)
     out = {"us_per_call": round(call_ms * 1e3, 3), "tflops": round(flops / call_ms / 1e9, 3),
            "nominal_tflops": round(nominal_flops(w) / call_ms / 1e9, 3), "steps": steps,
-           "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "frac", "traffic")},
+           "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
            "hbm_gbs": round(algorithmic_bytes(w, wl.lens) / call_ms / 1e6, 1),
            "input_sets": len(wl.sets)}
     if call_ms < 0.05:

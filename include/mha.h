@@ -204,6 +204,16 @@ MHA_API void mha_set_bf16_grid(int ctas);
  */
 MHA_API void mha_set_f32_kernel(int which);
 
+/*
+ * mha_set_bf16_decode -- kernel-choice hook for tests and benchmarks of the
+ * bf16 path.  0 = automatic: mha_fwd calls with at most 8 query rows run the
+ * decode kernel (the keys of each (b, h) split over a thread-block cluster of
+ * up to 8 CTAs, partial results combined in distributed shared memory);
+ * 1 = never (always the tensor-core kernel).  Other values act as 0.
+ * Affects later calls from any thread of the process.
+ */
+MHA_API void mha_set_bf16_decode(int mode);
+
 #ifdef __cplusplus
 }
 #endif

@@ -60,6 +60,8 @@ def lib():
         L.mha_set_bf16_grid.restype = None
         L.mha_set_f32_kernel.argtypes = [i]
         L.mha_set_f32_kernel.restype = None
+        L.mha_set_bf16_decode.argtypes = [i]
+        L.mha_set_bf16_decode.restype = None
         _lib = L
     return _lib
 
@@ -225,6 +227,11 @@ def selftest_umma(variant, kn, a, b, c, stream=None):
 
 def set_bf16_grid(ctas):
     lib().mha_set_bf16_grid(int(ctas))
+
+
+def set_bf16_decode(mode):
+    """0 automatic (decode kernel for bf16 calls with Lq <= 8), 1 never."""
+    lib().mha_set_bf16_decode(int(mode))
 
 
 def set_f32_kernel(which):

@@ -214,4 +214,6 @@ void mha_set_bf16_grid(int ctas) { mha::set_bf16_grid_override(ctas); }
 
 void mha_set_f32_kernel(int which) { mha::set_f32_kernel_override(which); }
 
+void mha_set_bf16_decode(int mode) { mha::set_decode_override(mode); }
+
 }  // extern "C"

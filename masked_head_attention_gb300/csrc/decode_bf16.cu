@@ -1,0 +1,327 @@
+// decode_bf16.cu -- masked multi-head attention forward for a few query rows
+// (Lq <= 8) against a long bf16 key/value cache: the decode step of a
+// KV-cached model, or its short chunks.  Same semantics as the main kernels
+// (top-left causal rule, per-batch valid lengths, scale, zero rows when no key
+// is visible); only the work split differs.
+//
+// The step is memory-bound (every visible K/V row is read once and used for
+// at most 8 query rows), so the keys of one (b, h) are split over a
+// thread-block cluster of up to 8 CTAs, each streaming its own contiguous key
+// range:
+//   - 8 warps per CTA; a warp takes blocks of 32 keys (lane = key) and forms
+//     S for all R query rows with 16-byte loads of its key's K row (Q is
+//     broadcast from shared memory), then runs an exact online softmax per
+//     row (warp max / sum by shuffles) and adds P.V with lanes over the
+//     output columns (each V row read once, coalesced).
+//   - The 8 warps' partial (max, sum, O) meet in shared memory; the CTAs'
+//     partials meet on cluster rank 0 through distributed shared memory, and
+//     rank 0 writes O once.  No workspace in global memory, no mbarrier
+//     waits: the only waits are the cluster's hardware barriers, which every
+//     CTA reaches unconditionally.
+//
+// Page sections this follows: "masked multi head attention" CUDA article
+// (2kiu.com) 6.3 (attention against a cached K/V, llama.cpp-style); "Why
+// attention must compute the max first" (gsyq.cn) 2.3-2.4 (online softmax
+// with the max shift; partial results combined by rescaling with the
+// difference of their maxima).
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = 32 * kDecWarps;
+constexpr int kDecMaxCluster = 8;
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Whole-cluster barrier (every thread of every CTA of the cluster arrives;
+// release / acquire order the shared-memory writes before it with the reads
+// after it).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of `p` (this CTA's shared memory) in the shared memory of cluster
+// CTA `rank`, for ld.shared::cluster.
+__device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Partial result of a set of keys for R query rows: running max (base-2
+// logits), sum of 2^(s - max), and O = sum of 2^(s - max) V.
+template <int D, int R>
+struct DecPartial {
+    float m[R];
+    float l[R];
+    float o[R][D];
+};
+
+template <int D, int R>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    attn_decode_bf16_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                            const __nv_bfloat16 *__restrict__ v, const int32_t *__restrict__ kv_lengths,
+                            __nv_bfloat16 *__restrict__ out, int H, int Lq, int Lk, int mask_kind,
+                            float scale_log2, int chunk) {
+    constexpr int DC = D / 32;   // output columns per lane
+    __shared__ float sQ[R][D];
+    __shared__ DecPartial<D, R> sW[kDecWarps];   // per-warp partials
+    __shared__ DecPartial<D, R> sC;              // this CTA's partial (read by cluster rank 0)
+
+    const int split = blockIdx.x, nsplit = gridDim.x;
+    const int bh = blockIdx.y;
+    const int b = bh / H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool causal = (mask_kind & 1) != 0;
+    int len = Lk;
+    if (mask_kind & 2) len = max(0, min((int)kv_lengths[b], Lk));
+    int kend = len;                                     // keys any row can see
+    if (causal) kend = min(kend, Lq);
+    const int k0 = split * chunk, k1 = min(kend, k0 + chunk);
+
+    const __nv_bfloat16 *Qg = q + (size_t)bh * Lq * D;
+    const __nv_bfloat16 *Kg = k + (size_t)bh * Lk * D;
+    const __nv_bfloat16 *Vg = v + (size_t)bh * Lk * D;
+    for (int e = tid; e < R * D; e += kDecThreads) {
+        const int r = e / D, d = e % D;
+        sQ[r][d] = r < Lq ? __bfloat162float(Qg[(size_t)r * D + d]) : 0.f;
+    }
+    __syncthreads();
+
+    float m[R], l[R], o[R][DC];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+#pragma unroll
+        for (int c = 0; c < DC; ++c) o[r][c] = 0.f;
+    }
+    // V rows in flight per batch: the whole 32-key block when the registers
+    // allow (few query rows), else 8.
+    constexpr int VB = R <= 2 ? 32 : 8;
+    for (int base = k0 + 32 * warp; base < k1; base += 32 * kDecWarps) {
+        const int key = base + lane;
+        const bool live = key < k1;
+        // Every load of the block's K rows is issued before any use (keys past
+        // the range read the last valid row and are masked below).
+        const uint4 *kr = reinterpret_cast<const uint4 *>(Kg + (size_t)min(key, k1 - 1) * D);
+        uint4 ku[D / 8];
+#pragma unroll
+        for (int c8 = 0; c8 < D / 8; ++c8) ku[c8] = __ldg(kr + c8);
+        // S for this lane's key and every row.
+        float s[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) s[r] = 0.f;
+#pragma unroll
+        for (int c8 = 0; c8 < D / 8; ++c8) {
+            const uint4 u = ku[c8];
+            const float kf[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
+                                 bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[r] = fmaf(sQ[r][c8 * 8 + e], kf[e], s[r]);
+        }
+        // Mask, block max, rescale, exponentials, row sums (base 2).
+        float p[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool vis = live && r < Lq && (!causal || key <= r);
+            const float x = vis ? s[r] * scale_log2 : -INFINITY;
+            float mb = x;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+            const float m_new = fmaxf(m[r], mb);
+            const float msub = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = ex2_approx(m[r] - msub);
+            m[r] = m_new;
+            p[r] = ex2_approx(x - msub);
+            float ps = p[r];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+            l[r] = fmaf(l[r], alpha, ps);
+#pragma unroll
+            for (int c = 0; c < DC; ++c) o[r][c] *= alpha;
+        }
+        // O += P V over the block's keys; lane holds output columns lane*DC...
+        // VB V rows are in flight at a time; rows past the range are read
+        // from the last valid row and carry weight 0 (their p is 2^-inf).
+        const int nk = min(32, k1 - base);
+#pragma unroll
+        for (int j0 = 0; j0 < 32; j0 += VB) {
+            if (j0 >= nk) break;
+            float vv[VB][DC];
+#pragma unroll
+            for (int jj = 0; jj < VB; ++jj) {
+                const int vrow = min(base + j0 + jj, k1 - 1);
+                const __nv_bfloat16 *vr = Vg + (size_t)vrow * D + lane * DC;
+                if (DC == 4) {
+                    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(vr));
+                    vv[jj][0] = bf_lo(u.x);
+                    vv[jj][1] = bf_hi(u.x);
+                    vv[jj][DC - 2] = bf_lo(u.y);
+                    vv[jj][DC - 1] = bf_hi(u.y);
+                } else {
+                    const uint32_t u = __ldg(reinterpret_cast<const uint32_t *>(vr));
+                    vv[jj][0] = bf_lo(u);
+                    vv[jj][DC - 1] = bf_hi(u);
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < VB; ++jj)
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float pj = __shfl_sync(0xffffffffu, p[r], j0 + jj);
+#pragma unroll
+                    for (int c = 0; c < DC; ++c) o[r][c] = fmaf(pj, vv[jj][c], o[r][c]);
+                }
+        }
+    }
+    // Warp partials -> shared memory.
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if (lane == 0) {
+            sW[warp].m[r] = m[r];
+            sW[warp].l[r] = l[r];
+        }
+#pragma unroll
+        for (int c = 0; c < DC; ++c) sW[warp].o[r][lane * DC + c] = o[r][c];
+    }
+    __syncthreads();
+    // CTA partial: combine the warps with 2^(m_w - m) (warp r handles row r).
+    if (warp < R) {
+        const int r = warp;
+        float mm = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, sW[w].m[r]);
+        const float msub = (mm == -INFINITY) ? 0.f : mm;
+        float ll = 0.f, oc[DC];
+#pragma unroll
+        for (int c = 0; c < DC; ++c) oc[c] = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) {
+            const float f = ex2_approx(sW[w].m[r] - msub);
+            ll = fmaf(sW[w].l[r], f, ll);
+#pragma unroll
+            for (int c = 0; c < DC; ++c) oc[c] = fmaf(sW[w].o[r][lane * DC + c], f, oc[c]);
+        }
+        if (lane == 0) {
+            sC.m[r] = mm;
+            sC.l[r] = ll;
+        }
+#pragma unroll
+        for (int c = 0; c < DC; ++c) sC.o[r][lane * DC + c] = oc[c];
+    }
+    // Cluster: rank 0 combines every CTA's partial and writes O (bf16).
+    cluster_sync_all();
+    if (cluster_ctarank() == 0 && warp < R && warp < Lq) {
+        const int r = warp;
+        float mm = -INFINITY;
+        for (int s = 0; s < nsplit; ++s) mm = fmaxf(mm, ld_cluster_f32(map_to_rank(&sC.m[r], s)));
+        const float msub = (mm == -INFINITY) ? 0.f : mm;
+        float ll = 0.f, oc[DC];
+#pragma unroll
+        for (int c = 0; c < DC; ++c) oc[c] = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+            const float f = ex2_approx(ld_cluster_f32(map_to_rank(&sC.m[r], s)) - msub);
+            ll = fmaf(ld_cluster_f32(map_to_rank(&sC.l[r], s)), f, ll);
+#pragma unroll
+            for (int c = 0; c < DC; ++c)
+                oc[c] = fmaf(ld_cluster_f32(map_to_rank(&sC.o[r][lane * DC + c], s)), f, oc[c]);
+        }
+        // A row that saw no visible key is written as zeros.
+        const float inv = ll > 0.f ? 1.f / ll : 0.f;
+        __nv_bfloat16 *dst = out + ((size_t)bh * Lq + r) * D + lane * DC;
+#pragma unroll
+        for (int c = 0; c < DC; ++c) dst[c] = __float2bfloat16_rn(oc[c] * inv);
+    }
+    // No CTA leaves while rank 0 may still read its shared memory.
+    cluster_sync_all();
+}
+
+int g_decode_override = 0;   // 0 automatic, 1 never
+
+template <int D, int R>
+cudaError_t launch_dec(const Bf16Call &c, int splits, int chunk, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)splits, (unsigned)(c.B * c.H), 1);
+    cfg.blockDim = dim3(kDecThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_decode_bf16_kernel<D, R>,
+                              reinterpret_cast<const __nv_bfloat16 *>(c.q),
+                              reinterpret_cast<const __nv_bfloat16 *>(c.k),
+                              reinterpret_cast<const __nv_bfloat16 *>(c.v),
+                              (c.mask_kind & 2) ? c.kv_lengths : nullptr,
+                              reinterpret_cast<__nv_bfloat16 *>(c.out), c.H, c.Lq, c.Lk,
+                              c.mask_kind, c.scale * 1.4426950408889634f, chunk);
+}
+
+template <int D>
+cudaError_t launch_dec_rows(const Bf16Call &c, int splits, int chunk, cudaStream_t stream) {
+    if (c.Lq <= 1) return launch_dec<D, 1>(c, splits, chunk, stream);
+    if (c.Lq <= 2) return launch_dec<D, 2>(c, splits, chunk, stream);
+    if (c.Lq <= 4) return launch_dec<D, 4>(c, splits, chunk, stream);
+    return launch_dec<D, 8>(c, splits, chunk, stream);
+}
+
+}  // namespace
+
+void set_decode_override(int which) { g_decode_override = which; }
+
+bool decode_applies(const Bf16Call &c) {
+    // (b, h) problems are the grid's y dimension (at most 65535).
+    return c.x == nullptr && c.Lq <= kDecodeMaxRows && g_decode_override != 1 &&
+           (int64_t)c.B * c.H <= 65535;
+}
+
+cudaError_t launch_decode_bf16(const Bf16Call &c, int num_sms, cudaStream_t stream) {
+    // Keys any row can see at most; the split covers them in contiguous
+    // chunks of a multiple of 32 keys.
+    const int kend = (c.mask_kind & 1) ? (c.Lq < c.Lk ? c.Lq : c.Lk) : c.Lk;
+    const int64_t BH = (int64_t)c.B * c.H;
+    // About two CTAs per SM in total, at least 256 keys per CTA, at most a
+    // portable cluster of 8.
+    int64_t want = (2 * (int64_t)num_sms + BH - 1) / BH;
+    const int64_t by_keys = (kend + 255) / 256;
+    if (want > by_keys) want = by_keys;
+    if (want > kDecMaxCluster) want = kDecMaxCluster;
+    if (want < 1) want = 1;
+    const int splits = (int)want;
+    int chunk = (kend + splits - 1) / splits;
+    chunk = ((chunk + 31) / 32) * 32;
+    if (chunk < 32) chunk = 32;
+    return c.D == 64 ? launch_dec_rows<64>(c, splits, chunk, stream)
+                     : launch_dec_rows<128>(c, splits, chunk, stream);
+}
+
+}  // namespace mha

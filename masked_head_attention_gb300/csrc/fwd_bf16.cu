@@ -1003,6 +1003,8 @@ cudaError_t launch_ln_row_stats(const void *x, float2 *stats, int64_t rows, int 
 cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_err,
                             float2 *ln_stats) {
     *driver_err = 0;
+    // A few query rows against many keys: the cluster split-K decode kernel.
+    if (decode_applies(c)) return launch_decode_bf16(c, device_info().sms, stream);
     AttnParams p;
     std::memset(&p, 0, sizeof(p));
     const bool prenorm = c.x != nullptr;

@@ -36,6 +36,13 @@ struct Bf16Call {
 cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_err,
                             float2 *ln_stats);
 
+// Decode path (decode_bf16.cu): bf16 self-attention with at most
+// kDecodeMaxRows query rows, keys split over a thread-block cluster.
+constexpr int kDecodeMaxRows = 8;
+bool decode_applies(const Bf16Call &c);
+cudaError_t launch_decode_bf16(const Bf16Call &c, int num_sms, cudaStream_t stream);
+void set_decode_override(int which);
+
 // Diagnostic single-tile tcgen05 GEMM (fwd_bf16.cu).
 cudaError_t launch_selftest_umma(int variant, int K_or_N, const void *a, const void *b,
                                  float *c, cudaStream_t stream, int *driver_err);

@@ -72,6 +72,11 @@ WORKLOADS = {
     "c5_long_causal_bf16": Workload(
         "c5_long_causal_bf16", "mha", "bf16", B=2, H=32, Lq=8192, Lk=8192, D=128,
         mask=MASK_CAUSAL, note="long causal self-attention, bf16, Q/K/V iid N(0,1)"),
+    "c6_decode_bf16": Workload(
+        "c6_decode_bf16", "mha", "bf16", B=8, H=32, Lq=1, Lk=8192, D=128, mask=MASK_KV_LEN,
+        len_range=(4096, 8192),
+        note="decode step: one new query row per (b, h) against a KV cache of U{4096..8192} "
+             "valid keys, bf16"),
 }
 
 
