@@ -44,7 +44,10 @@ def _bind(L):
     L.oracle_prenorm_cross_attn_residual.argtypes = [P, P, P, d, P, P, P, P, i, i, i, i, i, d]
     L.oracle_prenorm_rows.argtypes = [P, P, P, d, P, P, P, P, i64, P, i, i, i, i, i, d]
     L.oracle_prenorm_residual_rows.argtypes = [P, P, P, d, P, P, P, P, i64, P, i, i, i, i, i, d]
+    L.oracle_mha_lse.argtypes = [P, P, i, P, P, i, i, i, i, i, d]
+    L.oracle_mha_bwd.argtypes = [P, P, P, P, i, P, P, P, P, i, i, i, i, i, d]
     for f in ("oracle_mha_fwd", "oracle_mha_rows", "oracle_softmax_probs",
+              "oracle_mha_lse", "oracle_mha_bwd",
               "oracle_layer_norm", "oracle_prenorm_cross_attn", "oracle_prenorm_rows",
               "oracle_prenorm_cross_attn_residual", "oracle_prenorm_residual_rows"):
         getattr(L, f).restype = i
@@ -111,6 +114,31 @@ def softmax_probs(q, k, mask_kind=MASK_NONE, kv_lengths=None, scale=None, path=N
     _check(lib(path).oracle_softmax_probs(_p(q), _p(k), mask_kind, _p(_lens(kv_lengths)), _p(p),
                                           B, H, Lq, Lk, D, scale), "oracle_softmax_probs")
     return p
+
+
+def mha_lse(q, k, mask_kind=MASK_NONE, kv_lengths=None, scale=None, path=None):
+    """Row log-sum-exp of the scaled, masked logits -> [B,H,Lq] (-inf: no visible key)."""
+    q, k = _f64(q), _f64(k)
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    lse = np.zeros((B, H, Lq), np.float64)
+    _check(lib(path).oracle_mha_lse(_p(q), _p(k), mask_kind, _p(_lens(kv_lengths)), _p(lse),
+                                    B, H, Lq, Lk, D, scale), "oracle_mha_lse")
+    return lse
+
+
+def mha_bwd(q, k, v, dout, mask_kind=MASK_NONE, kv_lengths=None, scale=None, path=None):
+    """Gradients (dq, dk, dv) of sum(dout * mha_fwd(q, k, v)) -> shapes of q, k, v."""
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    _check(lib(path).oracle_mha_bwd(_p(q), _p(k), _p(v), _p(g), mask_kind,
+                                    _p(_lens(kv_lengths)), _p(dq), _p(dk), _p(dv),
+                                    B, H, Lq, Lk, D, scale), "oracle_mha_bwd")
+    return dq, dk, dv
 
 
 def layer_norm(x, gamma, beta, eps, path=None):

@@ -21,14 +21,19 @@
  *  - "Why attention must compute the max first" essay (gsyq.cn/news/340375),
  *    section 2.1: three-pass softmax (max, exp-sum, divide); section 3.1:
  *    every shifted logit is <= 0, so every exponential is in [0, 1];
- *    section 5.2: logits are divided by sqrt(d_k).
+ *    section 5.2: logits are divided by sqrt(d_k); section 3.3: the softmax
+ *    Jacobian d p_j / d s_k = p_j (delta_jk - p_k), used by the backward
+ *    pass (oracle_mha_bwd) together with the row log-sum-exp (oracle_mha_lse).
  *
  * Readings taken where the pages are silent (each is listed in the design doc):
  *  - scale is passed explicitly (the kernels' default is 1/sqrt(D));
  *  - causal alignment is top-left: key j is visible to query i iff j <= i;
  *  - the padding mask hides keys j >= len_b; query rows are all computed;
  *  - len_b is clamped to [0, Lk];
- *  - a row with no visible key returns a row of zeros;
+ *  - a row with no visible key returns a row of zeros (and so passes no
+ *    gradient back: its output is a constant);
+ *  - the backward pass is the gradient of L = sum(dout * O) with respect to
+ *    q, k and v, in the same fp64 arithmetic;
  *  - LayerNorm uses the biased variance (divide by N) and eps inside the
  *    square root; Q is the head slice of LN(x), with no projection after it.
  *
@@ -345,3 +350,122 @@ int oracle_prenorm_residual_rows(const double *x, const double *gamma,
     return 0;
 }
 
+
+/*
+ * Log-sum-exp of each row's scaled logits over its visible keys, the softmax
+ * statistic a backward pass recomputes the weights from:
+ *     lse[b,h,i] = log sum_{visible j} exp(s_ij),   s_ij = scale * q_i . k_j,
+ * taken as M + log(sum exp(s_ij - M)) with M the row maximum (the max-first
+ * order of the gsyq.cn essay "Why attention must compute the max first",
+ * sections 2.1 and 3.1).  A row with no visible key gets -INFINITY.
+ * q [B,H,Lq,D], k [B,H,Lk,D], lse [B,H,Lq].
+ */
+int oracle_mha_lse(const double *q, const double *k, int mask_kind,
+                   const int32_t *kv_lengths, double *lse,
+                   int B, int H, int Lq, int Lk, int D, double scale) {
+    if (bad_shape(B, H, Lq, Lk, D)) return -1;
+    int fail = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : fail)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            double *s = (double *)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
+            if (!s) { fail = 1; continue; }
+            size_t bh = (size_t)b * H + h;
+            const double *Q = q + bh * (size_t)Lq * D;
+            const double *K = k + bh * (size_t)Lk * D;
+            int len = visible_len(mask_kind, kv_lengths, b, Lk);
+            for (int i = 0; i < Lq; ++i) {
+                double M = -INFINITY;
+                int any = 0;
+                for (int j = 0; j < Lk; ++j) {
+                    if (!key_visible(i, j, mask_kind, len)) continue;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += Q[(size_t)i * D + d] * K[(size_t)j * D + d];
+                    s[j] = dot * scale;
+                    if (!any || M < s[j]) M = s[j];
+                    any = 1;
+                }
+                if (!any) { lse[bh * Lq + (size_t)i] = -INFINITY; continue; }
+                double Z = 0.0;
+                for (int j = 0; j < Lk; ++j)
+                    if (key_visible(i, j, mask_kind, len)) Z += exp(s[j] - M);
+                lse[bh * Lq + (size_t)i] = M + log(Z);
+            }
+            free(s);
+        }
+    }
+    return fail ? -2 : 0;
+}
+
+/*
+ * Gradients of the forward above for the loss L = sum(dout * O), i.e. the
+ * backward pass: dq [B,H,Lq,D], dk and dv [B,H,Lk,D] from dout [B,H,Lq,D].
+ * Per query row i the softmax row p_i is formed again (attend_row), then the
+ * softmax Jacobian of the gsyq.cn essay, section 3.3,
+ *     d p_ij / d s_ik = p_ij (delta_jk - p_ik),
+ * is applied to dP_ij = dL/dp_ij = dout_i . v_j:
+ *     c_i   = sum_j p_ij dP_ij
+ *     dS_ij = p_ij (dP_ij - c_i)
+ * and the three products are accumulated over the visible keys j:
+ *     dv_j += p_ij dout_i
+ *     dq_i += scale * dS_ij k_j
+ *     dk_j += scale * dS_ij q_i
+ * Hidden keys have p_ij = 0 and receive nothing; a row with no visible key
+ * has a constant (zero) output and contributes nothing.
+ */
+int oracle_mha_bwd(const double *q, const double *k, const double *v,
+                   const double *dout, int mask_kind, const int32_t *kv_lengths,
+                   double *dq, double *dk, double *dv,
+                   int B, int H, int Lq, int Lk, int D, double scale) {
+    if (bad_shape(B, H, Lq, Lk, D)) return -1;
+    int fail = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : fail)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            size_t nk = (size_t)(Lk > 0 ? Lk : 1);
+            double *s = (double *)malloc(sizeof(double) * nk);
+            double *p = (double *)malloc(sizeof(double) * nk);
+            double *dP = (double *)malloc(sizeof(double) * nk);
+            double *o = (double *)malloc(sizeof(double) * (size_t)D);
+            if (!s || !p || !dP || !o) {
+                free(s); free(p); free(dP); free(o);
+                fail = 1;
+                continue;
+            }
+            size_t bh = (size_t)b * H + h;
+            const double *Q = q + bh * (size_t)Lq * D;
+            const double *K = k + bh * (size_t)Lk * D;
+            const double *V = v + bh * (size_t)Lk * D;
+            const double *dO = dout + bh * (size_t)Lq * D;
+            double *dQ = dq + bh * (size_t)Lq * D;
+            double *dK = dk + bh * (size_t)Lk * D;
+            double *dV = dv + bh * (size_t)Lk * D;
+            for (size_t e = 0; e < (size_t)Lq * D; ++e) dQ[e] = 0.0;
+            for (size_t e = 0; e < (size_t)Lk * D; ++e) { dK[e] = 0.0; dV[e] = 0.0; }
+            int len = visible_len(mask_kind, kv_lengths, b, Lk);
+            for (int i = 0; i < Lq; ++i) {
+                const double *qi = Q + (size_t)i * D;
+                const double *gi = dO + (size_t)i * D;
+                attend_row(qi, K, V, Lk, D, scale, mask_kind, len, i, s, o, p);
+                double c = 0.0;
+                for (int j = 0; j < Lk; ++j) {
+                    dP[j] = 0.0;
+                    if (!key_visible(i, j, mask_kind, len)) continue;
+                    for (int d = 0; d < D; ++d) dP[j] += gi[d] * V[(size_t)j * D + d];
+                    c += p[j] * dP[j];
+                }
+                for (int j = 0; j < Lk; ++j) {
+                    if (!key_visible(i, j, mask_kind, len)) continue;
+                    double dS = p[j] * (dP[j] - c);
+                    for (int d = 0; d < D; ++d) {
+                        dV[(size_t)j * D + d] += p[j] * gi[d];
+                        dQ[(size_t)i * D + d] += scale * dS * K[(size_t)j * D + d];
+                        dK[(size_t)j * D + d] += scale * dS * qi[d];
+                    }
+                }
+            }
+            free(s); free(p); free(dP); free(o);
+        }
+    }
+    return fail ? -2 : 0;
+}

@@ -333,10 +333,149 @@ def check_prenorm_residual(path=None):
     return None
 
 
+def _loss(q, k, v, g, mk, lens, sc, path):
+    return float((oracle.mha_fwd(q, k, v, mk, lens, sc, path=path) * g).sum())
+
+
+def check_bwd_finite_difference(path=None):
+    """Every gradient element against a central difference of the (pinned)
+    forward oracle's loss sum(dout * O): error O(eps^2), far below 1e-8.
+    Covers all masks, Lq != Lk both ways and a batch with no visible key."""
+    r = _rng(21)
+    eps = 1e-5
+    cases = [(1, 1, 1, 1, 1, 0, None), (2, 2, 5, 6, 3, 0, None), (2, 2, 5, 6, 3, 1, None),
+             (2, 2, 5, 6, 3, 2, [4, 0]), (2, 1, 5, 6, 3, 3, [2, 6]), (1, 2, 4, 7, 2, 1, None),
+             (1, 2, 6, 3, 2, 3, [3])]
+    for (B, H, Lq, Lk, D, mk, lens) in cases:
+        q, k, v = (r.standard_normal((B, H, L, D)) for L in (Lq, Lk, Lk))
+        g = r.standard_normal((B, H, Lq, D))
+        lens = None if lens is None else np.array(lens, np.int32)
+        sc = 0.8
+        grads = oracle.mha_bwd(q, k, v, g, mk, lens, sc, path=path)
+        for name, x, gx in zip("qkv", (q, k, v), grads):
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += eps
+                xm[idx] -= eps
+                args_p = [q, k, v]
+                args_m = [q, k, v]
+                args_p["qkv".index(name)] = xp
+                args_m["qkv".index(name)] = xm
+                fd = (_loss(*args_p, g, mk, lens, sc, path) -
+                      _loss(*args_m, g, mk, lens, sc, path)) / (2 * eps)
+                if abs(fd - gx[idx]) > 1e-8:
+                    return "d%s%s: oracle %.12g, finite difference %.12g (case %s)" % (
+                        name, idx, gx[idx], fd, (B, H, Lq, Lk, D, mk))
+    return None
+
+
+def check_bwd_autograd(path=None):
+    """Against torch autograd through fp64 SDPA with the same boolean mask
+    (library routine); every row keeps at least one visible key."""
+    r = _rng(22)
+    for (B, H, Lq, Lk, D) in [(2, 3, 17, 23, 8), (1, 2, 40, 40, 16)]:
+        for mk in (0, 1, 2, 3):
+            q, k, v = (r.standard_normal((B, H, L, D)) for L in (Lq, Lk, Lk))
+            g = r.standard_normal((B, H, Lq, D))
+            lens = r.integers(1, Lk + 1, size=B).astype(np.int32) if mk & 2 else None
+            sc = 0.3
+            got = oracle.mha_bwd(q, k, v, g, mk, lens, sc, path=path)
+            t = [torch.from_numpy(a.copy()).requires_grad_(True) for a in (q, k, v)]
+            vis = torch.from_numpy(_visible(mk, lens, B, Lq, Lk))[:, None]
+            o = torch.nn.functional.scaled_dot_product_attention(*t, attn_mask=vis, scale=sc)
+            o.backward(torch.from_numpy(g))
+            for name, a, tt in zip("qkv", got, t):
+                err = np.abs(a - tt.grad.numpy()).max()
+                if err > 1e-12:
+                    return "d%s differs from autograd by %g (shape %s mask %d)" % (
+                        name, err, (B, H, Lq, Lk, D), mk)
+    return None
+
+
+def check_bwd_invariants(path=None):
+    """Closed forms: softmax rows sum to one, so sum_j dv_j = sum of dout over
+    rows with a visible key, and shifting every key by one vector leaves O
+    unchanged, so sum_j dk_j = 0; hidden keys get exactly zero gradient; with
+    a single key O = v_0 for every row, so dq = dk = 0 and dv_0 = sum_i dout_i;
+    with q = 0 the weights are uniform over the n_i visible keys, so
+    dv_j = sum_{i sees j} dout_i / n_i."""
+    r = _rng(23)
+    B, H, Lq, Lk, D = 3, 2, 19, 26, 5
+    q, k, v = (r.standard_normal((B, H, L, D)) for L in (Lq, Lk, Lk))
+    g = r.standard_normal((B, H, Lq, D))
+    lens = np.array([9, 0, 26], np.int32)
+    for mk in (2, 3):
+        dq, dk, dv = oracle.mha_bwd(q, k, v, g, mk, lens, 0.5, path=path)
+        vis = _visible(mk, lens, B, Lq, Lk)
+        rows = vis.any(axis=2)
+        for b in range(B):
+            want = (g[b] * rows[b][None, :, None]).sum(axis=1)
+            if np.abs(dv[b].sum(axis=1) - want).max() > 1e-12:
+                return "sum of dv is not the sum of dout (mask %d, batch %d)" % (mk, b)
+            if np.abs(dk[b].sum(axis=1)).max() > 1e-12:
+                return "sum of dk is not zero (mask %d, batch %d)" % (mk, b)
+            hidden = ~vis[b].any(axis=0)
+            if np.any(dk[b][:, hidden] != 0) or np.any(dv[b][:, hidden] != 0):
+                return "a hidden key received gradient (mask %d, batch %d)" % (mk, b)
+            if not rows[b].all() and np.any(dq[b][:, ~rows[b]] != 0):
+                return "a row with no visible key passed gradient to q"
+    k1, v1 = r.standard_normal((1, 2, 1, D)), r.standard_normal((1, 2, 1, D))
+    q1, g1 = r.standard_normal((1, 2, 7, D)), r.standard_normal((1, 2, 7, D))
+    dq, dk, dv = oracle.mha_bwd(q1, k1, v1, g1, 0, None, 0.5, path=path)
+    if np.abs(dq).max() > 1e-13 or np.abs(dk).max() > 1e-13:
+        return "single key: dq/dk not zero"
+    if np.abs(dv[0, :, 0] - g1[0].sum(axis=1)).max() > 1e-12:
+        return "single key: dv is not the sum of dout"
+    z = np.zeros((B, H, Lq, D))
+    for mk in (0, 1, 3):
+        _, _, dv = oracle.mha_bwd(z, k, v, g, mk, lens, 0.5, path=path)
+        vis = _visible(mk, lens, B, Lq, Lk).astype(float)
+        n = vis.sum(axis=2, keepdims=True)
+        w = np.divide(vis, n, out=np.zeros_like(vis), where=n > 0)
+        want = np.einsum("bij,bhid->bhjd", w, g)
+        if np.abs(dv - want).max() > 1e-12:
+            return "q = 0: dv is not the uniform-weight sum (mask %d)" % mk
+    return None
+
+
+def check_lse(path=None):
+    """Row log-sum-exp: brute force with plain exp/log on small logits; q = 0
+    gives log(number of visible keys); no visible key gives -inf; huge logits
+    (exp would overflow) give max + log(1 + sum exp(s - max)) exactly."""
+    r = _rng(24)
+    B, H, Lq, Lk, D = 2, 2, 6, 5, 3
+    q, k = r.standard_normal((B, H, Lq, D)), r.standard_normal((B, H, Lk, D))
+    lens = np.array([3, 0], np.int32)
+    for mk in (0, 1, 2, 3):
+        got = oracle.mha_lse(q, k, mk, lens, 0.7, path=path)
+        vis = _visible(mk, lens, B, Lq, Lk)
+        for b, h, i in np.ndindex(B, H, Lq):
+            js = [j for j in range(Lk) if vis[b, i, j]]
+            if not js:
+                if got[b, h, i] != -np.inf:
+                    return "empty row lse %r" % got[b, h, i]
+                continue
+            want = math.log(sum(math.exp(0.7 * float(q[b, h, i] @ k[b, h, j])) for j in js))
+            if abs(got[b, h, i] - want) > 1e-13:
+                return "lse brute force (%d,%d,%d) mask %d: %r vs %r" % (b, h, i, mk, got[b, h, i], want)
+    z = oracle.mha_lse(np.zeros((B, H, Lq, D)), k, 3, np.array([4, 2], np.int32), 0.7, path=path)
+    n = _visible(3, np.array([4, 2]), B, Lq, Lk).sum(axis=2)
+    if np.abs(z - np.log(n)[:, None, :]).max() > 1e-14:
+        return "q = 0: lse is not log(n)"
+    qh = np.array([[[[1.0]]]])
+    kh = np.array([[[[1000.0], [999.0], [-5.0]]]])
+    got = oracle.mha_lse(qh, kh, 0, None, 1.0, path=path)[0, 0, 0]
+    want = 1000.0 + math.log1p(math.exp(-1.0) + math.exp(-1005.0))
+    if not np.isfinite(got) or abs(got - want) > 1e-12:
+        return "large logits: lse %r want %r" % (got, want)
+    return None
+
+
 ALL = [check_brute_force, check_sdpa, check_golden, check_shift_invariance,
        check_rows_sum_to_one, check_zero_query_is_mean, check_causal_rules,
        check_padding_rules, check_hard_max_and_overflow, check_rows_api,
-       check_layer_norm, check_prenorm, check_prenorm_residual]
+       check_layer_norm, check_prenorm, check_prenorm_residual, check_bwd_finite_difference,
+       check_bwd_autograd, check_bwd_invariants, check_lse]
 
 
 def run_all(path=None):

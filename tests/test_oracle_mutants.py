@@ -35,6 +35,14 @@ MUTANTS = [
     ("residual_rows_wrong_head",
      "(size_t)i) * (size_t)H * D + (size_t)h * D;\n        for (int d = 0;",
      "(size_t)i) * (size_t)H * D;\n        for (int d = 0;"),
+    ("bwd_drop_row_term", "double dS = p[j] * (dP[j] - c);", "double dS = p[j] * dP[j];"),
+    ("bwd_row_term_sign", "c += p[j] * dP[j];", "c -= p[j] * dP[j];"),
+    ("bwd_dP_uses_k", "dP[j] += gi[d] * V[", "dP[j] += gi[d] * K["),
+    ("bwd_dq_uses_v", "dQ[(size_t)i * D + d] += scale * dS * K[", "dQ[(size_t)i * D + d] += scale * dS * V["),
+    ("bwd_dk_unscaled", "dK[(size_t)j * D + d] += scale * dS * qi[d];",
+     "dK[(size_t)j * D + d] += dS * qi[d];"),
+    ("bwd_dv_uses_dS", "dV[(size_t)j * D + d] += p[j] * gi[d];", "dV[(size_t)j * D + d] += dS * gi[d];"),
+    ("lse_drops_max", "lse[bh * Lq + (size_t)i] = M + log(Z);", "lse[bh * Lq + (size_t)i] = log(Z);"),
 ]
 
 
