@@ -42,13 +42,14 @@ KERNEL_OF = {  # dominant kernel of each workload
     "mha:bf16": "attn_fwd_bf16_kernel",
     "prenorm:bf16": "attn_fwd_bf16_kernel<prenorm>",
     "prenorm_residual:bf16": "attn_fwd_bf16_kernel<prenorm>",
+    "mha_bwd:f32": "mha_bwd_f32_kernel",
 }
 SMALL_F32_MAX_KD = 16384   # the fp32 path stages all keys at once when Lk * D is at most this
 DECODE_MAX_ROWS = 8        # bf16 self-attention with at most this many query rows: decode kernel
 
 
 def kernel_of(w):
-    if w.dtype == "f32" and w.Lk * w.D <= SMALL_F32_MAX_KD:
+    if w.kind == "mha" and w.dtype == "f32" and w.Lk * w.D <= SMALL_F32_MAX_KD:
         return "mha_fwd_f32_small_kernel"
     if w.kind == "mha" and w.dtype == "bf16" and w.Lq <= DECODE_MAX_ROWS:
         return "attn_decode_bf16_kernel"
@@ -62,23 +63,38 @@ def visible_lengths(w, lens):
     return [max(0, min(int(x), w.Lk)) for x in lens]
 
 
+def flops_per_pair(w):
+    """FLOP per (query row, key, feature): 4 for the forward (QK^T and PV);
+    10 for the backward (S = QK^T and dP = dout V^T formed again, then dV,
+    dK and dQ: five products of 2 FLOP each)."""
+    return 10.0 if w.kind == "mha_bwd" else 4.0
+
+
 def mask_aware_flops(w, lens):
-    """4*B*H*Lq*Lk*D halved for causal; for kv lengths 4*H*D*Lq*sum(len)."""
+    """4*B*H*Lq*Lk*D halved for causal; for kv lengths 4*H*D*Lq*sum(len)
+    (10 instead of 4 for the backward)."""
+    c = flops_per_pair(w)
     if w.mask & synthetic.MASK_KV_LEN:
-        f = 4.0 * w.H * w.D * w.Lq * sum(visible_lengths(w, lens))
+        f = c * w.H * w.D * w.Lq * sum(visible_lengths(w, lens))
         return f / 2 if w.mask & synthetic.MASK_CAUSAL else f
-    f = 4.0 * w.B * w.H * w.Lq * w.Lk * w.D
+    f = c * w.B * w.H * w.Lq * w.Lk * w.D
     return f / 2 if w.mask & synthetic.MASK_CAUSAL else f
 
 
 def nominal_flops(w):
-    return 4.0 * w.B * w.H * w.Lq * w.Lk * w.D
+    return flops_per_pair(w) * w.B * w.H * w.Lq * w.Lk * w.D
 
 
 def algorithmic_bytes(w, lens):
-    """Bytes a perfect kernel moves: Q (or x) and O once, K/V of visible keys once."""
+    """Bytes a perfect kernel moves: Q (or x) and O once, K/V of visible keys
+    once.  Backward: q, o, dout, lse read and dq written once; K/V of visible
+    keys read once; dk, dv written once for every key."""
     e = 4 if w.dtype == "f32" else 2
     kv_rows = sum(visible_lengths(w, lens)) * w.H
+    if w.kind == "mha_bwd":
+        rows_q = w.B * w.H * w.Lq
+        return (4 * rows_q * w.D * e + 4 * rows_q + 2 * kv_rows * w.D * e
+                + 2 * w.B * w.H * w.Lk * w.D * e)
     qo = 2 * w.B * w.H * w.Lq * w.D * e
     extra = 2 * 4 * w.H * w.D if w.kind != "mha" else 0   # gamma, beta
     return qo + 2 * kv_rows * w.D * e + extra
@@ -185,11 +201,14 @@ class GpuWorkload:
         self.host = synthetic.make(w, seed)
         self.lens = None if self.host["kv_lengths"] is None else self.host["kv_lengths"].tolist()
         self.device = device
-        keys = ["q", "k", "v"] if w.kind == "mha" else ["x", "gamma", "beta", "k", "v"]
+        keys = {"mha": ["q", "k", "v"], "mha_bwd": ["q", "k", "v", "dout"]}.get(
+            w.kind, ["x", "gamma", "beta", "k", "v"])
         self.in_keys = keys
         set_bytes = sum(self.host[k].numel() * self.host[k].element_size() for k in keys)
-        out_like = self.host["q"] if w.kind == "mha" else self.host["x"]
+        out_like = self.host["q"] if w.kind in ("mha", "mha_bwd") else self.host["x"]
         set_bytes += out_like.numel() * out_like.element_size()
+        if w.kind == "mha_bwd":   # o and lse (inputs), dq, dk, dv (outputs)
+            set_bytes += 3 * out_like.numel() * 4 + self.host["k"].numel() * 8
         self.set_bytes = set_bytes
         n = max(1, math.ceil(2 * l2_bytes / set_bytes))
         n = max(1, min(n, max_bytes // set_bytes))
@@ -200,6 +219,15 @@ class GpuWorkload:
             self.sets.append(s)
         self.kv = None if self.host["kv_lengths"] is None else self.host["kv_lengths"].to(device)
         self.i = 0
+        if w.kind == "mha_bwd":
+            # The forward's output and row statistic are inputs of the backward
+            # step; they are formed once, outside any timed region.
+            for s in self.sets:
+                s["o"], s["lse"] = mha.mha_fwd_lse(s["q"], s["k"], s["v"], w.mask, self.kv,
+                                                   scale=w.scale)
+                s["dk"] = torch.empty_like(s["k"])
+                s["dv"] = torch.empty_like(s["v"])
+            torch.cuda.synchronize()
 
     def step(self, s=None):
         w = self.w
@@ -208,6 +236,9 @@ class GpuWorkload:
             self.i += 1
         if w.kind == "mha":
             self.mha.mha_fwd(s["q"], s["k"], s["v"], w.mask, self.kv, out=s["out"], scale=w.scale)
+        elif w.kind == "mha_bwd":   # s["out"] receives dq
+            self.mha.mha_bwd(s["q"], s["k"], s["v"], s["o"], s["dout"], s["lse"], w.mask, self.kv,
+                             dq=s["out"], dk=s["dk"], dv=s["dv"], scale=w.scale)
         elif w.kind == "prenorm":
             self.mha.prenorm_cross_attn_fwd(s["x"], s["gamma"], s["beta"], w.eps, s["k"], s["v"],
                                             self.kv, out=s["out"], scale=w.scale)
@@ -223,7 +254,10 @@ class GpuWorkload:
 
     def output_bytes(self):
         o = self.sets[0]["out"]
-        return o.numel() * o.element_size()
+        n = o.numel() * o.element_size()
+        if self.w.kind == "mha_bwd":
+            n += 2 * self.sets[0]["dk"].numel() * 4
+        return n
 
 
 def time_steps(wl, steps, warmup, sync_ranks=None):
@@ -324,10 +358,12 @@ def oracle_sample(w, host, budget_s, max_problems=None):
     BH = w.B * w.H
     # (b, h) problems as a flat batch of single-head problems.
     plens = None if lens is None else np.repeat(lens, w.H).astype(np.int32)
-    if w.kind == "mha":
+    if w.kind in ("mha", "mha_bwd"):
         q = host["q"].float().numpy().reshape(BH, 1, w.Lq, w.D)
         k = host["k"].float().numpy().reshape(BH, 1, w.Lk, w.D)
         v = host["v"].float().numpy().reshape(BH, 1, w.Lk, w.D)
+        if w.kind == "mha_bwd":
+            g = host["dout"].float().numpy().reshape(BH, 1, w.Lq, w.D)
     else:
         x = host["x"].float().numpy()
         k, v = host["k"].float().numpy(), host["v"].float().numpy()
@@ -345,6 +381,8 @@ def oracle_sample(w, host, budget_s, max_problems=None):
         t0 = time.perf_counter()
         if w.kind == "mha":
             oracle.mha_fwd(q[p0:p1], k[p0:p1], v[p0:p1], w.mask, lb, w.scale)
+        elif w.kind == "mha_bwd":
+            oracle.mha_bwd(q[p0:p1], k[p0:p1], v[p0:p1], g[p0:p1], w.mask, lb, w.scale)
         else:
             rows = np.array([(pp // w.H, pp % w.H, i) for pp in range(p0, p1)
                              for i in range(w.Lq)], np.int64)

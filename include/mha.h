@@ -22,9 +22,10 @@
  *
  * Conventions for every entry point.
  *  - Pointers are DEVICE pointers owned by the caller; the library keeps no
- *    per-call state.  mha_fwd allocates no device memory;
+ *    per-call state.  mha_fwd and mha_fwd_lse allocate no device memory;
  *    prenorm_cross_attn_fwd takes a stream-ordered workspace of 8*B*Lq bytes
- *    (cudaMallocAsync / cudaFreeAsync on `stream`) for the row statistics.
+ *    and mha_bwd one of 4*B*H*Lq bytes (cudaMallocAsync / cudaFreeAsync on
+ *    `stream`) for per-row statistics.
  *  - Layouts are dense and row-major: q, out [B,H,Lq,D]; k, v [B,H,Lk,D];
  *    kv_lengths int32 [B].  Every tensor pointer must be 16-byte aligned.
  *  - Work is enqueued on `stream` (0 = legacy default stream); no entry
@@ -90,6 +91,53 @@ enum { MHA_F32 = 0, MHA_BF16 = 1 };
 MHA_API int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
             const int32_t *kv_lengths, void *out, int B, int H, int Lq, int Lk,
             int D, float scale, int dtype, cudaStream_t stream);
+
+/*
+ * mha_fwd_lse -- mha_fwd that also writes each row's log-sum-exp, the
+ * statistic the backward pass forms the softmax weights from again:
+ *     lse[b,h,i] = log sum_{visible j} exp(s_ij)   (natural log, fp32)
+ * and -INFINITY for a row with no visible key.  ("Why attention must compute
+ * the max first", gsyq.cn, sections 2.1 and 3.1: it is the row maximum plus
+ * the log of the shifted sum, both already held by the online softmax.)
+ *   lse         device fp32 [B,H,Lq], 16-byte aligned, written once.
+ *   dtype       must be MHA_F32 (MHA_ERR_UNSUPPORTED otherwise).
+ * Other arguments, layouts and errors as for mha_fwd.
+ */
+MHA_API int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_kind,
+                        const int32_t *kv_lengths, void *out, float *lse, int B, int H,
+                        int Lq, int Lk, int D, float scale, int dtype, cudaStream_t stream);
+
+/*
+ * mha_bwd -- backward pass of mha_fwd: the gradients of the loss
+ * sum(dout * O) with respect to q, k and v.  With p_ij the softmax weight
+ * (formed again as exp(s_ij - lse_i) at visible positions, exactly 0 at
+ * hidden ones) and the softmax Jacobian d p_ij / d s_ik = p_ij (delta_jk -
+ * p_ik) ("Why attention must compute the max first", gsyq.cn, section 3.3):
+ *     dP_ij = dout_i . v_j,   Delta_i = dout_i . o_i  (= sum_j p_ij dP_ij)
+ *     dS_ij = p_ij (dP_ij - Delta_i)
+ *     dv_j = sum_i p_ij dout_i
+ *     dq_i = scale * sum_j dS_ij k_j,   dk_j = scale * sum_i dS_ij q_i
+ * A row with no visible key passes no gradient; a key no row can see gets
+ * zero dk and dv.
+ *   q, k, v, mask_kind, kv_lengths, B, H, Lq, Lk, D, scale
+ *               exactly as given to the forward call.
+ *   out         the forward's output O [B,H,Lq,D].
+ *   dout        dL/dO [B,H,Lq,D].
+ *   lse         the forward's row log-sum-exp [B,H,Lq] (mha_fwd_lse).
+ *   dq          [B,H,Lq,D]; dk, dv [B,H,Lk,D]: outputs, fully written (dq
+ *               is zeroed and then accumulated with fp32 atomic adds, so
+ *               its last bits can differ between runs).  Must not alias
+ *               any input.
+ *   dtype       must be MHA_F32 (MHA_ERR_UNSUPPORTED otherwise).
+ * Memory: a stream-ordered workspace of 4*B*H*Lq bytes (cudaMallocAsync /
+ * cudaFreeAsync on `stream`) holds Delta.  Two kernels run on `stream`: a
+ * row pass (Delta, dq = 0) and the key-tile kernel.  Lq == 0 with Lk > 0
+ * writes zero dk and dv.  Returns MHA_OK or a negative mha_status.
+ */
+MHA_API int mha_bwd(const void *q, const void *k, const void *v, const void *out,
+                    const void *dout, const float *lse, int mask_kind,
+                    const int32_t *kv_lengths, void *dq, void *dk, void *dv, int B, int H,
+                    int Lq, int Lk, int D, float scale, int dtype, cudaStream_t stream);
 
 /*
  * prenorm_cross_attn_fwd -- Pre-LayerNorm cross-attention forward

@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) fused masked multi-head attention forward.
+"""GB300 (sm_103a) fused masked multi-head attention: forward, decode and backward.
 
 Thin ctypes binding over the C ABI of libmha.so (include/mha.h).  Every step
 of the computation runs in the library's CUDA kernels; this module only
@@ -50,6 +50,10 @@ def lib():
         L.prenorm_cross_attn_fwd.restype = i
         L.prenorm_cross_attn_residual_fwd.argtypes = [P, P, P, f, P, P, P, P, i, i, i, i, i, f, i, P]
         L.prenorm_cross_attn_residual_fwd.restype = i
+        L.mha_fwd_lse.argtypes = [P, P, P, i, P, P, P, i, i, i, i, i, f, i, P]
+        L.mha_fwd_lse.restype = i
+        L.mha_bwd.argtypes = [P, P, P, P, P, P, i, P, P, P, P, i, i, i, i, i, f, i, P]
+        L.mha_bwd.restype = i
         L.mha_strerror.argtypes = [i]
         L.mha_strerror.restype = ctypes.c_char_p
         L.mha_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
@@ -143,6 +147,65 @@ def mha_fwd(q, k, v, mask_kind=MASK_NONE, kv_lengths=None, out=None, scale=None,
                          B, H, Lq, Lk, D, scale, _dtype_code(q), _stream(stream, q.get_device())),
            "mha_fwd")
     return out
+
+
+def mha_fwd_lse(q, k, v, mask_kind=MASK_NONE, kv_lengths=None, out=None, lse=None, scale=None,
+                stream=None):
+    """mha_fwd that also returns each row's log-sum-exp (fp32 inputs only).
+
+    Returns (out [B,H,Lq,D], lse [B,H,Lq] fp32, natural log, -inf for a row
+    with no visible key)."""
+    torch = _torch()
+    _dev(q, "q", torch.float32)
+    _dev(k, "k", torch.float32)
+    _dev(v, "v", torch.float32)
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    if tuple(k.shape) != (B, H, Lk, D) or tuple(v.shape) != (B, H, Lk, D):
+        raise ValueError("k and v must be [B,H,Lk,D] matching q")
+    if kv_lengths is not None:
+        _dev(kv_lengths, "kv_lengths", torch.int32)
+    out = torch.empty_like(q) if out is None else _dev(out, "out", q.dtype)
+    if lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    else:
+        _dev(lse, "lse", torch.float32)
+        if tuple(lse.shape) != (B, H, Lq):
+            raise ValueError("lse must be [B,H,Lq]")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(lib().mha_fwd_lse(_ptr(q), _ptr(k), _ptr(v), int(mask_kind), _ptr(kv_lengths),
+                             _ptr(out), _ptr(lse), B, H, Lq, Lk, D, scale, F32,
+                             _stream(stream, q.get_device())), "mha_fwd_lse")
+    return out, lse
+
+
+def mha_bwd(q, k, v, out, dout, lse, mask_kind=MASK_NONE, kv_lengths=None, dq=None, dk=None,
+            dv=None, scale=None, stream=None):
+    """Gradients (dq, dk, dv) of sum(dout * out) for out, lse = mha_fwd_lse(q, k, v, ...).
+
+    fp32 only; every tensor contiguous on the same device.  q, k, v,
+    mask_kind, kv_lengths and scale must be those of the forward call."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (lse, "lse")):
+        _dev(t, n, torch.float32)
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    if tuple(k.shape) != (B, H, Lk, D) or tuple(v.shape) != (B, H, Lk, D):
+        raise ValueError("k and v must be [B,H,Lk,D] matching q")
+    if tuple(out.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("out and dout must have the shape of q")
+    if tuple(lse.shape) != (B, H, Lq):
+        raise ValueError("lse must be [B,H,Lq]")
+    if kv_lengths is not None:
+        _dev(kv_lengths, "kv_lengths", torch.int32)
+    dq = torch.empty_like(q) if dq is None else _dev(dq, "dq", torch.float32)
+    dk = torch.empty_like(k) if dk is None else _dev(dk, "dk", torch.float32)
+    dv = torch.empty_like(v) if dv is None else _dev(dv, "dv", torch.float32)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(lib().mha_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                         int(mask_kind), _ptr(kv_lengths), _ptr(dq), _ptr(dk), _ptr(dv),
+                         B, H, Lq, Lk, D, scale, F32, _stream(stream, q.get_device())), "mha_bwd")
+    return dq, dk, dv
 
 
 def prenorm_cross_attn_fwd(x_q, gamma, beta, eps, k, v, kv_lengths=None, out=None, scale=None,

@@ -1,6 +1,6 @@
 // api.cu -- the extern "C" boundary of libmha.so: argument validation,
 // dispatch by (entry point, dtype, D), and status reporting.  Host code only;
-// the kernels live in fwd_f32.cu and fwd_bf16.cu.
+// the kernels live in fwd_f32.cu, fwd_bf16.cu, decode_bf16.cu and bwd_f32.cu.
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -47,8 +47,8 @@ int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
     if (dtype == MHA_F32)
         return from_cuda(mha::launch_fwd_f32(
             static_cast<const float *>(q), static_cast<const float *>(k),
-            static_cast<const float *>(v), kv_lengths, static_cast<float *>(out), B, H, Lq, Lk,
-            D, mask_kind, scale, stream));
+            static_cast<const float *>(v), kv_lengths, static_cast<float *>(out), nullptr, B, H,
+            Lq, Lk, D, mask_kind, scale, stream));
     mha::Bf16Call c{};
     c.q = q;
     c.k = k;
@@ -65,6 +65,64 @@ int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
     int drv = 0;
     cudaError_t e = mha::launch_fwd_bf16(c, stream, &drv, nullptr);
     if (drv != 0) return MHA_ERR_CUDA;
+    return from_cuda(e);
+}
+
+int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_kind,
+                const int32_t *kv_lengths, void *out, float *lse, int B, int H, int Lq, int Lk,
+                int D, float scale, int dtype, cudaStream_t stream) {
+    int empty = 0;
+    int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
+    if (st != MHA_OK) return st;
+    if (mask_kind < 0 || mask_kind > (MHA_MASK_CAUSAL | MHA_MASK_KV_LEN)) return MHA_ERR_INVALID_ARG;
+    if (dtype != MHA_F32) return MHA_ERR_UNSUPPORTED;
+    if (empty) return MHA_OK;
+    if (!q || !out || !lse || (Lk > 0 && (!k || !v))) return MHA_ERR_INVALID_ARG;
+    if ((mask_kind & MHA_MASK_KV_LEN) && !kv_lengths) return MHA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(lse) ||
+        (Lk > 0 && (!aligned16(k) || !aligned16(v))))
+        return MHA_ERR_MISALIGNED;
+    return from_cuda(mha::launch_fwd_f32(
+        static_cast<const float *>(q), static_cast<const float *>(k),
+        static_cast<const float *>(v), kv_lengths, static_cast<float *>(out), lse, B, H, Lq, Lk,
+        D, mask_kind, scale, stream));
+}
+
+int mha_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
+            const float *lse, int mask_kind, const int32_t *kv_lengths, void *dq, void *dk,
+            void *dv, int B, int H, int Lq, int Lk, int D, float scale, int dtype,
+            cudaStream_t stream) {
+    int empty = 0;
+    int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
+    if (st != MHA_OK) return st;
+    if (mask_kind < 0 || mask_kind > (MHA_MASK_CAUSAL | MHA_MASK_KV_LEN)) return MHA_ERR_INVALID_ARG;
+    if (dtype != MHA_F32) return MHA_ERR_UNSUPPORTED;
+    // Lq == 0 with keys present still owes zero dk and dv.
+    if (B == 0 || H == 0 || (Lq == 0 && Lk == 0)) return MHA_OK;
+    (void)empty;
+    if ((Lq > 0 && (!q || !out || !dout || !lse || !dq)) || (Lk > 0 && (!k || !v || !dk || !dv)))
+        return MHA_ERR_INVALID_ARG;
+    if ((mask_kind & MHA_MASK_KV_LEN) && !kv_lengths) return MHA_ERR_INVALID_ARG;
+    if ((Lq > 0 && (!aligned16(q) || !aligned16(out) || !aligned16(dout) || !aligned16(lse) ||
+                    !aligned16(dq))) ||
+        (Lk > 0 && (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))))
+        return MHA_ERR_MISALIGNED;
+    // Per-row Delta = dout . o lives in a stream-ordered workspace for this call.
+    float *delta = nullptr;
+    const size_t rows = (size_t)B * H * Lq;
+    if (rows > 0 && cudaMallocAsync(reinterpret_cast<void **>(&delta), sizeof(float) * rows,
+                                    stream) != cudaSuccess)
+        return MHA_ERR_CUDA;
+    cudaError_t e = mha::launch_bwd_f32(
+        static_cast<const float *>(q), static_cast<const float *>(k),
+        static_cast<const float *>(v), static_cast<const float *>(out),
+        static_cast<const float *>(dout), lse, kv_lengths, static_cast<float *>(dq),
+        static_cast<float *>(dk), static_cast<float *>(dv), delta, B, H, Lq, Lk, D, mask_kind,
+        scale, stream);
+    if (delta != nullptr) {
+        const cudaError_t ef = cudaFreeAsync(delta, stream);
+        if (e == cudaSuccess) e = ef;
+    }
     return from_cuda(e);
 }
 

@@ -1,0 +1,349 @@
+// bwd_f32.cu -- backward pass of fused masked multi-head attention for fp32
+// inputs on CUDA-core FFMA (sm_103a): dq, dk, dv from q, k, v, the forward's
+// output o, its row log-sum-exp lse and the output gradient dout.
+//
+// The softmax weights are never stored by the forward; here they are formed
+// again from the saved row statistic, p_ij = exp(s_ij - lse_i), and the
+// softmax Jacobian d p_ij / d s_ik = p_ij (delta_jk - p_ik) ("Why attention
+// must compute the max first", gsyq.cn, section 3.3) is applied as
+//     dS_ij = p_ij (dP_ij - Delta_i),  dP_ij = dout_i . v_j,
+// where Delta_i = sum_j p_ij dP_ij = dout_i . o_i (the two are equal because
+// o_i = sum_j p_ij v_j), so it costs one dot product per row instead of a
+// pass over the keys.
+//
+// Two kernels:
+//  1. bwd_row_delta: Delta_i = dout_i . o_i for every row, and dq zeroed (dq
+//     is accumulated by the second kernel).  HBM-bound, one pass.
+//  2. mha_bwd_f32_kernel: one CTA of 256 threads owns a 64-key tile of one
+//     (b, h) with K and V resident in shared memory, and walks the query
+//     tiles of 64 rows that can see any of its keys (under the causal rule:
+//     rows >= the tile's first key).  Per query tile it stages Q, dout, lse
+//     and Delta, forms S = Q K^T and dP = dout V^T together (each thread a
+//     4 x 4 block), P and dS, then accumulates dV += P^T dout and
+//     dK += dS^T Q in registers (each thread 4 keys x D/16 columns) and adds
+//     its share of dQ = dS K into global memory with 16-byte fp32 atomic
+//     adds.  dK (times scale) and dV are written once at the end; keys no
+//     row can see get zeros.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kBwdBM = 64;        // query rows per tile
+constexpr int kBwdBN = 64;        // keys per CTA
+constexpr int kBwdThreads = 256;  // 16 x 16: ty owns 4 rows (or keys), tx 4 columns
+
+template <int D>
+struct BwdCfg {
+    static constexpr int LD = D + 4;        // padded row stride of Q/K/V/dout tiles (floats)
+    static constexpr int LDP = kBwdBN + 4;  // padded row stride of the P and dS tiles
+    static constexpr int OC = D / 16;       // accumulator columns per thread
+    static constexpr size_t kSmem =
+        sizeof(float) * ((size_t)4 * 64 * LD + (size_t)2 * kBwdBM * LDP + 2 * kBwdBM);
+};
+
+// Rows [row0, row0 + 64) of a [rows, D] fp32 matrix into a padded tile;
+// rows at or beyond `nrows` become zero.
+template <int D>
+__device__ __forceinline__ void bwd_load_tile(float *dst, const float *__restrict__ src,
+                                              int row0, int nrows, int tid) {
+    constexpr int V4 = D / 4;
+#pragma unroll
+    for (int idx = tid; idx < 64 * V4; idx += kBwdThreads) {
+        const int r = idx / V4, c = idx % V4;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row0 + r < nrows)
+            val = __ldg(reinterpret_cast<const float4 *>(src + (size_t)(row0 + r) * D) + c);
+        *reinterpret_cast<float4 *>(dst + r * BwdCfg<D>::LD + 4 * c) = val;
+    }
+}
+
+// Delta_i = dout_i . o_i; dq_i = 0.  A half-warp (16 lanes) per row.
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_row_delta_kernel(const float *__restrict__ o, const float *__restrict__ dout,
+                         float *__restrict__ delta, float *__restrict__ dq, int64_t rows) {
+    constexpr int PER = D / 64;   // float4 per lane
+    const int64_t row = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4);
+    const int lane = threadIdx.x & 15;
+    float acc = 0.f;
+    if (row < rows) {
+        const float4 *po = reinterpret_cast<const float4 *>(o + row * D);
+        const float4 *pg = reinterpret_cast<const float4 *>(dout + row * D);
+        float4 *pq = reinterpret_cast<float4 *>(dq + row * D);
+#pragma unroll
+        for (int t = 0; t < PER; ++t) {
+            const float4 a = __ldg(po + lane + 16 * t), g = __ldg(pg + lane + 16 * t);
+            acc = fmaf(a.x, g.x, acc);
+            acc = fmaf(a.y, g.y, acc);
+            acc = fmaf(a.z, g.z, acc);
+            acc = fmaf(a.w, g.w, acc);
+            pq[lane + 16 * t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && lane == 0) delta[row] = acc;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
+    mha_bwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
+                       const float *__restrict__ v, const float *__restrict__ dout,
+                       const float *__restrict__ lse, const float *__restrict__ delta,
+                       const int32_t *__restrict__ kv_lengths, float *__restrict__ dq,
+                       float *__restrict__ dk, float *__restrict__ dv, int H, int Lq, int Lk,
+                       int mask_kind, float scale, float scale_log2) {
+    using C = BwdCfg<D>;
+    constexpr int OC = C::OC;
+    extern __shared__ float4 bwd_smem[];
+    float *sK = reinterpret_cast<float *>(bwd_smem);
+    float *sV = sK + 64 * C::LD;
+    float *sQ = sV + 64 * C::LD;
+    float *sG = sQ + 64 * C::LD;          // dout tile
+    float *sP = sG + 64 * C::LD;          // P  [query][key]
+    float *sS = sP + kBwdBM * C::LDP;     // dS [query][key]
+    float *sL = sS + kBwdBM * C::LDP;     // lse * log2(e) per query row
+    float *sDl = sL + kBwdBM;             // Delta per query row
+
+    // Key tile 0 (the heaviest under a causal mask) is launched first.
+    const int k0 = blockIdx.x * kBwdBN;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const size_t bh = (size_t)b * H + h;
+    const float *Qg = q + bh * (size_t)Lq * D;
+    const float *Kg = k + bh * (size_t)Lk * D;
+    const float *Vg = v + bh * (size_t)Lk * D;
+    const float *Gg = dout + bh * (size_t)Lq * D;
+    const float *Lg = lse + bh * (size_t)Lq;
+    const float *Dg = delta + bh * (size_t)Lq;
+    float *dQg = dq + bh * (size_t)Lq * D;
+
+    const bool causal = (mask_kind & 1) != 0;
+    int len = Lk;
+    if (mask_kind & 2) len = max(0, min((int)kv_lengths[b], Lk));
+    // Query tiles that can see a key of this tile: none if the tile starts at
+    // or past the valid length; under the causal rule rows >= k0 only.
+    const int n_qt = (Lq + kBwdBM - 1) / kBwdBM;
+    const int qt0 = causal ? k0 / kBwdBM : 0;
+    const int qt1 = (k0 < len) ? n_qt : qt0;
+
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+
+    float accv[4][OC], acck[4][OC];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < OC; ++c) {
+            accv[i][c] = 0.f;
+            acck[i][c] = 0.f;
+        }
+
+    if (qt0 < qt1) {
+        bwd_load_tile<D>(sK, Kg, k0, Lk, tid);
+        bwd_load_tile<D>(sV, Vg, k0, Lk, tid);
+    }
+
+    for (int qt = qt0; qt < qt1; ++qt) {
+        const int q0 = qt * kBwdBM;
+        __syncthreads();   // the previous tile is done with sQ, sG, sP, sS, sL, sDl
+        bwd_load_tile<D>(sQ, Qg, q0, Lq, tid);
+        bwd_load_tile<D>(sG, Gg, q0, Lq, tid);
+        if (tid < kBwdBM) {
+            const int row = q0 + tid;
+            sL[tid] = row < Lq ? Lg[row] * 1.4426950408889634f : 0.f;
+            sDl[tid] = row < Lq ? Dg[row] : 0.f;
+        }
+        __syncthreads();
+
+        // S = Q K^T and dP = dout V^T for rows ty*4 + i, keys tx + 16 j.
+        float s[4][4], dp[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                s[i][j] = 0.f;
+                dp[i][j] = 0.f;
+            }
+#pragma unroll 2
+        for (int d = 0; d < D; d += 4) {
+            float4 qa[4], ga[4], kb[4], vb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                qa[i] = *reinterpret_cast<const float4 *>(sQ + (ty * 4 + i) * C::LD + d);
+                ga[i] = *reinterpret_cast<const float4 *>(sG + (ty * 4 + i) * C::LD + d);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                kb[j] = *reinterpret_cast<const float4 *>(sK + (tx + 16 * j) * C::LD + d);
+                vb[j] = *reinterpret_cast<const float4 *>(sV + (tx + 16 * j) * C::LD + d);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    s[i][j] = fmaf(qa[i].x, kb[j].x, s[i][j]);
+                    s[i][j] = fmaf(qa[i].y, kb[j].y, s[i][j]);
+                    s[i][j] = fmaf(qa[i].z, kb[j].z, s[i][j]);
+                    s[i][j] = fmaf(qa[i].w, kb[j].w, s[i][j]);
+                    dp[i][j] = fmaf(ga[i].x, vb[j].x, dp[i][j]);
+                    dp[i][j] = fmaf(ga[i].y, vb[j].y, dp[i][j]);
+                    dp[i][j] = fmaf(ga[i].z, vb[j].z, dp[i][j]);
+                    dp[i][j] = fmaf(ga[i].w, vb[j].w, dp[i][j]);
+                }
+        }
+
+        // P = 2^(s * scale * log2(e) - lse * log2(e)) at visible positions, else
+        // exactly 0; dS = P (dP - Delta).  Only a tile crossing the visible end
+        // of a row (or the end of Lq) needs the element test.
+        const bool edge = (k0 + kBwdBN > len) || (causal && k0 + kBwdBN - 1 > q0) ||
+                          (q0 + kBwdBM > Lq);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rl = ty * 4 + i, row = q0 + rl;
+            const int vis_end = causal ? min(len, row + 1) : len;
+            const float l2 = sL[rl], dl = sDl[rl];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int key = k0 + tx + 16 * j;
+                float p = ex2_approx(fmaf(s[i][j], scale_log2, -l2));
+                if (edge && (key >= vis_end || row >= Lq)) p = 0.f;
+                sP[rl * C::LDP + tx + 16 * j] = p;
+                sS[rl * C::LDP + tx + 16 * j] = p * (dp[i][j] - dl);
+            }
+        }
+        __syncthreads();
+
+        // dV += P^T dout and dK += dS^T Q for keys ty*4 + i, columns tx*4 (+ 64).
+#pragma unroll 4
+        for (int r = 0; r < kBwdBM; ++r) {
+            const float4 pa = *reinterpret_cast<const float4 *>(sP + r * C::LDP + ty * 4);
+            const float4 sa = *reinterpret_cast<const float4 *>(sS + r * C::LDP + ty * 4);
+            const float pr[4] = {pa.x, pa.y, pa.z, pa.w};
+            const float sr[4] = {sa.x, sa.y, sa.z, sa.w};
+#pragma unroll
+            for (int hv = 0; hv < OC / 4; ++hv) {
+                const float4 g = *reinterpret_cast<const float4 *>(sG + r * C::LD + tx * 4 + 64 * hv);
+                const float4 qq = *reinterpret_cast<const float4 *>(sQ + r * C::LD + tx * 4 + 64 * hv);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    accv[i][4 * hv + 0] = fmaf(pr[i], g.x, accv[i][4 * hv + 0]);
+                    accv[i][4 * hv + 1] = fmaf(pr[i], g.y, accv[i][4 * hv + 1]);
+                    accv[i][4 * hv + 2] = fmaf(pr[i], g.z, accv[i][4 * hv + 2]);
+                    accv[i][4 * hv + 3] = fmaf(pr[i], g.w, accv[i][4 * hv + 3]);
+                    acck[i][4 * hv + 0] = fmaf(sr[i], qq.x, acck[i][4 * hv + 0]);
+                    acck[i][4 * hv + 1] = fmaf(sr[i], qq.y, acck[i][4 * hv + 1]);
+                    acck[i][4 * hv + 2] = fmaf(sr[i], qq.z, acck[i][4 * hv + 2]);
+                    acck[i][4 * hv + 3] = fmaf(sr[i], qq.w, acck[i][4 * hv + 3]);
+                }
+            }
+        }
+
+        // dQ (rows ty*4 + i, columns tx*4 (+ 64)) += scale * dS K, added to the
+        // global accumulator with one 16-byte atomic per 4 columns.
+        float accq[4][OC];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int c = 0; c < OC; ++c) accq[i][c] = 0.f;
+#pragma unroll 2
+        for (int j = 0; j < kBwdBN; j += 4) {
+            float4 sa[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                sa[i] = *reinterpret_cast<const float4 *>(sS + (ty * 4 + i) * C::LDP + j);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const float *krow = sK + (j + jj) * C::LD + tx * 4;
+#pragma unroll
+                for (int hv = 0; hv < OC / 4; ++hv) {
+                    const float4 kk = *reinterpret_cast<const float4 *>(krow + 64 * hv);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float w = jj == 0 ? sa[i].x : jj == 1 ? sa[i].y : jj == 2 ? sa[i].z : sa[i].w;
+                        accq[i][4 * hv + 0] = fmaf(w, kk.x, accq[i][4 * hv + 0]);
+                        accq[i][4 * hv + 1] = fmaf(w, kk.y, accq[i][4 * hv + 1]);
+                        accq[i][4 * hv + 2] = fmaf(w, kk.z, accq[i][4 * hv + 2]);
+                        accq[i][4 * hv + 3] = fmaf(w, kk.w, accq[i][4 * hv + 3]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = q0 + ty * 4 + i;
+            if (row >= Lq) continue;
+#pragma unroll
+            for (int hv = 0; hv < OC / 4; ++hv)
+                atomicAdd(reinterpret_cast<float4 *>(dQg + (size_t)row * D + tx * 4 + 64 * hv),
+                          make_float4(accq[i][4 * hv] * scale, accq[i][4 * hv + 1] * scale,
+                                      accq[i][4 * hv + 2] * scale, accq[i][4 * hv + 3] * scale));
+        }
+    }
+
+    // dK = scale * dS^T Q, dV = P^T dout for the tile's keys (zeros where no
+    // row could see the key).
+    float *dKg = dk + bh * (size_t)Lk * D;
+    float *dVg = dv + bh * (size_t)Lk * D;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int key = k0 + ty * 4 + i;
+        if (key >= Lk) continue;
+#pragma unroll
+        for (int hv = 0; hv < OC / 4; ++hv) {
+            const size_t off = (size_t)key * D + tx * 4 + 64 * hv;
+            *reinterpret_cast<float4 *>(dVg + off) =
+                make_float4(accv[i][4 * hv], accv[i][4 * hv + 1], accv[i][4 * hv + 2],
+                            accv[i][4 * hv + 3]);
+            *reinterpret_cast<float4 *>(dKg + off) =
+                make_float4(acck[i][4 * hv] * scale, acck[i][4 * hv + 1] * scale,
+                            acck[i][4 * hv + 2] * scale, acck[i][4 * hv + 3] * scale);
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_bwd(const float *q, const float *k, const float *v, const float *o,
+                       const float *dout, const float *lse, const int32_t *kv, float *dq,
+                       float *dk, float *dv, float *delta, int B, int H, int Lq, int Lk,
+                       int mask_kind, float scale, cudaStream_t stream) {
+    const int64_t rows = (int64_t)B * H * Lq;
+    cudaError_t e = cudaSuccess;
+    if (rows > 0) {
+        bwd_row_delta_kernel<D><<<(unsigned)((rows + 15) / 16), 256, 0, stream>>>(o, dout, delta,
+                                                                                 dq, rows);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess || Lk == 0) return e;
+    constexpr size_t smem = BwdCfg<D>::kSmem;
+    static bool configured = false;
+    if (!configured) {
+        e = cudaFuncSetAttribute(mha_bwd_f32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const dim3 grid((Lk + kBwdBN - 1) / kBwdBN, H, B);
+    mha_bwd_f32_kernel<D><<<grid, kBwdThreads, smem, stream>>>(
+        q, k, v, dout, lse, delta, kv, dq, dk, dv, H, Lq, Lk, mask_kind, scale,
+        scale * 1.4426950408889634f);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const float *o,
+                           const float *dout, const float *lse, const int32_t *kv_lengths,
+                           float *dq, float *dk, float *dv, float *delta, int B, int H, int Lq,
+                           int Lk, int D, int mask_kind, float scale, cudaStream_t stream) {
+    if (D == 64)
+        return launch_bwd<64>(q, k, v, o, dout, lse, kv_lengths, dq, dk, dv, delta, B, H, Lq, Lk,
+                              mask_kind, scale, stream);
+    return launch_bwd<128>(q, k, v, o, dout, lse, kv_lengths, dq, dk, dv, delta, B, H, Lq, Lk,
+                           mask_kind, scale, stream);
+}
+
+}  // namespace mha

@@ -51,12 +51,20 @@ __device__ __forceinline__ void load_tile(float *dst, const float *__restrict__ 
     }
 }
 
+// Natural-log log-sum-exp of a row from its base-2 running maximum m2 (of
+// the logits times scale * log2(e)) and its sum l of 2^(x - m2):
+// lse = ln(2) * (m2 + log2(l)); -infinity when the row saw no visible key.
+__device__ __forceinline__ float row_lse(float m2, float l) {
+    if (m2 == -INFINITY || !(l > 0.f)) return -INFINITY;
+    return 0.69314718055994531f * (m2 + log2f(l));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads)
     mha_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                        const float *__restrict__ v, const int32_t *__restrict__ kv_lengths,
-                       float *__restrict__ out, int H, int Lq, int Lk, int mask_kind,
-                       float scale_log2) {
+                       float *__restrict__ out, float *__restrict__ lse, int H, int Lq, int Lk,
+                       int mask_kind, float scale_log2) {
     using C = F32Cfg<D>;
     extern __shared__ float4 f32_smem[];
     float *sQ = reinterpret_cast<float *>(f32_smem);
@@ -213,6 +221,8 @@ __global__ void __launch_bounds__(kThreads)
         for (int off = 1; off < 16; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
         const int row = q0 + ty * 4 + i;
+        if (lse != nullptr && tx == 0 && row < Lq)
+            lse[bh * (size_t)Lq + row] = row_lse(m[i], lt);
         if (row < Lq) {
             float *dst = Og + (size_t)row * D + tx * 4;
 #pragma unroll
@@ -329,8 +339,8 @@ template <int D>
 __global__ void __launch_bounds__(kSmallThreads, 2)
     mha_fwd_f32_small_kernel(const float *__restrict__ q, const float *__restrict__ k,
                              const float *__restrict__ v, const int32_t *__restrict__ kv_lengths,
-                             float *__restrict__ out, int H, int Lq, int Lk, int mask_kind,
-                             float scale_log2, int keys_cap) {
+                             float *__restrict__ out, float *__restrict__ lse, int H, int Lq,
+                             int Lk, int mask_kind, float scale_log2, int keys_cap) {
     using C = SmallCfg<D>;
     constexpr int DC = D / 32;   // output columns per lane
     constexpr int R = kSmallR;
@@ -407,7 +417,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
             break;
     }
     // Mask, scale into base 2, row max / exp / row sum (warp shuffles).
-    float l[R];
+    float l[R], mrow[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int row = r0 + r;
@@ -433,6 +443,17 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
         l[r] = sum;
+        mrow[r] = mx;
+    }
+    if (lse != nullptr && lane < R && r0 + lane < Lq) {
+        float mm = mrow[0], ll = l[0];
+#pragma unroll
+        for (int r = 1; r < R; ++r)
+            if (lane == r) {
+                mm = mrow[r];
+                ll = l[r];
+            }
+        lse[bh * (size_t)Lq + r0 + lane] = row_lse(mm, ll);
     }
     float *Pw = sP + (size_t)warp * keys_cap * R;
 #pragma unroll
@@ -485,7 +506,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
 
 template <int D>
 cudaError_t launch_small(const float *q, const float *k, const float *v, const int32_t *kv,
-                         float *out, int B, int H, int Lq, int Lk, int mask_kind, float scale,
+                         float *out, float *lse, int B, int H, int Lq, int Lk, int mask_kind, float scale,
                          cudaStream_t stream) {
     using C = SmallCfg<D>;
     const int keys_cap = ((Lk + 31) / 32) * 32;
@@ -500,13 +521,13 @@ cudaError_t launch_small(const float *q, const float *k, const float *v, const i
     }
     const dim3 grid((Lq + kSmallRows - 1) / kSmallRows, H, B);
     mha_fwd_f32_small_kernel<D><<<grid, kSmallThreads, smem, stream>>>(
-        q, k, v, kv, out, H, Lq, Lk, mask_kind, scale * 1.4426950408889634f, keys_cap);
+        q, k, v, kv, out, lse, H, Lq, Lk, mask_kind, scale * 1.4426950408889634f, keys_cap);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch(const float *q, const float *k, const float *v, const int32_t *kv,
-                   float *out, int B, int H, int Lq, int Lk, int mask_kind, float scale,
+                   float *out, float *lse, int B, int H, int Lq, int Lk, int mask_kind, float scale,
                    cudaStream_t stream) {
     constexpr size_t smem = F32Cfg<D>::kSmem;
     static bool configured = false;
@@ -518,7 +539,7 @@ cudaError_t launch(const float *q, const float *k, const float *v, const int32_t
     }
     const dim3 grid((Lq + kBM - 1) / kBM, H, B);
     const float scale_log2 = scale * 1.4426950408889634f;
-    mha_fwd_f32_kernel<D><<<grid, kThreads, smem, stream>>>(q, k, v, kv, out, H, Lq, Lk,
+    mha_fwd_f32_kernel<D><<<grid, kThreads, smem, stream>>>(q, k, v, kv, out, lse, H, Lq, Lk,
                                                             mask_kind, scale_log2);
     return cudaGetLastError();
 }
@@ -530,15 +551,19 @@ int g_f32_kernel = 0;   // 0 automatic, 1 tiled only, 2 short-key kernel where i
 void set_f32_kernel_override(int which) { g_f32_kernel = which; }
 
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v,
-                           const int32_t *kv_lengths, float *out, int B, int H, int Lq,
-                           int Lk, int D, int mask_kind, float scale, cudaStream_t stream) {
+                           const int32_t *kv_lengths, float *out, float *lse, int B, int H,
+                           int Lq, int Lk, int D, int mask_kind, float scale,
+                           cudaStream_t stream) {
     if ((int64_t)Lk * D <= kSmallMaxKD && g_f32_kernel != 1) {
         if (D == 64)
-            return launch_small<64>(q, k, v, kv_lengths, out, B, H, Lq, Lk, mask_kind, scale, stream);
-        return launch_small<128>(q, k, v, kv_lengths, out, B, H, Lq, Lk, mask_kind, scale, stream);
+            return launch_small<64>(q, k, v, kv_lengths, out, lse, B, H, Lq, Lk, mask_kind, scale,
+                                    stream);
+        return launch_small<128>(q, k, v, kv_lengths, out, lse, B, H, Lq, Lk, mask_kind, scale,
+                                 stream);
     }
-    if (D == 64) return launch<64>(q, k, v, kv_lengths, out, B, H, Lq, Lk, mask_kind, scale, stream);
-    return launch<128>(q, k, v, kv_lengths, out, B, H, Lq, Lk, mask_kind, scale, stream);
+    if (D == 64)
+        return launch<64>(q, k, v, kv_lengths, out, lse, B, H, Lq, Lk, mask_kind, scale, stream);
+    return launch<128>(q, k, v, kv_lengths, out, lse, B, H, Lq, Lk, mask_kind, scale, stream);
 }
 
 }  // namespace mha

@@ -7,9 +7,18 @@
 
 namespace mha {
 
-// fp32 CUDA-core path (fwd_f32.cu).  Arguments already validated.
+// fp32 CUDA-core path (fwd_f32.cu).  Arguments already validated.  `lse`
+// (fp32 [B,H,Lq], natural log) is written when non-null.
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v,
-                           const int32_t *kv_lengths, float *out, int B, int H, int Lq,
+                           const int32_t *kv_lengths, float *out, float *lse, int B, int H,
+                           int Lq, int Lk, int D, int mask_kind, float scale,
+                           cudaStream_t stream);
+
+// fp32 backward (bwd_f32.cu): dq, dk, dv from q, k, v, the forward output o,
+// its row log-sum-exp and dout.  `delta` is device scratch of B*H*Lq floats.
+cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const float *o,
+                           const float *dout, const float *lse, const int32_t *kv_lengths,
+                           float *dq, float *dk, float *dv, float *delta, int B, int H, int Lq,
                            int Lk, int D, int mask_kind, float scale, cudaStream_t stream);
 
 // bf16 tensor-core path (fwd_bf16.cu).  x/gamma/beta are null for plain

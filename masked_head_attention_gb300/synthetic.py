@@ -24,7 +24,8 @@ DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 @dataclass(frozen=True)
 class Workload:
     """One attention problem; `kind` is "mha" (self-attention), "prenorm"
-    (Pre-LN cross-attention) or "prenorm_residual" (the same plus x)."""
+    (Pre-LN cross-attention), "prenorm_residual" (the same plus x) or
+    "mha_bwd" (the backward of self-attention: q, k, v and dout)."""
     name: str
     kind: str
     dtype: str
@@ -77,6 +78,13 @@ WORKLOADS = {
         len_range=(4096, 8192),
         note="decode step: one new query row per (b, h) against a KV cache of U{4096..8192} "
              "valid keys, bf16"),
+    "b2_padding_f32_bwd": Workload(
+        "b2_padding_f32_bwd", "mha_bwd", "f32", B=16, H=8, Lq=512, Lk=512, D=64,
+        mask=MASK_KV_LEN, len_range=(1, 512),
+        note="backward (dq, dk, dv) of the c2 padding-mask workload, fp32; dout iid N(0,1)"),
+    "b3_causal_f32_bwd": Workload(
+        "b3_causal_f32_bwd", "mha_bwd", "f32", B=2, H=16, Lq=1024, Lk=1024, D=128,
+        mask=MASK_CAUSAL, note="backward of causal self-attention, fp32, D=128; dout iid N(0,1)"),
 }
 
 
@@ -104,10 +112,12 @@ def make(w: Workload, seed: int = 0):
     g = _gen(seed)
     dt = DTYPES[w.dtype]
     out = {"scale": w.scale, "kv_lengths": None}
-    if w.kind == "mha":
+    if w.kind in ("mha", "mha_bwd"):
         out["q"] = _normal(g, (w.B, w.H, w.Lq, w.D), w.qk_std, dt)
         out["k"] = _normal(g, (w.B, w.H, w.Lk, w.D), w.qk_std, dt)
         out["v"] = _normal(g, (w.B, w.H, w.Lk, w.D), w.v_std, dt)
+        if w.kind == "mha_bwd":
+            out["dout"] = _normal(g, (w.B, w.H, w.Lq, w.D), 1.0, dt)
     elif w.kind in ("prenorm", "prenorm_residual"):
         N = w.H * w.D
         out["x"] = _normal(g, (w.B, w.Lq, N), w.qk_std, dt)

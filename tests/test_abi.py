@@ -23,6 +23,8 @@ def L():
     lib.prenorm_cross_attn_fwd.argtypes = [P, P, P, f, P, P, P, P, i, i, i, i, i, f, i, P]
     lib.mha_strerror.restype = ctypes.c_char_p
     lib.mha_selftest_umma.argtypes = [i, i, P, P, P, P]
+    lib.mha_fwd_lse.argtypes = [P, P, P, i, P, P, P, i, i, i, i, i, f, i, P]
+    lib.mha_bwd.argtypes = [P, P, P, P, P, P, i, P, P, P, P, i, i, i, i, i, f, i, P]
     return lib
 
 
@@ -91,6 +93,45 @@ def pre(L, x=A, g=A2, b=A3, eps=1e-5, k=A, v=A2, lens=None, out=OUT, B=2, H=2, L
 ])
 def test_prenorm_host_validation(L, kw, want):
     assert pre(L, **kw) == want
+
+
+LSE = ctypes.c_void_p(0x50000)
+G = ctypes.c_void_p(0x60000)
+DQ, DK, DV = ctypes.c_void_p(0x70000), ctypes.c_void_p(0x80000), ctypes.c_void_p(0x90000)
+
+
+def fwd_lse(L, q=A, k=A2, v=A3, mask=0, lens=None, out=OUT, lse=LSE, B=2, H=2, Lq=8, Lk=8,
+            D=64, scale=0.125, dtype=0):
+    return L.mha_fwd_lse(q, k, v, mask, lens, out, lse, B, H, Lq, Lk, D, scale, dtype, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(lse=None), INVALID), (dict(q=None), INVALID), (dict(mask=8), INVALID),
+    (dict(dtype=1), UNSUPPORTED), (dict(D=80), UNSUPPORTED),
+    (dict(lse=ctypes.c_void_p(0x50004)), MISALIGNED), (dict(Lq=0), OK), (dict(B=0), OK),
+])
+def test_fwd_lse_host_validation(L, kw, want):
+    assert fwd_lse(L, **kw) == want
+
+
+def bwd(L, q=A, k=A2, v=A3, o=OUT, g=G, lse=LSE, mask=0, lens=None, dq=DQ, dk=DK, dv=DV,
+        B=2, H=2, Lq=8, Lk=8, D=64, scale=0.125, dtype=0):
+    return L.mha_bwd(q, k, v, o, g, lse, mask, lens, dq, dk, dv, B, H, Lq, Lk, D, scale, dtype,
+                     None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(g=None), INVALID), (dict(lse=None), INVALID), (dict(dq=None), INVALID),
+    (dict(dk=None), INVALID), (dict(o=None), INVALID), (dict(mask=2, lens=None), INVALID),
+    (dict(scale=0.0), INVALID), (dict(Lq=-1), INVALID),
+    (dict(dtype=1), UNSUPPORTED), (dict(D=32), UNSUPPORTED),
+    (dict(dv=ctypes.c_void_p(0x90008)), MISALIGNED), (dict(g=ctypes.c_void_p(0x60004)), MISALIGNED),
+    (dict(B=0), OK), (dict(H=0), OK), (dict(Lq=0, Lk=0), OK),
+    # Lq == 0 still writes dk, dv: the query-side pointers are not needed
+    (dict(Lq=0, q=None, o=None, g=None, lse=None, dq=None, dk=None), INVALID),
+])
+def test_bwd_host_validation(L, kw, want):
+    assert bwd(L, **kw) == want
 
 
 def test_selftest_host_validation(L):

@@ -1,0 +1,143 @@
+"""Backward pass (fp32 on CUDA cores) and the forward's row log-sum-exp
+against the fp64 oracle (GPU).
+
+Tolerance: the forward's fp32 bound (1e-4 max abs) scaled by the size of the
+gradient, max |gpu - oracle| <= 1e-4 * max(1, max |oracle|) per tensor.  Each
+gradient element is an fp32 sum over up to Lq (dk, dv) or Lk (dq) products
+whose terms are of the order of the largest gradient, so its rounding error
+grows with that scale, not with the fixed 1e-4 of an output bounded by |v|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import masked_head_attention_gb300 as mha
+import oracle
+from masked_head_attention_gb300 import synthetic
+from parity_util import as_np, check_f32, dev, lens_tensor, randn
+
+BWD_REL = 1e-4
+
+# (B, H, Lq, Lk, D, mask, lengths): tiles of 64 with ragged tails; Lq < Lk and
+# Lq > Lk under the causal rule; a batch with no visible key; a single key.
+CASES = [
+    (1, 1, 1, 1, 64, 0, None),
+    (2, 2, 70, 90, 64, 2, [90, 45]),
+    (1, 2, 130, 200, 128, 1, None),
+    (2, 3, 257, 129, 64, 3, [1, 129]),
+    (2, 1, 100, 300, 128, 1, None),
+    (1, 2, 300, 60, 64, 1, None),
+    (2, 2, 64, 64, 128, 2, [0, 64]),
+    (1, 1, 200, 1, 128, 0, None),
+    (2, 2, 192, 256, 64, 3, [256, 100]),
+]
+
+
+def check_grad(got, want, what):
+    got = np.asarray(got, np.float64)
+    assert np.all(np.isfinite(got)), "%s: non-finite gradient" % what
+    err = np.abs(got - want).max() if got.size else 0.0
+    tol = BWD_REL * max(1.0, float(np.abs(want).max()) if want.size else 1.0)
+    assert err <= tol, "%s: max abs %.3g > %.3g" % (what, err, tol)
+    return err
+
+
+def run_case(B, H, Lq, Lk, D, mask, lens, seed, scale=None):
+    q = randn((B, H, Lq, D), seed, 1.0)
+    k = randn((B, H, Lk, D), seed + 1, 1.0)
+    v = randn((B, H, Lk, D), seed + 2, 1.0)
+    g = randn((B, H, Lq, D), seed + 3, 1.0)
+    lt = lens_tensor(lens)
+    out, lse = mha.mha_fwd_lse(dev(q), dev(k), dev(v), mask, dev(lt), scale=scale)
+    dq, dk, dv = mha.mha_bwd(dev(q), dev(k), dev(v), out, dev(g), lse, mask, dev(lt),
+                             scale=scale)
+    torch.cuda.synchronize()
+    return (q, k, v, g), (out, lse, dq, dk, dv)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dLq%dLk%dD%dm%d" % c[:6])
+def test_backward_parity(case):
+    B, H, Lq, Lk, D, mask, lens = case
+    (q, k, v, g), (out, lse, dq, dk, dv) = run_case(*case, seed=81)
+    qn, kn, vn, gn = (t.numpy() for t in (q, k, v, g))
+    check_f32(as_np(out), oracle.mha_fwd(qn, kn, vn, mask, lens), "out %s" % (case,))
+    want_lse = oracle.mha_lse(qn, kn, mask, lens)
+    got_lse = as_np(lse)
+    fin = np.isfinite(want_lse)
+    assert np.array_equal(np.isfinite(got_lse), fin), "lse: -inf rows differ"
+    if fin.any():
+        assert np.abs(got_lse[fin] - want_lse[fin]).max() <= 1e-5, "lse"
+    wq, wk, wv = oracle.mha_bwd(qn, kn, vn, gn, mask, lens)
+    errs = [check_grad(as_np(t), w, "%s %s" % (n, case))
+            for n, t, w in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv))]
+    print(case, "dq %.2e dk %.2e dv %.2e" % tuple(errs))
+    assert mha.device_status() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kernel", [1, 2], ids=["tiled", "short"])
+def test_lse_both_forward_kernels(kernel):
+    """Both fp32 forward kernels write the same statistic."""
+    mha.set_f32_kernel(kernel)
+    try:
+        (q, k, _, _), (out, lse, _, _, _) = run_case(2, 2, 100, 128, 64, 3, [128, 70], seed=91)
+    finally:
+        mha.set_f32_kernel(0)
+    want = oracle.mha_lse(q.numpy(), k.numpy(), 3, [128, 70])
+    assert np.abs(as_np(lse) - want).max() <= 1e-5
+
+
+@pytest.mark.gpu
+def test_backward_hidden_keys_exact():
+    """Keys past a batch's length get exactly zero dk and dv; changing their
+    values leaves dk and dv of the visible keys bit-identical (dq is summed
+    with atomics, so only its values are compared)."""
+    B, H, Lq, Lk, D = 2, 2, 150, 200, 64
+    lens = [120, 200]
+    (q, k, v, g), (_, _, dq, dk, dv) = run_case(B, H, Lq, Lk, D, 3, lens, seed=101)
+    assert torch.count_nonzero(dk[0, :, 120:]) == 0 and torch.count_nonzero(dv[0, :, 120:]) == 0
+    k2, v2 = k.clone(), v.clone()
+    k2[0, :, 120:] = randn((H, Lk - 120, D), 102, 20.0)
+    v2[0, :, 120:] = randn((H, Lk - 120, D), 103, 20.0)
+    lt = dev(lens_tensor(lens))
+    out2, lse2 = mha.mha_fwd_lse(dev(q), dev(k2), dev(v2), 3, lt)
+    dq2, dk2, dv2 = mha.mha_bwd(dev(q), dev(k2), dev(v2), out2, dev(g), lse2, 3, lt)
+    torch.cuda.synchronize()
+    assert torch.equal(dk2[:, :, :120], dk[:, :, :120]) and torch.equal(dv2, dv)
+    assert torch.count_nonzero(dk2[0, :, 120:]) == 0
+    assert (dq2 - dq).abs().max().item() <= 1e-5
+
+
+@pytest.mark.gpu
+def test_backward_no_query_rows():
+    """Lq == 0: no row sees a key, so dk and dv are written as zeros."""
+    k = randn((1, 2, 70, 64), 111, 1.0).cuda()
+    v = randn((1, 2, 70, 64), 112, 1.0).cuda()
+    q = torch.empty((1, 2, 0, 64), device="cuda")
+    lse = torch.empty((1, 2, 0), device="cuda")
+    dk = torch.full_like(k, 7.0)
+    dv = torch.full_like(v, 7.0)
+    mha.mha_bwd(q, k, v, q, q, lse, 0, None, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+
+
+@pytest.mark.gpu
+def test_backward_workload_full():
+    """The backward workload of the benchmark, every gradient element
+    against the oracle."""
+    w = synthetic.WORKLOADS["b2_padding_f32_bwd"]
+    x = synthetic.make(w, seed=0)
+    lt = dev(x["kv_lengths"])
+    out, lse = mha.mha_fwd_lse(dev(x["q"]), dev(x["k"]), dev(x["v"]), w.mask, lt, scale=w.scale)
+    dq, dk, dv = mha.mha_bwd(dev(x["q"]), dev(x["k"]), dev(x["v"]), out, dev(x["dout"]), lse,
+                             w.mask, lt, scale=w.scale)
+    torch.cuda.synchronize()
+    lens = x["kv_lengths"].numpy()
+    wq, wk, wv = oracle.mha_bwd(x["q"].numpy(), x["k"].numpy(), x["v"].numpy(),
+                                x["dout"].numpy(), w.mask, lens, w.scale)
+    errs = [check_grad(as_np(t), ww, n) for n, t, ww in (("dq", dq, wq), ("dk", dk, wk),
+                                                        ("dv", dv, wv))]
+    print(w.name, "dq %.2e dk %.2e dv %.2e" % tuple(errs))
+    assert mha.device_status() == 0

@@ -27,6 +27,20 @@ def test_algorithmic_bytes():
     assert bench.algorithmic_bytes(w, None) == 4 * 32 * 2048 * 128 * 2
 
 
+def test_backward_accounting():
+    w = synthetic.WORKLOADS["b2_padding_f32_bwd"]
+    lens = [100, 512] + [0] * 14
+    assert bench.mask_aware_flops(w, lens) == 10 * 8 * 64 * 512 * 612
+    w3 = synthetic.WORKLOADS["b3_causal_f32_bwd"]
+    assert bench.mask_aware_flops(w3, None) == 10 * 2 * 16 * 1024 * 1024 * 128 / 2
+    rows_q = 16 * 8 * 512
+    want = 4 * rows_q * 64 * 4 + 4 * rows_q + 2 * 612 * 8 * 64 * 4 + 2 * 16 * 8 * 512 * 64 * 4
+    assert bench.algorithmic_bytes(w, lens) == want
+    assert bench.kernel_of(w) == "mha_bwd_f32_kernel"
+    small = synthetic.small(kind="mha_bwd", Lq=64, Lk=64)
+    assert bench.kernel_of(small) == "mha_bwd_f32_kernel"
+
+
 def test_fp32_alu_peak():
     assert abs(bench.fp32_alu_peak_tflops(152, 2070.0) - 80.54) < 0.01
 
