@@ -66,8 +66,9 @@ typedef enum {
 /* Mask kinds: bit flags, combinable (MHA_MASK_CAUSAL | MHA_MASK_KV_LEN). */
 enum { MHA_MASK_NONE = 0, MHA_MASK_CAUSAL = 1, MHA_MASK_KV_LEN = 2 };
 
-/* Element types of q/k/v/out (and x_q).  MHA_F32 runs on CUDA-core FFMA;
- * MHA_BF16 runs on tcgen05 tensor cores with fp32 accumulation in TMEM. */
+/* Element types of q/k/v/out (and x_q).  MHA_F32 runs on the tcgen05 tensor
+ * cores with a three-term TF32 split when D = 64, on CUDA-core FFMA when
+ * D = 128; MHA_BF16 runs on tcgen05 tensor cores.  Both accumulate in fp32. */
 enum { MHA_F32 = 0, MHA_BF16 = 1 };
 
 /*
@@ -243,12 +244,15 @@ MHA_API void mha_set_bf16_grid(int ctas);
 
 /*
  * mha_set_f32_kernel -- kernel-choice hook for tests and benchmarks of the
- * fp32 path.  0 = automatic: the short-key-range kernel (every visible K/V
- * row of a 16-row query block staged in shared memory at once) when
+ * fp32 path.  0 = automatic: for D = 64 the tensor-core kernel (three TF32
+ * MMAs per product: hi*hi + lo*hi + hi*lo of the operands split as
+ * x = tf32(x) + tf32(x - tf32(x)), fp32 accumulation in TMEM); for D = 128
+ * the CUDA-core kernels: the short-key-range kernel (every visible K/V row
+ * of a 16-row query block staged in shared memory at once) when
  * Lk * D <= 16384, else the tiled kernel (64-row query tiles, 64-key K/V
- * tiles); 1 = always the tiled kernel; 2 = the short-key-range kernel
- * whenever Lk * D <= 16384.  Other values act as 0.  Affects later calls
- * from any thread of the process.
+ * tiles).  1 = always the tiled CUDA-core kernel; 2 = the short-key-range
+ * kernel whenever Lk * D <= 16384, else the tiled one; 3 = as 0.  Other
+ * values act as 0.  Affects later calls from any thread of the process.
  */
 MHA_API void mha_set_f32_kernel(int which);
 

@@ -298,7 +298,8 @@ def set_bf16_decode(mode):
 
 
 def set_f32_kernel(which):
-    """0 automatic, 1 tiled kernel only, 2 short-key-range kernel where it applies."""
+    """0 automatic (tensor cores, 3xTF32, for D = 64), 1 tiled CUDA-core kernel
+    only, 2 short-key-range CUDA-core kernel where it applies, 3 as 0."""
     lib().mha_set_f32_kernel(int(which))
 
 

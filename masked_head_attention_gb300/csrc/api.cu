@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" boundary of libmha.so: argument validation,
 // dispatch by (entry point, dtype, D), and status reporting.  Host code only;
-// the kernels live in fwd_f32.cu, fwd_bf16.cu, decode_bf16.cu and bwd_f32.cu.
+// the kernels live in fwd_f32.cu, fwd_tf32.cu, fwd_bf16.cu, decode_bf16.cu and
+// bwd_f32.cu.
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -44,11 +45,14 @@ int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
     if ((mask_kind & MHA_MASK_KV_LEN) && !kv_lengths) return MHA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || (Lk > 0 && (!aligned16(k) || !aligned16(v))))
         return MHA_ERR_MISALIGNED;
-    if (dtype == MHA_F32)
-        return from_cuda(mha::launch_fwd_f32(
+    if (dtype == MHA_F32) {
+        int drv = 0;
+        const cudaError_t e = mha::launch_fwd_f32(
             static_cast<const float *>(q), static_cast<const float *>(k),
             static_cast<const float *>(v), kv_lengths, static_cast<float *>(out), nullptr, B, H,
-            Lq, Lk, D, mask_kind, scale, stream));
+            Lq, Lk, D, mask_kind, scale, stream, &drv);
+        return drv != 0 ? MHA_ERR_CUDA : from_cuda(e);
+    }
     mha::Bf16Call c{};
     c.q = q;
     c.k = k;
@@ -82,10 +86,12 @@ int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_kind,
     if (!aligned16(q) || !aligned16(out) || !aligned16(lse) ||
         (Lk > 0 && (!aligned16(k) || !aligned16(v))))
         return MHA_ERR_MISALIGNED;
-    return from_cuda(mha::launch_fwd_f32(
+    int drv = 0;
+    const cudaError_t e = mha::launch_fwd_f32(
         static_cast<const float *>(q), static_cast<const float *>(k),
         static_cast<const float *>(v), kv_lengths, static_cast<float *>(out), lse, B, H, Lq, Lk,
-        D, mask_kind, scale, stream));
+        D, mask_kind, scale, stream, &drv);
+    return drv != 0 ? MHA_ERR_CUDA : from_cuda(e);
 }
 
 int mha_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
@@ -251,7 +257,12 @@ const char *mha_strerror(int status) {
 }
 
 int mha_device_status(uint32_t *bits, int clear) {
-    return from_cuda(mha::read_device_status(bits, clear != 0));
+    // Each tensor-core translation unit keeps its own word; report their union.
+    uint32_t a = 0, b = 0;
+    cudaError_t e = mha::read_device_status(&a, clear != 0);
+    if (e == cudaSuccess) e = mha::read_device_status_tf32(&b, clear != 0);
+    if (bits) *bits = a | b;
+    return from_cuda(e);
 }
 
 int mha_selftest_umma(int variant, int K_or_N, const void *a, const void *b, float *c,

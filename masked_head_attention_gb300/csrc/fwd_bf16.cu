@@ -870,6 +870,8 @@ __global__ void __launch_bounds__(128, 1) selftest_umma_kernel(const __grid_cons
 }
 
 // ------------------------------ host side ----------------------------------
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -900,13 +902,7 @@ CUresult encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-int g_grid_override = 0;
-
 // SM count and L2 size of the current device (cached per device).
-struct DeviceInfo {
-    int sms = 0;
-    int l2 = 0;
-};
 DeviceInfo device_info() {
     constexpr int kMaxDevices = 64;
     static DeviceInfo info[kMaxDevices];
@@ -923,6 +919,10 @@ DeviceInfo device_info() {
     }
     return info[dev];
 }
+
+namespace {
+
+int g_grid_override = 0;
 
 template <int D, bool PRENORM>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {

@@ -544,7 +544,9 @@ cudaError_t launch(const float *q, const float *k, const float *v, const int32_t
     return cudaGetLastError();
 }
 
-int g_f32_kernel = 0;   // 0 automatic, 1 tiled only, 2 short-key kernel where it applies
+// 0 automatic, 1 tiled only, 2 short-key kernel where it applies, 3 the
+// tensor-core (3xTF32) kernel where it applies (D = 64).
+int g_f32_kernel = 0;
 
 }  // namespace
 
@@ -553,8 +555,13 @@ void set_f32_kernel_override(int which) { g_f32_kernel = which; }
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v,
                            const int32_t *kv_lengths, float *out, float *lse, int B, int H,
                            int Lq, int Lk, int D, int mask_kind, float scale,
-                           cudaStream_t stream) {
-    if ((int64_t)Lk * D <= kSmallMaxKD && g_f32_kernel != 1) {
+                           cudaStream_t stream, int *driver_err) {
+    *driver_err = 0;
+    const int which = (g_f32_kernel >= 1 && g_f32_kernel <= 3) ? g_f32_kernel : 0;
+    if ((which == 0 || which == 3) && tf32x3_applies(D))
+        return launch_fwd_tf32x3(q, k, v, kv_lengths, out, lse, B, H, Lq, Lk, D, mask_kind, scale,
+                                 stream, driver_err);
+    if ((int64_t)Lk * D <= kSmallMaxKD && which != 1) {
         if (D == 64)
             return launch_small<64>(q, k, v, kv_lengths, out, lse, B, H, Lq, Lk, mask_kind, scale,
                                     stream);

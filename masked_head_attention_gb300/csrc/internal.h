@@ -3,16 +3,40 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 namespace mha {
 
-// fp32 CUDA-core path (fwd_f32.cu).  Arguments already validated.  `lse`
-// (fp32 [B,H,Lq], natural log) is written when non-null.
+// SM count and L2 size of the current device (cached per device).
+struct DeviceInfo {
+    int sms = 0;
+    int l2 = 0;
+};
+DeviceInfo device_info();
+
+// cuTensorMapEncodeTiled from the driver (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// fp32 path (fwd_f32.cu): the 3xTF32 tensor-core kernel where it applies,
+// else the CUDA-core kernels.  Arguments already validated.  `lse` (fp32
+// [B,H,Lq], natural log) is written when non-null.  *driver_err receives a
+// nonzero CUresult when tensor-map encoding failed.
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v,
                            const int32_t *kv_lengths, float *out, float *lse, int B, int H,
                            int Lq, int Lk, int D, int mask_kind, float scale,
-                           cudaStream_t stream);
+                           cudaStream_t stream, int *driver_err);
+
+// fp32 on the tensor cores with the three-term TF32 split (fwd_tf32.cu):
+// D = 64 only (tf32x3_applies).  `lse` is written when non-null.  Returns
+// cudaErrorInvalidValue with *driver_err set when tensor-map encoding fails.
+bool tf32x3_applies(int D);
+cudaError_t launch_fwd_tf32x3(const float *q, const float *k, const float *v,
+                              const int32_t *kv_lengths, float *out, float *lse, int B, int H,
+                              int Lq, int Lk, int D, int mask_kind, float scale,
+                              cudaStream_t stream, int *driver_err);
+cudaError_t read_device_status_tf32(uint32_t *bits, bool clear);
 
 // fp32 backward (bwd_f32.cu): dq, dk, dv from q, k, v, the forward output o,
 // its row log-sum-exp and dout.  `delta` is device scratch of B*H*Lq floats.

@@ -1,4 +1,5 @@
-"""fp32 CUDA-core path against the fp64 oracle, element by element (GPU)."""
+"""fp32 path against the fp64 oracle, element by element (GPU): the
+tensor-core kernel (3xTF32, D = 64) and both CUDA-core kernels."""
 import numpy as np
 import pytest
 import torch
@@ -45,11 +46,14 @@ def f32_kernel(request):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("f32_kernel", [0, 1, 2], indirect=True, ids=["auto", "tiled", "short"])
+@pytest.mark.parametrize("f32_kernel", [0, 1, 2, 3], indirect=True,
+                         ids=["auto", "tiled", "short", "tf32x3"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dLq%dLk%dD%dm%d" % c[:6])
 def test_f32_small(case, f32_kernel):
     got, want = _run(*case)
-    check_f32(got, want, str(case))
+    err = check_f32(got, want, str(case))
+    print(case, f32_kernel, "max abs %.2e" % err)
+    assert mha.device_status() == 0
 
 
 @pytest.mark.gpu
@@ -62,11 +66,13 @@ def test_f32_full_workload(name):
     torch.cuda.synchronize()
     lens = None if x["kv_lengths"] is None else x["kv_lengths"].numpy()
     want = oracle.mha_fwd(x["q"].numpy(), x["k"].numpy(), x["v"].numpy(), w.mask, lens, w.scale)
-    check_f32(as_np(out), want, name)
+    err = check_f32(as_np(out), want, name)
+    print(name, "max abs %.2e" % err)
+    assert mha.device_status() == 0
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("f32_kernel", [1, 2], indirect=True, ids=["tiled", "short"])
+@pytest.mark.parametrize("f32_kernel", [1, 2, 3], indirect=True, ids=["tiled", "short", "tf32x3"])
 def test_f32_masked_keys_contribute_exactly_zero(f32_kernel):
     B, H, L, D = 2, 2, 160, 64
     q, k, v = randn((B, H, L, D), 5), randn((B, H, L, D), 6), randn((B, H, L, D), 7)
@@ -84,10 +90,25 @@ def test_f32_masked_keys_contribute_exactly_zero(f32_kernel):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("f32_kernel", [1, 2], indirect=True, ids=["tiled", "short"])
+@pytest.mark.parametrize("f32_kernel", [1, 2, 3], indirect=True, ids=["tiled", "short", "tf32x3"])
 def test_f32_zero_keys_gives_zeros(f32_kernel):
     q = randn((2, 2, 9, 64), 1).cuda()
     kv = torch.empty((2, 2, 0, 64), device="cuda")
     out = mha.mha_fwd(q, kv, kv, 0)
     torch.cuda.synchronize()
     assert torch.count_nonzero(out).item() == 0
+
+
+@pytest.mark.gpu
+def test_tf32x3_many_items_persistent():
+    """More 128-row tiles than SMs, mixed lengths (0 included): every CTA
+    walks several items, with and without work, through the same barriers."""
+    mha.set_f32_kernel(3)
+    try:
+        lens = [0, 1, 64, 65, 700, 333, 128, 1000] * 4
+        got, want = _run(32, 4, 700, 1000, 64, 3, lens, seed=40)
+    finally:
+        mha.set_f32_kernel(0)
+    err = check_f32(got, want, "many items")
+    print("many items max abs %.2e" % err)
+    assert mha.device_status() == 0
