@@ -38,7 +38,7 @@ METRIC = "mask-aware attention TFLOP/s and µs/call at 1 GB300; % of roofline"
 DEFAULT_WORKLOAD = "c2_padding_f32"
 DEFAULT_L2 = 129 * 1024 * 1024
 KERNEL_OF = {  # dominant kernel of each workload
-    "mha:f32": "mha_fwd_f32_kernel",
+    "mha:f32": "mha_fwd_f32_kernel",      # D = 128; D = 64 runs attn_fwd_tf32x3_kernel
     "mha:bf16": "attn_fwd_bf16_kernel",
     "prenorm:bf16": "attn_fwd_bf16_kernel<prenorm>",
     "prenorm_residual:bf16": "attn_fwd_bf16_kernel<prenorm>",
@@ -46,9 +46,19 @@ KERNEL_OF = {  # dominant kernel of each workload
 }
 SMALL_F32_MAX_KD = 16384   # the fp32 path stages all keys at once when Lk * D is at most this
 DECODE_MAX_ROWS = 8        # bf16 self-attention with at most this many query rows: decode kernel
+TF32X3_D = 64              # fp32 inputs with this head dimension run on the tensor cores (3xTF32)
+# Dense tf32 tensor rate relative to bf16 (nominal 1.1 vs 2.25 PFLOP/s per GPU); the
+# tf32 peak is the measured bf16 peak times this ratio.
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def uses_tf32x3(w):
+    return w.kind == "mha" and w.dtype == "f32" and w.D == TF32X3_D
 
 
 def kernel_of(w):
+    if uses_tf32x3(w):
+        return "attn_fwd_tf32x3_kernel"
     if w.kind == "mha" and w.dtype == "f32" and w.Lk * w.D <= SMALL_F32_MAX_KD:
         return "mha_fwd_f32_small_kernel"
     if w.kind == "mha" and w.dtype == "bf16" and w.Lq <= DECODE_MAX_ROWS:
@@ -318,13 +328,19 @@ def time_e2e(wl, steps, warmup):
 
 def roofline_for(w, lens, kernel_ms, peaks, n_sm):
     """The binding roofline of the workload's dominant kernel: compute (FFMA
-    for fp32 inputs, the tensor cores for bf16) or HBM, whichever takes
-    longer for the algorithmic work; achieved and peak in that roofline's
-    unit (TFLOP/s or GB/s)."""
+    for fp32 inputs on CUDA cores; the tensor cores for bf16 and for fp32 on
+    the 3xTF32 path) or HBM, whichever takes longer for the algorithmic
+    work; achieved and peak in that roofline's unit (TFLOP/s or GB/s).
+    The 3xTF32 path executes three tf32 MMAs per product, so its algorithmic
+    tensor work is 3x the mask-aware FLOP count, against the tf32 peak."""
     flops = mask_aware_flops(w, lens)
     nbytes = algorithmic_bytes(w, lens)
     kkey = kernel_of(w)
-    if w.dtype == "f32":
+    if uses_tf32x3(w):
+        flops *= 3
+        cpeak = peaks["bf16_tflops"] * TF32_OVER_BF16
+        cbound, csrc = "tensor", " bf16 burst x 1.1/2.25 (tf32); 3 tf32 MMAs per product"
+    elif w.dtype == "f32":
         cpeak = fp32_alu_peak_tflops(n_sm, peaks.get("sm_max_mhz", 2070.0))
         cbound, csrc = "alu", " (SMs x 128 lanes x 2 x max SM clock)"
     else:
@@ -584,7 +600,8 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
                 "us_per_call": round(ms_per_step * 1e3, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None,
-                "dtype": "f32" if w.dtype == "f32" else "bf16 (fp32 accumulate)",
+                "dtype": ("f32 (3xTF32 on tensor cores, fp32 accumulate)" if uses_tf32x3(w)
+                          else "f32" if w.dtype == "f32" else "bf16 (fp32 accumulate)"),
                 "data": "synthetic",
                 "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk,
                            "D": w.D, "mask": w.mask, "note": w.note,

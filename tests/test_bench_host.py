@@ -41,6 +41,20 @@ def test_backward_accounting():
     assert bench.kernel_of(small) == "mha_bwd_f32_kernel"
 
 
+def test_kernel_choice_and_tf32_roofline():
+    c2 = synthetic.WORKLOADS["c2_padding_f32"]
+    assert bench.kernel_of(c2) == "attn_fwd_tf32x3_kernel"
+    d128 = synthetic.small(dtype="f32", D=128, Lq=512, Lk=512)
+    assert bench.kernel_of(d128) == "mha_fwd_f32_kernel"
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 7000.0, "_source": "test"}
+    lens = [512] * 16
+    flops = bench.mask_aware_flops(c2, lens)
+    r = bench.roofline_for(c2, lens, 0.05, peaks, 152)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["peak"] - 2000.0 * 1.1 / 2.25) < 0.1
+    assert abs(r["achieved"] - 3 * flops / 0.05e-3 / 1e12) < 1e-3
+
+
 def test_fp32_alu_peak():
     assert abs(bench.fp32_alu_peak_tflops(152, 2070.0) - 80.54) < 0.01
 
