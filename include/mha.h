@@ -266,6 +266,15 @@ MHA_API void mha_set_f32_kernel(int which);
  */
 MHA_API void mha_set_bf16_decode(int mode);
 
+/*
+ * mha_set_bf16_decode_splits -- launch-shape hook for tests and benchmarks of
+ * the decode kernel: split the keys of every (b, h) over `splits` CTAs (one
+ * cluster; values above 8 act as 8); 0 restores the automatic choice (about
+ * one CTA per SM in total, at least 256 keys per CTA).  Affects later calls
+ * from any thread of the process.
+ */
+MHA_API void mha_set_bf16_decode_splits(int splits);
+
 #ifdef __cplusplus
 }
 #endif

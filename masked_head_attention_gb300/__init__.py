@@ -66,6 +66,8 @@ def lib():
         L.mha_set_f32_kernel.restype = None
         L.mha_set_bf16_decode.argtypes = [i]
         L.mha_set_bf16_decode.restype = None
+        L.mha_set_bf16_decode_splits.argtypes = [i]
+        L.mha_set_bf16_decode_splits.restype = None
         _lib = L
     return _lib
 
@@ -295,6 +297,11 @@ def set_bf16_grid(ctas):
 def set_bf16_decode(mode):
     """0 automatic (decode kernel for bf16 calls with Lq <= 8), 1 never."""
     lib().mha_set_bf16_decode(int(mode))
+
+
+def set_bf16_decode_splits(splits):
+    """Force the decode kernel's CTAs per (b, h) (1..8); 0 = automatic."""
+    lib().mha_set_bf16_decode_splits(int(splits))
 
 
 def set_f32_kernel(which):

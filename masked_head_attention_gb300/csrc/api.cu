@@ -285,4 +285,6 @@ void mha_set_f32_kernel(int which) { mha::set_f32_kernel_override(which); }
 
 void mha_set_bf16_decode(int mode) { mha::set_decode_override(mode); }
 
+void mha_set_bf16_decode_splits(int splits) { mha::set_decode_splits(splits); }
+
 }  // extern "C"

@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 }
 
 int g_decode_override = 0;   // 0 automatic, 1 never
+int g_decode_splits = 0;     // 0 automatic, else CTAs per (b, h) (at most 8)
 
 template <int D, int R>
 cudaError_t launch_dec(const Bf16Call &c, int splits, int chunk, cudaStream_t stream) {
@@ -297,6 +298,7 @@ cudaError_t launch_dec_rows(const Bf16Call &c, int splits, int chunk, cudaStream
 }  // namespace
 
 void set_decode_override(int which) { g_decode_override = which; }
+void set_decode_splits(int splits) { g_decode_splits = splits; }
 
 bool decode_applies(const Bf16Call &c) {
     // (b, h) problems are the grid's y dimension (at most 65535).
@@ -309,13 +311,17 @@ cudaError_t launch_decode_bf16(const Bf16Call &c, int num_sms, cudaStream_t stre
     // chunks of a multiple of 32 keys.
     const int kend = (c.mask_kind & 1) ? (c.Lq < c.Lk ? c.Lq : c.Lk) : c.Lk;
     const int64_t BH = (int64_t)c.B * c.H;
-    // About two CTAs per SM in total, at least 256 keys per CTA, at most a
-    // portable cluster of 8.
-    int64_t want = (2 * (int64_t)num_sms + BH - 1) / BH;
+    // About one CTA per SM in total, at least 256 keys per CTA, at most a
+    // portable cluster of 8.  Splitting costs more than the wave it fills
+    // (measured on the 8 x 32-head, 8192-key decode step: one CTA per (b, h)
+    // 171 us, two 195 us, eight 211 us), so problems with at least one
+    // (b, h) per SM are not split at all.
+    int64_t want = ((int64_t)num_sms + BH - 1) / BH;
     const int64_t by_keys = (kend + 255) / 256;
     if (want > by_keys) want = by_keys;
     if (want > kDecMaxCluster) want = kDecMaxCluster;
     if (want < 1) want = 1;
+    if (g_decode_splits > 0) want = g_decode_splits < kDecMaxCluster ? g_decode_splits : kDecMaxCluster;
     const int splits = (int)want;
     int chunk = (kend + splits - 1) / splits;
     chunk = ((chunk + 31) / 32) * 32;

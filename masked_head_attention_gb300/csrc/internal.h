@@ -75,6 +75,7 @@ constexpr int kDecodeMaxRows = 8;
 bool decode_applies(const Bf16Call &c);
 cudaError_t launch_decode_bf16(const Bf16Call &c, int num_sms, cudaStream_t stream);
 void set_decode_override(int which);
+void set_decode_splits(int splits);
 
 // Diagnostic single-tile tcgen05 GEMM (fwd_bf16.cu).
 cudaError_t launch_selftest_umma(int variant, int K_or_N, const void *a, const void *b,

@@ -78,3 +78,23 @@ def test_decode_workload_full():
     r = check_bf16(as_np(out), want, w.name)
     print(w.name, r)
     assert mha.device_status() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8])
+def test_decode_forced_splits(splits):
+    """Every cluster size combines its CTAs' partials correctly (keys split
+    in chunks of a multiple of 32, the last chunk ragged or empty)."""
+    B, H, Lq, Lk, D, mask, lens = 2, 3, 3, 2100, 128, 2, [2100, 700]
+    q = randn((B, H, Lq, D), 81, 1.0, torch.bfloat16)
+    k = randn((B, H, Lk, D), 82, 1.0, torch.bfloat16)
+    v = randn((B, H, Lk, D), 83, 1.0, torch.bfloat16)
+    mha.set_bf16_decode_splits(splits)
+    try:
+        out = mha.mha_fwd(dev(q), dev(k), dev(v), mask, dev(lens_tensor(lens)))
+        torch.cuda.synchronize()
+    finally:
+        mha.set_bf16_decode_splits(0)
+    want = oracle.mha_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), mask, lens)
+    check_bf16(as_np(out), want, "splits=%d" % splits)
+    assert mha.device_status() == 0
