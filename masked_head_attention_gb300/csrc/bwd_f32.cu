@@ -133,13 +133,15 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
 
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
 
-    float accv[4][OC], acck[4][OC];
+    // dV and dK accumulators as column pairs for the packed fp32x2 FMA (two
+    // FMAs per instruction: the same FMA-pipe rate in half the issue slots).
+    float2 accv[4][OC / 2], acck[4][OC / 2];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int c = 0; c < OC; ++c) {
-            accv[i][c] = 0.f;
-            acck[i][c] = 0.f;
+        for (int c = 0; c < OC / 2; ++c) {
+            accv[i][c] = make_float2(0.f, 0.f);
+            acck[i][c] = make_float2(0.f, 0.f);
         }
 
     if (qt0 < qt1) {
@@ -228,27 +230,26 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
             for (int hv = 0; hv < OC / 4; ++hv) {
                 const float4 g = *reinterpret_cast<const float4 *>(sG + r * C::LD + tx * 4 + 64 * hv);
                 const float4 qq = *reinterpret_cast<const float4 *>(sQ + r * C::LD + tx * 4 + 64 * hv);
+                const float2 g01 = make_float2(g.x, g.y), g23 = make_float2(g.z, g.w);
+                const float2 q01 = make_float2(qq.x, qq.y), q23 = make_float2(qq.z, qq.w);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    accv[i][4 * hv + 0] = fmaf(pr[i], g.x, accv[i][4 * hv + 0]);
-                    accv[i][4 * hv + 1] = fmaf(pr[i], g.y, accv[i][4 * hv + 1]);
-                    accv[i][4 * hv + 2] = fmaf(pr[i], g.z, accv[i][4 * hv + 2]);
-                    accv[i][4 * hv + 3] = fmaf(pr[i], g.w, accv[i][4 * hv + 3]);
-                    acck[i][4 * hv + 0] = fmaf(sr[i], qq.x, acck[i][4 * hv + 0]);
-                    acck[i][4 * hv + 1] = fmaf(sr[i], qq.y, acck[i][4 * hv + 1]);
-                    acck[i][4 * hv + 2] = fmaf(sr[i], qq.z, acck[i][4 * hv + 2]);
-                    acck[i][4 * hv + 3] = fmaf(sr[i], qq.w, acck[i][4 * hv + 3]);
+                    const float2 pp = make_float2(pr[i], pr[i]), ss = make_float2(sr[i], sr[i]);
+                    accv[i][2 * hv + 0] = __ffma2_rn(pp, g01, accv[i][2 * hv + 0]);
+                    accv[i][2 * hv + 1] = __ffma2_rn(pp, g23, accv[i][2 * hv + 1]);
+                    acck[i][2 * hv + 0] = __ffma2_rn(ss, q01, acck[i][2 * hv + 0]);
+                    acck[i][2 * hv + 1] = __ffma2_rn(ss, q23, acck[i][2 * hv + 1]);
                 }
             }
         }
 
         // dQ (rows ty*4 + i, columns tx*4 (+ 64)) += scale * dS K, added to the
         // global accumulator with one 16-byte atomic per 4 columns.
-        float accq[4][OC];
+        float2 accq[4][OC / 2];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int c = 0; c < OC; ++c) accq[i][c] = 0.f;
+            for (int c = 0; c < OC / 2; ++c) accq[i][c] = make_float2(0.f, 0.f);
 #pragma unroll 2
         for (int j = 0; j < kBwdBN; j += 4) {
             float4 sa[4];
@@ -261,13 +262,13 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
 #pragma unroll
                 for (int hv = 0; hv < OC / 4; ++hv) {
                     const float4 kk = *reinterpret_cast<const float4 *>(krow + 64 * hv);
+                    const float2 k01 = make_float2(kk.x, kk.y), k23 = make_float2(kk.z, kk.w);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const float w = jj == 0 ? sa[i].x : jj == 1 ? sa[i].y : jj == 2 ? sa[i].z : sa[i].w;
-                        accq[i][4 * hv + 0] = fmaf(w, kk.x, accq[i][4 * hv + 0]);
-                        accq[i][4 * hv + 1] = fmaf(w, kk.y, accq[i][4 * hv + 1]);
-                        accq[i][4 * hv + 2] = fmaf(w, kk.z, accq[i][4 * hv + 2]);
-                        accq[i][4 * hv + 3] = fmaf(w, kk.w, accq[i][4 * hv + 3]);
+                        const float2 ww = make_float2(w, w);
+                        accq[i][2 * hv + 0] = __ffma2_rn(ww, k01, accq[i][2 * hv + 0]);
+                        accq[i][2 * hv + 1] = __ffma2_rn(ww, k23, accq[i][2 * hv + 1]);
                     }
                 }
             }
@@ -279,8 +280,8 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
 #pragma unroll
             for (int hv = 0; hv < OC / 4; ++hv)
                 atomicAdd(reinterpret_cast<float4 *>(dQg + (size_t)row * D + tx * 4 + 64 * hv),
-                          make_float4(accq[i][4 * hv] * scale, accq[i][4 * hv + 1] * scale,
-                                      accq[i][4 * hv + 2] * scale, accq[i][4 * hv + 3] * scale));
+                          make_float4(accq[i][2 * hv].x * scale, accq[i][2 * hv].y * scale,
+                                      accq[i][2 * hv + 1].x * scale, accq[i][2 * hv + 1].y * scale));
         }
     }
 
@@ -296,11 +297,11 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
         for (int hv = 0; hv < OC / 4; ++hv) {
             const size_t off = (size_t)key * D + tx * 4 + 64 * hv;
             *reinterpret_cast<float4 *>(dVg + off) =
-                make_float4(accv[i][4 * hv], accv[i][4 * hv + 1], accv[i][4 * hv + 2],
-                            accv[i][4 * hv + 3]);
+                make_float4(accv[i][2 * hv].x, accv[i][2 * hv].y, accv[i][2 * hv + 1].x,
+                            accv[i][2 * hv + 1].y);
             *reinterpret_cast<float4 *>(dKg + off) =
-                make_float4(acck[i][4 * hv] * scale, acck[i][4 * hv + 1] * scale,
-                            acck[i][4 * hv + 2] * scale, acck[i][4 * hv + 3] * scale);
+                make_float4(acck[i][2 * hv].x * scale, acck[i][2 * hv].y * scale,
+                            acck[i][2 * hv + 1].x * scale, acck[i][2 * hv + 1].y * scale);
         }
     }
 }
