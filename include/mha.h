@@ -101,7 +101,9 @@ MHA_API int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
  * the max first", gsyq.cn, sections 2.1 and 3.1: it is the row maximum plus
  * the log of the shifted sum, both already held by the online softmax.)
  *   lse         device fp32 [B,H,Lq], 16-byte aligned, written once.
- *   dtype       must be MHA_F32 (MHA_ERR_UNSUPPORTED otherwise).
+ *   dtype       MHA_F32 or MHA_BF16 (self-attention, every kernel of
+ *               mha_fwd: the statistic comes from each kernel's own running
+ *               maximum and sum).
  * Other arguments, layouts and errors as for mha_fwd.
  */
 MHA_API int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_kind,
@@ -125,15 +127,19 @@ MHA_API int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_ki
  *   out         the forward's output O [B,H,Lq,D].
  *   dout        dL/dO [B,H,Lq,D].
  *   lse         the forward's row log-sum-exp [B,H,Lq] (mha_fwd_lse).
- *   dq          [B,H,Lq,D]; dk, dv [B,H,Lk,D]: outputs, fully written (dq
- *               is zeroed and then accumulated with fp32 atomic adds, so
- *               its last bits can differ between runs).  Must not alias
- *               any input.
- *   dtype       must be MHA_F32 (MHA_ERR_UNSUPPORTED otherwise).
- * Memory: a stream-ordered workspace of 4*B*H*Lq bytes (cudaMallocAsync /
- * cudaFreeAsync on `stream`) holds Delta.  Two kernels run on `stream`: a
- * row pass (Delta, dq = 0) and the key-tile kernel.  Lq == 0 with Lk > 0
- * writes zero dk and dv.  Returns MHA_OK or a negative mha_status.
+ *   dq          [B,H,Lq,D]; dk, dv [B,H,Lk,D]: outputs of `dtype`, fully
+ *               written (dq is accumulated in fp32 with atomic adds, so its
+ *               last bits can differ between runs).  Must not alias any
+ *               input.
+ *   dtype       MHA_F32 or MHA_BF16: q, k, v, out, dout and the gradients
+ *               all of that type; the arithmetic is fp32 either way and the
+ *               bf16 gradients are rounded once, to nearest even.
+ * Memory: a stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on
+ * `stream`) of 4*B*H*Lq bytes (rounded up to 256) for Delta, plus, for
+ * bf16, 4*B*H*Lq*D bytes for the fp32 dq accumulator.  Kernels on `stream`:
+ * a row pass (Delta, dq accumulator = 0), the key-tile kernel and, for
+ * bf16, the conversion of dq.  Lq == 0 with Lk > 0 writes zero dk and dv.
+ * Returns MHA_OK or a negative mha_status.
  */
 MHA_API int mha_bwd(const void *q, const void *k, const void *v, const void *out,
                     const void *dout, const float *lse, int mask_kind,

@@ -153,14 +153,14 @@ def mha_fwd(q, k, v, mask_kind=MASK_NONE, kv_lengths=None, out=None, scale=None,
 
 def mha_fwd_lse(q, k, v, mask_kind=MASK_NONE, kv_lengths=None, out=None, lse=None, scale=None,
                 stream=None):
-    """mha_fwd that also returns each row's log-sum-exp (fp32 inputs only).
+    """mha_fwd that also returns each row's log-sum-exp (fp32 or bf16 inputs).
 
-    Returns (out [B,H,Lq,D], lse [B,H,Lq] fp32, natural log, -inf for a row
-    with no visible key)."""
+    Returns (out [B,H,Lq,D] of q's dtype, lse [B,H,Lq] fp32, natural log,
+    -inf for a row with no visible key)."""
     torch = _torch()
-    _dev(q, "q", torch.float32)
-    _dev(k, "k", torch.float32)
-    _dev(v, "v", torch.float32)
+    _dev(q, "q")
+    _dev(k, "k", q.dtype)
+    _dev(v, "v", q.dtype)
     B, H, Lq, D = q.shape
     Lk = k.shape[2]
     if tuple(k.shape) != (B, H, Lk, D) or tuple(v.shape) != (B, H, Lk, D):
@@ -176,7 +176,7 @@ def mha_fwd_lse(q, k, v, mask_kind=MASK_NONE, kv_lengths=None, out=None, lse=Non
             raise ValueError("lse must be [B,H,Lq]")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     _check(lib().mha_fwd_lse(_ptr(q), _ptr(k), _ptr(v), int(mask_kind), _ptr(kv_lengths),
-                             _ptr(out), _ptr(lse), B, H, Lq, Lk, D, scale, F32,
+                             _ptr(out), _ptr(lse), B, H, Lq, Lk, D, scale, _dtype_code(q),
                              _stream(stream, q.get_device())), "mha_fwd_lse")
     return out, lse
 
@@ -185,11 +185,14 @@ def mha_bwd(q, k, v, out, dout, lse, mask_kind=MASK_NONE, kv_lengths=None, dq=No
             dv=None, scale=None, stream=None):
     """Gradients (dq, dk, dv) of sum(dout * out) for out, lse = mha_fwd_lse(q, k, v, ...).
 
-    fp32 only; every tensor contiguous on the same device.  q, k, v,
-    mask_kind, kv_lengths and scale must be those of the forward call."""
+    fp32 or bf16 (q, k, v, out, dout and the gradients of one dtype; lse fp32);
+    every tensor contiguous on the same device.  q, k, v, mask_kind,
+    kv_lengths and scale must be those of the forward call."""
     torch = _torch()
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (lse, "lse")):
-        _dev(t, n, torch.float32)
+    _dev(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _dev(t, n, q.dtype)
+    _dev(lse, "lse", torch.float32)
     B, H, Lq, D = q.shape
     Lk = k.shape[2]
     if tuple(k.shape) != (B, H, Lk, D) or tuple(v.shape) != (B, H, Lk, D):
@@ -200,13 +203,14 @@ def mha_bwd(q, k, v, out, dout, lse, mask_kind=MASK_NONE, kv_lengths=None, dq=No
         raise ValueError("lse must be [B,H,Lq]")
     if kv_lengths is not None:
         _dev(kv_lengths, "kv_lengths", torch.int32)
-    dq = torch.empty_like(q) if dq is None else _dev(dq, "dq", torch.float32)
-    dk = torch.empty_like(k) if dk is None else _dev(dk, "dk", torch.float32)
-    dv = torch.empty_like(v) if dv is None else _dev(dv, "dv", torch.float32)
+    dq = torch.empty_like(q) if dq is None else _dev(dq, "dq", q.dtype)
+    dk = torch.empty_like(k) if dk is None else _dev(dk, "dk", q.dtype)
+    dv = torch.empty_like(v) if dv is None else _dev(dv, "dv", q.dtype)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     _check(lib().mha_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
                          int(mask_kind), _ptr(kv_lengths), _ptr(dq), _ptr(dk), _ptr(dv),
-                         B, H, Lq, Lk, D, scale, F32, _stream(stream, q.get_device())), "mha_bwd")
+                         B, H, Lq, Lk, D, scale, _dtype_code(q), _stream(stream, q.get_device())),
+           "mha_bwd")
     return dq, dk, dv
 
 

@@ -1,7 +1,7 @@
 // api.cu -- the extern "C" boundary of libmha.so: argument validation,
 // dispatch by (entry point, dtype, D), and status reporting.  Host code only;
 // the kernels live in fwd_f32.cu, fwd_tf32.cu, fwd_bf16.cu, decode_bf16.cu and
-// bwd_f32.cu.
+// bwd.cu.
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -79,7 +79,7 @@ int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_kind,
     int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
     if (st != MHA_OK) return st;
     if (mask_kind < 0 || mask_kind > (MHA_MASK_CAUSAL | MHA_MASK_KV_LEN)) return MHA_ERR_INVALID_ARG;
-    if (dtype != MHA_F32) return MHA_ERR_UNSUPPORTED;
+    if (dtype != MHA_F32 && dtype != MHA_BF16) return MHA_ERR_UNSUPPORTED;
     if (empty) return MHA_OK;
     if (!q || !out || !lse || (Lk > 0 && (!k || !v))) return MHA_ERR_INVALID_ARG;
     if ((mask_kind & MHA_MASK_KV_LEN) && !kv_lengths) return MHA_ERR_INVALID_ARG;
@@ -87,10 +87,29 @@ int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_kind,
         (Lk > 0 && (!aligned16(k) || !aligned16(v))))
         return MHA_ERR_MISALIGNED;
     int drv = 0;
-    const cudaError_t e = mha::launch_fwd_f32(
-        static_cast<const float *>(q), static_cast<const float *>(k),
-        static_cast<const float *>(v), kv_lengths, static_cast<float *>(out), lse, B, H, Lq, Lk,
-        D, mask_kind, scale, stream, &drv);
+    cudaError_t e;
+    if (dtype == MHA_F32) {
+        e = mha::launch_fwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                                static_cast<const float *>(v), kv_lengths,
+                                static_cast<float *>(out), lse, B, H, Lq, Lk, D, mask_kind, scale,
+                                stream, &drv);
+    } else {
+        mha::Bf16Call c{};
+        c.q = q;
+        c.k = k;
+        c.v = v;
+        c.kv_lengths = kv_lengths;
+        c.out = out;
+        c.lse = lse;
+        c.B = B;
+        c.H = H;
+        c.Lq = Lq;
+        c.Lk = Lk;
+        c.D = D;
+        c.mask_kind = mask_kind;
+        c.scale = scale;
+        e = mha::launch_fwd_bf16(c, stream, &drv, nullptr);
+    }
     return drv != 0 ? MHA_ERR_CUDA : from_cuda(e);
 }
 
@@ -102,7 +121,7 @@ int mha_bwd(const void *q, const void *k, const void *v, const void *out, const 
     int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
     if (st != MHA_OK) return st;
     if (mask_kind < 0 || mask_kind > (MHA_MASK_CAUSAL | MHA_MASK_KV_LEN)) return MHA_ERR_INVALID_ARG;
-    if (dtype != MHA_F32) return MHA_ERR_UNSUPPORTED;
+    if (dtype != MHA_F32 && dtype != MHA_BF16) return MHA_ERR_UNSUPPORTED;
     // Lq == 0 with keys present still owes zero dk and dv.
     if (B == 0 || H == 0 || (Lq == 0 && Lk == 0)) return MHA_OK;
     (void)empty;
@@ -113,20 +132,30 @@ int mha_bwd(const void *q, const void *k, const void *v, const void *out, const 
                     !aligned16(dq))) ||
         (Lk > 0 && (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))))
         return MHA_ERR_MISALIGNED;
-    // Per-row Delta = dout . o lives in a stream-ordered workspace for this call.
-    float *delta = nullptr;
+    // Per-row Delta = dout . o (and, for bf16, the fp32 dq accumulator) live in
+    // a stream-ordered workspace for this call.
     const size_t rows = (size_t)B * H * Lq;
-    if (rows > 0 && cudaMallocAsync(reinterpret_cast<void **>(&delta), sizeof(float) * rows,
-                                    stream) != cudaSuccess)
+    const size_t delta_bytes = (sizeof(float) * rows + 255) & ~(size_t)255;
+    const size_t ws_bytes = delta_bytes + (dtype == MHA_BF16 ? sizeof(float) * rows * D : 0);
+    char *ws = nullptr;
+    if (ws_bytes > 0 &&
+        cudaMallocAsync(reinterpret_cast<void **>(&ws), ws_bytes, stream) != cudaSuccess)
         return MHA_ERR_CUDA;
-    cudaError_t e = mha::launch_bwd_f32(
-        static_cast<const float *>(q), static_cast<const float *>(k),
-        static_cast<const float *>(v), static_cast<const float *>(out),
-        static_cast<const float *>(dout), lse, kv_lengths, static_cast<float *>(dq),
-        static_cast<float *>(dk), static_cast<float *>(dv), delta, B, H, Lq, Lk, D, mask_kind,
-        scale, stream);
-    if (delta != nullptr) {
-        const cudaError_t ef = cudaFreeAsync(delta, stream);
+    float *delta = reinterpret_cast<float *>(ws);
+    cudaError_t e;
+    if (dtype == MHA_F32)
+        e = mha::launch_bwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                                static_cast<const float *>(v), static_cast<const float *>(out),
+                                static_cast<const float *>(dout), lse, kv_lengths,
+                                static_cast<float *>(dq), static_cast<float *>(dk),
+                                static_cast<float *>(dv), delta, B, H, Lq, Lk, D, mask_kind, scale,
+                                stream);
+    else
+        e = mha::launch_bwd_bf16(q, k, v, out, dout, lse, kv_lengths, dq, dk, dv,
+                                 reinterpret_cast<float *>(ws + delta_bytes), delta, B, H, Lq, Lk,
+                                 D, mask_kind, scale, stream);
+    if (ws != nullptr) {
+        const cudaError_t ef = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess) e = ef;
     }
     return from_cuda(e);

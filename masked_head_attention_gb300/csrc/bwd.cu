@@ -1,6 +1,8 @@
-// bwd_f32.cu -- backward pass of fused masked multi-head attention for fp32
-// inputs on CUDA-core FFMA (sm_103a): dq, dk, dv from q, k, v, the forward's
-// output o, its row log-sum-exp lse and the output gradient dout.
+// bwd.cu -- backward pass of fused masked multi-head attention on CUDA-core
+// FFMA (sm_103a): dq, dk, dv from q, k, v, the forward's output o, its row
+// log-sum-exp lse and the output gradient dout.  fp32 or bf16 inputs; the
+// arithmetic is fp32 either way, and the gradients come out in the input type
+// (for bf16, dq is accumulated in an fp32 workspace and converted at the end).
 //
 // The softmax weights are never stored by the forward; here they are formed
 // again from the saved row statistic, p_ij = exp(s_ij - lse_i), and the
@@ -11,9 +13,10 @@
 // o_i = sum_j p_ij v_j), so it costs one dot product per row instead of a
 // pass over the keys.
 //
-// Two kernels:
-//  1. bwd_row_delta: Delta_i = dout_i . o_i for every row, and dq zeroed (dq
-//     is accumulated by the second kernel).  HBM-bound, one pass.
+// Kernels:
+//  1. bwd_row_delta: Delta_i = dout_i . o_i for every row, and the fp32 dq
+//     accumulator zeroed (dq is accumulated by the second kernel).  HBM-bound,
+//     one pass.
 //  2. mha_bwd_f32_kernel: one CTA of 256 threads owns a 64-key tile of one
 //     (b, h) with K and V resident in shared memory, and walks the query
 //     tiles of 64 rows that can see any of its keys (under the causal rule:
@@ -24,7 +27,9 @@
 //     its share of dQ = dS K into global memory with 16-byte fp32 atomic
 //     adds.  dK (times scale) and dV are written once at the end; keys no
 //     row can see get zeros.
+//  3. (bf16) bwd_dq_convert: the fp32 dq accumulator to bf16.
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -46,38 +51,56 @@ struct BwdCfg {
         sizeof(float) * ((size_t)4 * 64 * LD + (size_t)2 * kBwdBM * LDP + 2 * kBwdBM);
 };
 
-// Rows [row0, row0 + 64) of a [rows, D] fp32 matrix into a padded tile;
+// Four consecutive elements as fp32 (bf16: an 8-byte load, widened).
+__device__ __forceinline__ float4 load4(const float *p) {
+    return __ldg(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+// Four consecutive elements from fp32 (bf16: rounded to nearest even).
+__device__ __forceinline__ void store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 v) {
+    uint2 u;
+    u.x = pack_bf16x2(v.x, v.y);
+    u.y = pack_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
+// Rows [row0, row0 + 64) of a [rows, D] matrix into a padded fp32 tile;
 // rows at or beyond `nrows` become zero.
-template <int D>
-__device__ __forceinline__ void bwd_load_tile(float *dst, const float *__restrict__ src,
-                                              int row0, int nrows, int tid) {
+template <int D, typename T>
+__device__ __forceinline__ void bwd_load_tile(float *dst, const T *__restrict__ src, int row0,
+                                              int nrows, int tid) {
     constexpr int V4 = D / 4;
 #pragma unroll
     for (int idx = tid; idx < 64 * V4; idx += kBwdThreads) {
         const int r = idx / V4, c = idx % V4;
         float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row0 + r < nrows)
-            val = __ldg(reinterpret_cast<const float4 *>(src + (size_t)(row0 + r) * D) + c);
+        if (row0 + r < nrows) val = load4(src + (size_t)(row0 + r) * D + 4 * c);
         *reinterpret_cast<float4 *>(dst + r * BwdCfg<D>::LD + 4 * c) = val;
     }
 }
 
-// Delta_i = dout_i . o_i; dq_i = 0.  A half-warp (16 lanes) per row.
-template <int D>
+// Delta_i = dout_i . o_i; dq_i = 0 (the fp32 accumulator).  A half-warp
+// (16 lanes) per row.
+template <int D, typename T>
 __global__ void __launch_bounds__(256)
-    bwd_row_delta_kernel(const float *__restrict__ o, const float *__restrict__ dout,
+    bwd_row_delta_kernel(const T *__restrict__ o, const T *__restrict__ dout,
                          float *__restrict__ delta, float *__restrict__ dq, int64_t rows) {
-    constexpr int PER = D / 64;   // float4 per lane
+    constexpr int PER = D / 64;   // groups of 4 elements per lane
     const int64_t row = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4);
     const int lane = threadIdx.x & 15;
     float acc = 0.f;
     if (row < rows) {
-        const float4 *po = reinterpret_cast<const float4 *>(o + row * D);
-        const float4 *pg = reinterpret_cast<const float4 *>(dout + row * D);
+        const T *po = o + row * D;
+        const T *pg = dout + row * D;
         float4 *pq = reinterpret_cast<float4 *>(dq + row * D);
 #pragma unroll
         for (int t = 0; t < PER; ++t) {
-            const float4 a = __ldg(po + lane + 16 * t), g = __ldg(pg + lane + 16 * t);
+            const float4 a = load4(po + 4 * (lane + 16 * t)), g = load4(pg + 4 * (lane + 16 * t));
             acc = fmaf(a.x, g.x, acc);
             acc = fmaf(a.y, g.y, acc);
             acc = fmaf(a.z, g.z, acc);
@@ -90,14 +113,13 @@ __global__ void __launch_bounds__(256)
     if (row < rows && lane == 0) delta[row] = acc;
 }
 
-template <int D>
+template <int D, typename T>
 __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
-    mha_bwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
-                       const float *__restrict__ v, const float *__restrict__ dout,
-                       const float *__restrict__ lse, const float *__restrict__ delta,
-                       const int32_t *__restrict__ kv_lengths, float *__restrict__ dq,
-                       float *__restrict__ dk, float *__restrict__ dv, int H, int Lq, int Lk,
-                       int mask_kind, float scale, float scale_log2) {
+    mha_bwd_f32_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                       const T *__restrict__ dout, const float *__restrict__ lse,
+                       const float *__restrict__ delta, const int32_t *__restrict__ kv_lengths,
+                       float *__restrict__ dq, T *__restrict__ dk, T *__restrict__ dv, int H,
+                       int Lq, int Lk, int mask_kind, float scale, float scale_log2) {
     using C = BwdCfg<D>;
     constexpr int OC = C::OC;
     extern __shared__ float4 bwd_smem[];
@@ -114,10 +136,10 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
     const int k0 = blockIdx.x * kBwdBN;
     const int h = blockIdx.y, b = blockIdx.z;
     const size_t bh = (size_t)b * H + h;
-    const float *Qg = q + bh * (size_t)Lq * D;
-    const float *Kg = k + bh * (size_t)Lk * D;
-    const float *Vg = v + bh * (size_t)Lk * D;
-    const float *Gg = dout + bh * (size_t)Lq * D;
+    const T *Qg = q + bh * (size_t)Lq * D;
+    const T *Kg = k + bh * (size_t)Lk * D;
+    const T *Vg = v + bh * (size_t)Lk * D;
+    const T *Gg = dout + bh * (size_t)Lq * D;
     const float *Lg = lse + bh * (size_t)Lq;
     const float *Dg = delta + bh * (size_t)Lq;
     float *dQg = dq + bh * (size_t)Lq * D;
@@ -145,15 +167,15 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
         }
 
     if (qt0 < qt1) {
-        bwd_load_tile<D>(sK, Kg, k0, Lk, tid);
-        bwd_load_tile<D>(sV, Vg, k0, Lk, tid);
+        bwd_load_tile<D, T>(sK, Kg, k0, Lk, tid);
+        bwd_load_tile<D, T>(sV, Vg, k0, Lk, tid);
     }
 
     for (int qt = qt0; qt < qt1; ++qt) {
         const int q0 = qt * kBwdBM;
         __syncthreads();   // the previous tile is done with sQ, sG, sP, sS, sL, sDl
-        bwd_load_tile<D>(sQ, Qg, q0, Lq, tid);
-        bwd_load_tile<D>(sG, Gg, q0, Lq, tid);
+        bwd_load_tile<D, T>(sQ, Qg, q0, Lq, tid);
+        bwd_load_tile<D, T>(sG, Gg, q0, Lq, tid);
         if (tid < kBwdBM) {
             const int row = q0 + tid;
             sL[tid] = row < Lq ? Lg[row] * 1.4426950408889634f : 0.f;
@@ -287,8 +309,8 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
 
     // dK = scale * dS^T Q, dV = P^T dout for the tile's keys (zeros where no
     // row could see the key).
-    float *dKg = dk + bh * (size_t)Lk * D;
-    float *dVg = dv + bh * (size_t)Lk * D;
+    T *dKg = dk + bh * (size_t)Lk * D;
+    T *dVg = dv + bh * (size_t)Lk * D;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int key = k0 + ty * 4 + i;
@@ -296,40 +318,53 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
 #pragma unroll
         for (int hv = 0; hv < OC / 4; ++hv) {
             const size_t off = (size_t)key * D + tx * 4 + 64 * hv;
-            *reinterpret_cast<float4 *>(dVg + off) =
-                make_float4(accv[i][2 * hv].x, accv[i][2 * hv].y, accv[i][2 * hv + 1].x,
-                            accv[i][2 * hv + 1].y);
-            *reinterpret_cast<float4 *>(dKg + off) =
-                make_float4(acck[i][2 * hv].x * scale, acck[i][2 * hv].y * scale,
-                            acck[i][2 * hv + 1].x * scale, acck[i][2 * hv + 1].y * scale);
+            store4(dVg + off, make_float4(accv[i][2 * hv].x, accv[i][2 * hv].y,
+                                          accv[i][2 * hv + 1].x, accv[i][2 * hv + 1].y));
+            store4(dKg + off, make_float4(acck[i][2 * hv].x * scale, acck[i][2 * hv].y * scale,
+                                          acck[i][2 * hv + 1].x * scale, acck[i][2 * hv + 1].y * scale));
         }
     }
 }
 
-template <int D>
-cudaError_t launch_bwd(const float *q, const float *k, const float *v, const float *o,
-                       const float *dout, const float *lse, const int32_t *kv, float *dq,
-                       float *dk, float *dv, float *delta, int B, int H, int Lq, int Lk,
-                       int mask_kind, float scale, cudaStream_t stream) {
+// dq (bf16) from the fp32 accumulator, 8 elements per thread.
+__global__ void __launch_bounds__(256)
+    bwd_dq_convert_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, int64_t n8) {
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (i >= n8) return;
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(acc) + 2 * i);
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(acc) + 2 * i + 1);
+    uint4 u;
+    u.x = pack_bf16x2(a.x, a.y);
+    u.y = pack_bf16x2(a.z, a.w);
+    u.z = pack_bf16x2(b.x, b.y);
+    u.w = pack_bf16x2(b.z, b.w);
+    reinterpret_cast<uint4 *>(dq)[i] = u;
+}
+
+template <int D, typename T>
+cudaError_t launch_bwd(const T *q, const T *k, const T *v, const T *o, const T *dout,
+                       const float *lse, const int32_t *kv, float *dq_acc, T *dk, T *dv,
+                       float *delta, int B, int H, int Lq, int Lk, int mask_kind, float scale,
+                       cudaStream_t stream) {
     const int64_t rows = (int64_t)B * H * Lq;
     cudaError_t e = cudaSuccess;
     if (rows > 0) {
-        bwd_row_delta_kernel<D><<<(unsigned)((rows + 15) / 16), 256, 0, stream>>>(o, dout, delta,
-                                                                                 dq, rows);
+        bwd_row_delta_kernel<D, T><<<(unsigned)((rows + 15) / 16), 256, 0, stream>>>(
+            o, dout, delta, dq_acc, rows);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess || Lk == 0) return e;
     constexpr size_t smem = BwdCfg<D>::kSmem;
     static bool configured = false;
     if (!configured) {
-        e = cudaFuncSetAttribute(mha_bwd_f32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+        e = cudaFuncSetAttribute(mha_bwd_f32_kernel<D, T>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const dim3 grid((Lk + kBwdBN - 1) / kBwdBN, H, B);
-    mha_bwd_f32_kernel<D><<<grid, kBwdThreads, smem, stream>>>(
-        q, k, v, dout, lse, delta, kv, dq, dk, dv, H, Lq, Lk, mask_kind, scale,
+    mha_bwd_f32_kernel<D, T><<<grid, kBwdThreads, smem, stream>>>(
+        q, k, v, dout, lse, delta, kv, dq_acc, dk, dv, H, Lq, Lk, mask_kind, scale,
         scale * 1.4426950408889634f);
     return cudaGetLastError();
 }
@@ -341,10 +376,33 @@ cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const
                            float *dq, float *dk, float *dv, float *delta, int B, int H, int Lq,
                            int Lk, int D, int mask_kind, float scale, cudaStream_t stream) {
     if (D == 64)
-        return launch_bwd<64>(q, k, v, o, dout, lse, kv_lengths, dq, dk, dv, delta, B, H, Lq, Lk,
-                              mask_kind, scale, stream);
-    return launch_bwd<128>(q, k, v, o, dout, lse, kv_lengths, dq, dk, dv, delta, B, H, Lq, Lk,
-                           mask_kind, scale, stream);
+        return launch_bwd<64, float>(q, k, v, o, dout, lse, kv_lengths, dq, dk, dv, delta, B, H,
+                                     Lq, Lk, mask_kind, scale, stream);
+    return launch_bwd<128, float>(q, k, v, o, dout, lse, kv_lengths, dq, dk, dv, delta, B, H, Lq,
+                                  Lk, mask_kind, scale, stream);
+}
+
+cudaError_t launch_bwd_bf16(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, const float *lse, const int32_t *kv_lengths,
+                            void *dq, void *dk, void *dv, float *dq_acc, float *delta, int B,
+                            int H, int Lq, int Lk, int D, int mask_kind, float scale,
+                            cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+    const bf *Q = static_cast<const bf *>(q), *K = static_cast<const bf *>(k);
+    const bf *V = static_cast<const bf *>(v), *O = static_cast<const bf *>(o);
+    const bf *G = static_cast<const bf *>(dout);
+    bf *dK = static_cast<bf *>(dk), *dV = static_cast<bf *>(dv);
+    cudaError_t e =
+        D == 64 ? launch_bwd<64, bf>(Q, K, V, O, G, lse, kv_lengths, dq_acc, dK, dV, delta, B, H,
+                                     Lq, Lk, mask_kind, scale, stream)
+                : launch_bwd<128, bf>(Q, K, V, O, G, lse, kv_lengths, dq_acc, dK, dV, delta, B, H,
+                                      Lq, Lk, mask_kind, scale, stream);
+    if (e != cudaSuccess) return e;
+    const int64_t n8 = (int64_t)B * H * Lq * D / 8;
+    if (n8 == 0) return cudaSuccess;
+    bwd_dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(
+        dq_acc, static_cast<bf *>(dq), n8);
+    return cudaGetLastError();
 }
 
 }  // namespace mha

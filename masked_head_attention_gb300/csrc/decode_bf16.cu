@@ -83,8 +83,8 @@ template <int D, int R>
 __global__ void __launch_bounds__(kDecThreads, 1)
     attn_decode_bf16_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                             const __nv_bfloat16 *__restrict__ v, const int32_t *__restrict__ kv_lengths,
-                            __nv_bfloat16 *__restrict__ out, int H, int Lq, int Lk, int mask_kind,
-                            float scale_log2, int chunk) {
+                            __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, int H,
+                            int Lq, int Lk, int mask_kind, float scale_log2, int chunk) {
     constexpr int DC = D / 32;   // output columns per lane
     __shared__ float sQ[R][D];
     __shared__ DecPartial<D, R> sW[kDecWarps];   // per-warp partials
@@ -253,6 +253,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         // A row that saw no visible key is written as zeros.
         const float inv = ll > 0.f ? 1.f / ll : 0.f;
+        if (lse != nullptr && lane == 0)
+            lse[(size_t)bh * Lq + r] =
+                (ll > 0.f && mm != -INFINITY) ? 0.69314718055994531f * (mm + log2f(ll)) : -INFINITY;
         __nv_bfloat16 *dst = out + ((size_t)bh * Lq + r) * D + lane * DC;
 #pragma unroll
         for (int c = 0; c < DC; ++c) dst[c] = __float2bfloat16_rn(oc[c] * inv);
@@ -283,7 +286,7 @@ cudaError_t launch_dec(const Bf16Call &c, int splits, int chunk, cudaStream_t st
                               reinterpret_cast<const __nv_bfloat16 *>(c.k),
                               reinterpret_cast<const __nv_bfloat16 *>(c.v),
                               (c.mask_kind & 2) ? c.kv_lengths : nullptr,
-                              reinterpret_cast<__nv_bfloat16 *>(c.out), c.H, c.Lq, c.Lk,
+                              reinterpret_cast<__nv_bfloat16 *>(c.out), c.lse, c.H, c.Lq, c.Lk,
                               c.mask_kind, c.scale * 1.4426950408889634f, chunk);
 }
 

@@ -81,6 +81,7 @@ struct AttnParams {
     const float *beta;
     const int32_t *kv_lengths;   // null unless the kv-length mask is on
     const __nv_bfloat16 *residual;   // Pre-LN with residual add: x [B][Lq][H*D]; else null
+    float *lse;           // self-attention: row log-sum-exp [B*H][Lq] (natural log), or null
     int B, H, Lq, Lk;
     int causal;
     float scale_log2;     // scale * log2(e)
@@ -618,12 +619,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int cc = 0; cc < kTileRows; ++cc)
                         if (cc >= lim) s[cc] = f2u(-INFINITY);
                 }
-                // Row max: eight independent chains of three-input max.
+                // Row max: eight independent chains of three-input max over
+                // columns 8..119, the first and last eight columns by two-input max.
+                static_assert((kTileRows - 16) % 16 == 0, "row max covers the tile exactly");
                 float mx[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) mx[q] = u2f(s[q]);
+                for (int q = 0; q < 8; ++q) mx[q] = fmaxf(u2f(s[q]), u2f(s[kTileRows - 8 + q]));
 #pragma unroll
-                for (int cc = 8; cc < kTileRows; cc += 16)
+                for (int cc = 8; cc < kTileRows - 8; cc += 16)
 #pragma unroll
                     for (int q = 0; q < 8; ++q) mx[q] = max3f(mx[q], u2f(s[cc + q]), u2f(s[cc + 8 + q]));
                 const float m_tile = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
@@ -750,6 +753,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(dst + ch * 8) =
                         res ? __ldg(res + ch) : make_uint4(0, 0, 0, 0);
             }
+            // Row log-sum-exp (natural log) of the scaled logits, from the base-2
+            // running max and sum: ln(2) * (m + log2(l)); -inf with no visible key.
+            if (!PRENORM && p.lse != nullptr && row < p.Lq)
+                p.lse[(size_t)it.bh * p.Lq + row] =
+                    (n > 0 && l > 0.f && m_used != -INFINITY) ? 0.69314718055994531f * (m_used + log2f(l))
+                                                             : -INFINITY;
             c += n;
             e += n > 0 ? 1 : 0;
             ++k;
@@ -1037,6 +1046,7 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     p.beta = c.beta;
     p.kv_lengths = (c.mask_kind & 2) ? c.kv_lengths : nullptr;
     p.residual = prenorm ? reinterpret_cast<const __nv_bfloat16 *>(c.residual) : nullptr;
+    p.lse = prenorm ? nullptr : c.lse;
     p.B = c.B;
     p.H = c.H;
     p.Lq = c.Lq;

@@ -38,12 +38,19 @@ cudaError_t launch_fwd_tf32x3(const float *q, const float *k, const float *v,
                               cudaStream_t stream, int *driver_err);
 cudaError_t read_device_status_tf32(uint32_t *bits, bool clear);
 
-// fp32 backward (bwd_f32.cu): dq, dk, dv from q, k, v, the forward output o,
-// its row log-sum-exp and dout.  `delta` is device scratch of B*H*Lq floats.
+// Backward (bwd.cu): dq, dk, dv from q, k, v, the forward output o, its row
+// log-sum-exp and dout.  `delta` is device scratch of B*H*Lq floats.  fp32:
+// dq is accumulated in place.  bf16: `dq_acc` is fp32 scratch of B*H*Lq*D
+// floats, converted into dq at the end.
 cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const float *o,
                            const float *dout, const float *lse, const int32_t *kv_lengths,
                            float *dq, float *dk, float *dv, float *delta, int B, int H, int Lq,
                            int Lk, int D, int mask_kind, float scale, cudaStream_t stream);
+cudaError_t launch_bwd_bf16(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, const float *lse, const int32_t *kv_lengths,
+                            void *dq, void *dk, void *dv, float *dq_acc, float *delta, int B,
+                            int H, int Lq, int Lk, int D, int mask_kind, float scale,
+                            cudaStream_t stream);
 
 // bf16 tensor-core path (fwd_bf16.cu).  x/gamma/beta are null for plain
 // self-attention; for the Pre-LN variant q is null and x/gamma/beta are set.
@@ -58,6 +65,7 @@ struct Bf16Call {
     const void *v;
     const int32_t *kv_lengths;
     void *out;              // [B,H,Lq,D] or [B,Lq,H*D]
+    float *lse;             // self-attention: row log-sum-exp [B,H,Lq] (natural log), or null
     int B, H, Lq, Lk, D;
     int mask_kind;
     float scale;

@@ -107,7 +107,7 @@ def fwd_lse(L, q=A, k=A2, v=A3, mask=0, lens=None, out=OUT, lse=LSE, B=2, H=2, L
 
 @pytest.mark.parametrize("kw,want", [
     (dict(lse=None), INVALID), (dict(q=None), INVALID), (dict(mask=8), INVALID),
-    (dict(dtype=1), UNSUPPORTED), (dict(D=80), UNSUPPORTED),
+    (dict(dtype=5), UNSUPPORTED), (dict(D=80), UNSUPPORTED),
     (dict(lse=ctypes.c_void_p(0x50004)), MISALIGNED), (dict(Lq=0), OK), (dict(B=0), OK),
 ])
 def test_fwd_lse_host_validation(L, kw, want):
@@ -124,7 +124,7 @@ def bwd(L, q=A, k=A2, v=A3, o=OUT, g=G, lse=LSE, mask=0, lens=None, dq=DQ, dk=DK
     (dict(g=None), INVALID), (dict(lse=None), INVALID), (dict(dq=None), INVALID),
     (dict(dk=None), INVALID), (dict(o=None), INVALID), (dict(mask=2, lens=None), INVALID),
     (dict(scale=0.0), INVALID), (dict(Lq=-1), INVALID),
-    (dict(dtype=1), UNSUPPORTED), (dict(D=32), UNSUPPORTED),
+    (dict(dtype=2), UNSUPPORTED), (dict(D=32), UNSUPPORTED),
     (dict(dv=ctypes.c_void_p(0x90008)), MISALIGNED), (dict(g=ctypes.c_void_p(0x60004)), MISALIGNED),
     (dict(B=0), OK), (dict(H=0), OK), (dict(Lq=0, Lk=0), OK),
     # Lq == 0 still writes dk, dv: the query-side pointers are not needed

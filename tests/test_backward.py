@@ -141,3 +141,68 @@ def test_backward_workload_full():
                                                         ("dv", dv, wv))]
     print(w.name, "dq %.2e dk %.2e dv %.2e" % tuple(errs))
     assert mha.device_status() == 0
+
+
+# bf16: the same computation in fp32 from bf16 inputs, gradients rounded to
+# bf16 once.  Error sources beyond fp32 rounding: the bf16 output rounding of
+# each gradient (half an ulp, 2^-9 relative) and Delta = dout . o formed from
+# the forward's bf16-rounded o (each o element within 2^-9 relative), which
+# moves dS = P (dP - Delta) by P * |dout| * |o| * 2^-9 per row.  Bound:
+#   per element |gpu - oracle| <= ulp_bf16(oracle) / 2 + BF16_GRAD_ABS * s
+#   mean |gpu - oracle| <= BF16_GRAD_MEAN * s,  s = max(1, max |oracle|)
+BF16_GRAD_ABS = 1e-2
+BF16_GRAD_MEAN = 1e-3
+
+BF16_CASES = [
+    (1, 1, 1, 1, 64, 0, None),
+    (2, 2, 70, 90, 64, 2, [90, 45]),
+    (1, 2, 130, 200, 128, 1, None),
+    (2, 3, 257, 129, 64, 3, [1, 129]),
+    (2, 2, 64, 64, 128, 2, [0, 64]),
+    (2, 2, 4, 700, 128, 2, [700, 300]),   # few query rows: the decode kernel's log-sum-exp
+]
+
+
+def check_grad_bf16(got, want, what):
+    from parity_util import ulp_bf16
+    got = np.asarray(got, np.float64)
+    assert np.all(np.isfinite(got)), "%s: non-finite gradient" % what
+    if got.size == 0:
+        return 0.0, 0.0
+    s = max(1.0, float(np.abs(want).max()))
+    err = np.abs(got - want)
+    tol = ulp_bf16(want) / 2 + BF16_GRAD_ABS * s
+    bad = err > tol
+    assert not bad.any(), "%s: %d elements over tolerance, worst %.3g (scale %.3g)" % (
+        what, bad.sum(), err.max(), s)
+    assert err.mean() <= BF16_GRAD_MEAN * s, "%s: mean abs %.3g > %.3g" % (
+        what, err.mean(), BF16_GRAD_MEAN * s)
+    return float(err.max() / s), float(err.mean() / s)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", BF16_CASES, ids=lambda c: "B%dH%dLq%dLk%dD%dm%d" % c[:6])
+def test_backward_parity_bf16(case):
+    B, H, Lq, Lk, D, mask, lens = case
+    q = randn((B, H, Lq, D), 121, 1.0, torch.bfloat16)
+    k = randn((B, H, Lk, D), 122, 1.0, torch.bfloat16)
+    v = randn((B, H, Lk, D), 123, 1.0, torch.bfloat16)
+    g = randn((B, H, Lq, D), 124, 1.0, torch.bfloat16)
+    lt = dev(lens_tensor(lens))
+    out, lse = mha.mha_fwd_lse(dev(q), dev(k), dev(v), mask, lt)
+    dq, dk, dv = mha.mha_bwd(dev(q), dev(k), dev(v), out, dev(g), lse, mask, lt)
+    torch.cuda.synchronize()
+    assert dq.dtype == torch.bfloat16 and dk.dtype == torch.bfloat16
+    qn, kn, vn, gn = (t.float().numpy() for t in (q, k, v, g))
+    want_lse = oracle.mha_lse(qn, kn, mask, lens)
+    got_lse = as_np(lse)
+    fin = np.isfinite(want_lse)
+    assert np.array_equal(np.isfinite(got_lse), fin), "lse: -inf rows differ"
+    if fin.any():
+        assert np.abs(got_lse[fin] - want_lse[fin]).max() <= 1e-4, "lse"
+    wq, wk, wv = oracle.mha_bwd(qn, kn, vn, gn, mask, lens)
+    r = [check_grad_bf16(as_np(t), w, "%s %s" % (n, case))
+         for n, t, w in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv))]
+    print(case, "relative max/mean: dq %.1e/%.1e dk %.1e/%.1e dv %.1e/%.1e" % (
+        r[0] + r[1] + r[2]))
+    assert mha.device_status() == 0

@@ -164,3 +164,21 @@ def test_bf16_many_items_per_cta_mixed_work(D, ctas):
         mha.set_bf16_grid(0)
     want = oracle.mha_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), 3, lens)
     check_bf16(as_np(out), want, "many items D=%d ctas=%d" % (D, ctas))
+
+
+@pytest.mark.gpu
+def test_single_visible_key_returns_its_v_row():
+    """A row with exactly one visible key has softmax weight 1 on it, so its
+    output is that key's V row, bit for bit in bf16 -- whatever the sign of
+    the logit (the row maximum is that logit itself)."""
+    B, H, Lq, Lk, D = 2, 3, 300, 129, 64
+    q = randn((B, H, Lq, D), 131, 1.0, torch.bfloat16)
+    k = randn((B, H, Lk, D), 132, 1.0, torch.bfloat16)
+    v = randn((B, H, Lk, D), 133, 1.0, torch.bfloat16)
+    lens = torch.tensor([1, 129], dtype=torch.int32)
+    for mask in (2, 3):
+        out = mha.mha_fwd(dev(q), dev(k), dev(v), mask, dev(lens)).cpu()
+        assert torch.equal(out[0], v[0, :, 0:1, :].expand(H, Lq, D)), "mask %d" % mask
+        if mask & 1:   # causal: row 0 of every batch sees key 0 only
+            assert torch.equal(out[1, :, 0], v[1, :, 0])
+    assert mha.device_status() == 0
