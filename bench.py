@@ -43,6 +43,7 @@ KERNEL_OF = {  # dominant kernel of each workload
     "prenorm:bf16": "attn_fwd_bf16_kernel<prenorm>",
     "prenorm_residual:bf16": "attn_fwd_bf16_kernel<prenorm>",
     "mha_bwd:f32": "mha_bwd_f32_kernel",
+    "mha_bwd:bf16": "attn_bwd_bf16_kernel",   # tensor cores: key- and query-stationary kernels
 }
 SMALL_F32_MAX_KD = 16384   # the fp32 path stages all keys at once when Lk * D is at most this
 DECODE_MAX_ROWS = 8        # bf16 self-attention with at most this many query rows: decode kernel
@@ -218,7 +219,8 @@ class GpuWorkload:
         out_like = self.host["q"] if w.kind in ("mha", "mha_bwd") else self.host["x"]
         set_bytes += out_like.numel() * out_like.element_size()
         if w.kind == "mha_bwd":   # o and lse (inputs), dq, dk, dv (outputs)
-            set_bytes += 3 * out_like.numel() * 4 + self.host["k"].numel() * 8
+            e = out_like.element_size()
+            set_bytes += 2 * out_like.numel() * e + out_like.numel() // w.D * 4 + self.host["k"].numel() * 2 * e
         self.set_bytes = set_bytes
         n = max(1, math.ceil(2 * l2_bytes / set_bytes))
         n = max(1, min(n, max_bytes // set_bytes))
@@ -266,7 +268,7 @@ class GpuWorkload:
         o = self.sets[0]["out"]
         n = o.numel() * o.element_size()
         if self.w.kind == "mha_bwd":
-            n += 2 * self.sets[0]["dk"].numel() * 4
+            n += 2 * self.sets[0]["dk"].numel() * self.sets[0]["dk"].element_size()
         return n
 
 

@@ -132,14 +132,20 @@ MHA_API int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_ki
  *               last bits can differ between runs).  Must not alias any
  *               input.
  *   dtype       MHA_F32 or MHA_BF16: q, k, v, out, dout and the gradients
- *               all of that type; the arithmetic is fp32 either way and the
- *               bf16 gradients are rounded once, to nearest even.
+ *               all of that type, rounded once (to nearest even) for bf16.
+ * Kernels.  fp32: CUDA-core FFMA, a row pass (Delta, dq = 0) and a key-tile
+ * kernel adding dq with fp32 atomics (its last bits can differ between
+ * runs).  bf16 (default): the tensor cores, fp32 accumulation in TMEM, P and
+ * dS rounded to bf16 for the products; the row pass (Delta), a key-
+ * stationary kernel writing dk and dv and a query-stationary kernel writing
+ * dq -- every element written once, the same on every run.  bf16 with
+ * mha_set_bwd_kernel(1): the CUDA-core kernels (fp32 arithmetic, dq through
+ * an fp32 accumulator and a conversion pass).
  * Memory: a stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on
- * `stream`) of 4*B*H*Lq bytes (rounded up to 256) for Delta, plus, for
- * bf16, 4*B*H*Lq*D bytes for the fp32 dq accumulator.  Kernels on `stream`:
- * a row pass (Delta, dq accumulator = 0), the key-tile kernel and, for
- * bf16, the conversion of dq.  Lq == 0 with Lk > 0 writes zero dk and dv.
- * Returns MHA_OK or a negative mha_status.
+ * `stream`) of 4*B*H*Lq bytes (rounded up to 256) for Delta, plus, for bf16
+ * on CUDA cores, 4*B*H*Lq*D bytes for the fp32 dq accumulator.  Lq == 0
+ * with Lk > 0 writes zero dk and dv.  Returns MHA_OK or a negative
+ * mha_status.
  */
 MHA_API int mha_bwd(const void *q, const void *k, const void *v, const void *out,
                     const void *dout, const float *lse, int mask_kind,
@@ -280,6 +286,14 @@ MHA_API void mha_set_bf16_decode(int mode);
  * from any thread of the process.
  */
 MHA_API void mha_set_bf16_decode_splits(int splits);
+
+/*
+ * mha_set_bwd_kernel -- kernel-choice hook for tests and benchmarks of
+ * mha_bwd: 0 = automatic (bf16 on the tensor cores, fp32 on CUDA cores);
+ * 1 = CUDA cores for both.  Other values act as 0.  Affects later calls from
+ * any thread of the process.
+ */
+MHA_API void mha_set_bwd_kernel(int which);
 
 #ifdef __cplusplus
 }

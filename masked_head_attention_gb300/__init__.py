@@ -68,6 +68,8 @@ def lib():
         L.mha_set_bf16_decode.restype = None
         L.mha_set_bf16_decode_splits.argtypes = [i]
         L.mha_set_bf16_decode_splits.restype = None
+        L.mha_set_bwd_kernel.argtypes = [i]
+        L.mha_set_bwd_kernel.restype = None
         _lib = L
     return _lib
 
@@ -306,6 +308,11 @@ def set_bf16_decode(mode):
 def set_bf16_decode_splits(splits):
     """Force the decode kernel's CTAs per (b, h) (1..8); 0 = automatic."""
     lib().mha_set_bf16_decode_splits(int(splits))
+
+
+def set_bwd_kernel(which):
+    """Backward kernels: 0 automatic (bf16 on the tensor cores), 1 CUDA cores."""
+    lib().mha_set_bwd_kernel(int(which))
 
 
 def set_f32_kernel(which):

@@ -15,6 +15,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA; }
 
+// Backward kernel choice: 0 automatic (bf16 on the tensor cores, fp32 on CUDA
+// cores), 1 CUDA cores for both.
+int g_bwd_kernel = 0;
+
 // Shared checks of the shape arguments; 1 means "nothing to do".
 int check_shape(int B, int H, int Lq, int Lk, int D, float scale, int *empty) {
     *empty = 0;
@@ -132,18 +136,26 @@ int mha_bwd(const void *q, const void *k, const void *v, const void *out, const 
                     !aligned16(dq))) ||
         (Lk > 0 && (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))))
         return MHA_ERR_MISALIGNED;
-    // Per-row Delta = dout . o (and, for bf16, the fp32 dq accumulator) live in
-    // a stream-ordered workspace for this call.
+    // Per-row Delta = dout . o (and, for bf16 on CUDA cores, the fp32 dq
+    // accumulator) live in a stream-ordered workspace for this call.
+    const bool tensor = dtype == MHA_BF16 && g_bwd_kernel != 1;
     const size_t rows = (size_t)B * H * Lq;
     const size_t delta_bytes = (sizeof(float) * rows + 255) & ~(size_t)255;
-    const size_t ws_bytes = delta_bytes + (dtype == MHA_BF16 ? sizeof(float) * rows * D : 0);
+    const size_t ws_bytes =
+        delta_bytes + (dtype == MHA_BF16 && !tensor ? sizeof(float) * rows * D : 0);
     char *ws = nullptr;
     if (ws_bytes > 0 &&
         cudaMallocAsync(reinterpret_cast<void **>(&ws), ws_bytes, stream) != cudaSuccess)
         return MHA_ERR_CUDA;
     float *delta = reinterpret_cast<float *>(ws);
     cudaError_t e;
-    if (dtype == MHA_F32)
+    int drv = 0;
+    if (tensor) {
+        e = mha::launch_bwd_row_delta_bf16(out, dout, delta, (int64_t)rows, D, stream);
+        if (e == cudaSuccess)
+            e = mha::launch_bwd_bf16_tensor(q, k, v, dout, lse, delta, kv_lengths, dq, dk, dv, B, H,
+                                            Lq, Lk, D, mask_kind, scale, stream, &drv);
+    } else if (dtype == MHA_F32)
         e = mha::launch_bwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
                                 static_cast<const float *>(v), static_cast<const float *>(out),
                                 static_cast<const float *>(dout), lse, kv_lengths,
@@ -158,6 +170,7 @@ int mha_bwd(const void *q, const void *k, const void *v, const void *out, const 
         const cudaError_t ef = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess) e = ef;
     }
+    if (drv != 0) return MHA_ERR_CUDA;
     return from_cuda(e);
 }
 
@@ -315,5 +328,7 @@ void mha_set_f32_kernel(int which) { mha::set_f32_kernel_override(which); }
 void mha_set_bf16_decode(int mode) { mha::set_decode_override(mode); }
 
 void mha_set_bf16_decode_splits(int splits) { mha::set_decode_splits(splits); }
+
+void mha_set_bwd_kernel(int which) { g_bwd_kernel = (which == 1) ? 1 : 0; }
 
 }  // extern "C"

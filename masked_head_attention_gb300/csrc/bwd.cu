@@ -84,8 +84,8 @@ __device__ __forceinline__ void bwd_load_tile(float *dst, const T *__restrict__ 
     }
 }
 
-// Delta_i = dout_i . o_i; dq_i = 0 (the fp32 accumulator).  A half-warp
-// (16 lanes) per row.
+// Delta_i = dout_i . o_i; dq_i = 0 (the fp32 accumulator; skipped when dq is
+// null).  A half-warp (16 lanes) per row.
 template <int D, typename T>
 __global__ void __launch_bounds__(256)
     bwd_row_delta_kernel(const T *__restrict__ o, const T *__restrict__ dout,
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256)
     if (row < rows) {
         const T *po = o + row * D;
         const T *pg = dout + row * D;
-        float4 *pq = reinterpret_cast<float4 *>(dq + row * D);
+        float4 *pq = dq != nullptr ? reinterpret_cast<float4 *>(dq + row * D) : nullptr;
 #pragma unroll
         for (int t = 0; t < PER; ++t) {
             const float4 a = load4(po + 4 * (lane + 16 * t)), g = load4(pg + 4 * (lane + 16 * t));
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(256)
             acc = fmaf(a.y, g.y, acc);
             acc = fmaf(a.z, g.z, acc);
             acc = fmaf(a.w, g.w, acc);
-            pq[lane + 16 * t] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (dq != nullptr) pq[lane + 16 * t] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
 #pragma unroll
@@ -380,6 +380,20 @@ cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const
                                      Lq, Lk, mask_kind, scale, stream);
     return launch_bwd<128, float>(q, k, v, o, dout, lse, kv_lengths, dq, dk, dv, delta, B, H, Lq,
                                   Lk, mask_kind, scale, stream);
+}
+
+cudaError_t launch_bwd_row_delta_bf16(const void *o, const void *dout, float *delta, int64_t rows,
+                                      int D, cudaStream_t stream) {
+    if (rows <= 0) return cudaSuccess;
+    using bf = __nv_bfloat16;
+    const unsigned grid = (unsigned)((rows + 15) / 16);
+    if (D == 64)
+        bwd_row_delta_kernel<64, bf><<<grid, 256, 0, stream>>>(
+            static_cast<const bf *>(o), static_cast<const bf *>(dout), delta, nullptr, rows);
+    else
+        bwd_row_delta_kernel<128, bf><<<grid, 256, 0, stream>>>(
+            static_cast<const bf *>(o), static_cast<const bf *>(dout), delta, nullptr, rows);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_bf16(const void *q, const void *k, const void *v, const void *o,

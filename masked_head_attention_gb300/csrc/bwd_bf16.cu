@@ -1,0 +1,464 @@
+// bwd_bf16.cu -- backward pass of fused masked multi-head attention for bf16
+// inputs on the sm_103a tensor cores (tcgen05 MMAs accumulating in TMEM,
+// operands staged by TMA).
+//
+// The softmax weights are formed again from the forward's row log-sum-exp,
+// p_ij = 2^(s_ij * scale * log2(e) - lse_i * log2(e)), and the softmax
+// Jacobian of "Why attention must compute the max first" (gsyq.cn, section
+// 3.3) is applied as dS_ij = p_ij (dP_ij - Delta_i), dP_ij = dout_i . v_j,
+// Delta_i = dout_i . o_i (one row pass, shared with the CUDA-core backward).
+// Two kernels of one template, each holding 128 rows of one (b, h) in TMEM
+// lanes and streaming 64-row tiles of the other side:
+//   KV = true  (key-stationary): rows = keys, stream query tiles.
+//              S^T = K Q^T, dP^T = V dout^T; P^T and dS^T into TMEM;
+//              dV += P^T dout, dK += dS^T Q  (dK scaled at the end).
+//   KV = false (query-stationary): rows = queries, stream key tiles.
+//              S = Q K^T, dP = dout V^T; dS into TMEM; dQ += dS K.
+// No atomics: every gradient element is written once, the same on every run.
+// The price is forming S and dP twice (seven products instead of five).
+//
+// CTA = 6 warps: warps 0-3 softmax (thread t owns row t, TMEM lane t),
+// warp 4 TMA producer, warp 5 MMA issuer and TMEM owner.  Stream tiles go
+// through two shared-memory stages.  Per stream tile j the MMA warp issues
+// S(j) and dP(j), waits for the softmax's P / dS, then the accumulating
+// products, which read the stage and the P / dS columns before S(j + 1)
+// overwrites them (the tensor pipe executes one thread's MMAs in order).
+// TMEM: S 0-63 (P / dS packed bf16 pairs over its first 32 columns), dP
+// 64-127 (dS over its first 32 columns for KV), accumulators from 128.
+// All hand-offs are mbarriers; every wait is bounded.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kRowsB = 128;    // stationary rows per CTA
+constexpr int kColsB = 64;     // rows of a stream tile
+constexpr int kThreadsB = 192;
+constexpr int kProdWarpB = 4;
+constexpr int kMmaWarpB = 5;
+constexpr uint32_t kColSB = 0, kColDpB = 64, kColAccB = 128;
+
+struct BwdBf16Params {
+    CUtensorMap tm_x, tm_y;     // stationary: KV: K, V; else Q, dout   (box rows 128)
+    CUtensorMap tm_xs, tm_ys;   // stream:     KV: Q, dout; else K, V   (box rows 64)
+    const float *lse;           // [B*H][Lq] natural log
+    const float *delta;         // [B*H][Lq]
+    const int32_t *kv_lengths;  // null unless the kv-length mask is on
+    __nv_bfloat16 *g1;          // KV: dK; else dQ     [B*H][rows][D]
+    __nv_bfloat16 *g2;          // KV: dV; else unused
+    int B, H, Lq, Lk;
+    int causal;
+    float scale, scale_log2;
+};
+
+struct __align__(8) BwdBars {
+    uint64_t x_full;
+    uint64_t st_full[2], st_empty[2];
+    uint64_t s_full, p_full, acc_full, drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int D>
+struct BwdBf16Cfg {
+    static constexpr int NH = D / 64;                      // 64-column halves
+    static constexpr uint32_t kHalfX = kRowsB * 128;       // 16 KB
+    static constexpr uint32_t kHalfS = kColsB * 128;       // 8 KB
+    static constexpr uint32_t kTileX = NH * kHalfX;
+    static constexpr uint32_t kTileS = NH * kHalfS;
+    static constexpr uint32_t kX = 0, kY = kTileX;
+    static constexpr uint32_t kStage = 2 * kTileX;          // stage s: xs at kStage + s*2*kTileS
+    static constexpr uint32_t kStat = kStage + 4 * kTileS;  // per softmax warp: 64 lse2 + 64 Delta
+    static constexpr uint32_t kBars = kStat + 4 * 128 * 4;
+    static constexpr size_t kSmem = 1024 + kBars + sizeof(BwdBars);
+};
+
+// TMEM columns: S and dP (128), then one (dQ) or two (dV, dK) accumulators
+// of D columns; a power of two.
+template <int D, bool KV>
+constexpr uint32_t bwd_tmem_cols() {
+    return (128 + (KV ? 2 : 1) * D) <= 256 ? 256u : 512u;
+}
+
+// K-major descriptor of K-step kk (16 bf16 along the row) of a tile stored as
+// 64-column halves of `half` bytes in the 128-byte swizzled layout.
+__device__ __forceinline__ uint64_t desc_k(uint32_t tile, int kk, uint32_t half) {
+    return sdesc_sw128(tile + (kk >> 2) * half + (kk & 3) * 32, 16, 1024);
+}
+// MN-major descriptor of K-step kk (16 rows) of a [rows][D] tile used as the
+// B operand with N = D (64-column halves `half` bytes apart).
+__device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk, uint32_t half) {
+    return sdesc_sw128(tile + kk * 2048, half, 1024);
+}
+
+template <int D, bool KV>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    attn_bwd_bf16_kernel(const __grid_constant__ BwdBf16Params p) {
+    using C = BwdBf16Cfg<D>;
+    constexpr int NH = C::NH;
+    if (*reinterpret_cast<volatile unsigned int *>(&g_status) != 0u) return;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t *base = smem_raw + pad;
+    BwdBars *bars = reinterpret_cast<BwdBars *>(base + C::kBars);
+    volatile int *abort = &bars->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // This CTA's stationary tile and the stream tiles it visits.
+    const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int bh = b * p.H + h;
+    const int r0 = tile * kRowsB;
+    int len = p.Lk;
+    if (p.kv_lengths) len = max(0, min((int)p.kv_lengths[b], p.Lk));
+    int j0, j1;   // stream tiles [j0, j1)
+    if (KV) {
+        // Query tiles that see a key of [r0, r0 + 128): none past the length;
+        // under the causal rule only queries >= r0.
+        j0 = p.causal ? r0 / kColsB : 0;
+        j1 = r0 < len ? (p.Lq + kColsB - 1) / kColsB : j0;
+    } else {
+        int kend = len;
+        if (p.causal) kend = min(kend, r0 + kRowsB);
+        j0 = 0;
+        j1 = (kend + kColsB - 1) / kColsB;
+    }
+    const int n = max(0, j1 - j0);
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->x_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->st_full[s], 1);
+            mbar_init(&bars->st_empty[s], 1);
+        }
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->p_full, 4);   // one arrival per softmax warp
+        mbar_init(&bars->acc_full, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        mbar_fence_init();
+    }
+    constexpr uint32_t kTmemCols = bwd_tmem_cols<D, KV>();
+    if (warp == kMmaWarpB) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    auto wwait = [&](uint64_t *bar, uint32_t parity, uint32_t site) -> bool {
+        const bool r = mbar_wait(bar, parity, site, abort);
+        return __all_sync(0xffffffffu, r);
+    };
+
+    if (warp == kProdWarpB) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0 && n > 0) {
+            bool ok = true;
+            mbar_arrive_expect_tx(&bars->x_full, 2 * C::kTileX);
+            for (int hh = 0; hh < NH; ++hh) {
+                tma_load_3d(base + C::kX + hh * C::kHalfX, &p.tm_x, &bars->x_full, hh * 64, r0, bh);
+                tma_load_3d(base + C::kY + hh * C::kHalfX, &p.tm_y, &bars->x_full, hh * 64, r0, bh);
+            }
+            int issued = 0;
+            for (int j = 0; ok && j < n; ++j) {
+                const int s = j & 1;
+                if (j >= 2) ok = mbar_wait(&bars->st_empty[s], ((j >> 1) - 1) & 1, kSiteKvEmpty, abort);
+                if (!ok) break;
+                uint8_t *st = base + C::kStage + s * 2 * C::kTileS;
+                const int c0 = (j0 + j) * kColsB;
+                mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::kTileS);
+                for (int hh = 0; hh < NH; ++hh) {
+                    tma_load_3d(st + hh * C::kHalfS, &p.tm_xs, &bars->st_full[s], hh * 64, c0, bh);
+                    tma_load_3d(st + C::kTileS + hh * C::kHalfS, &p.tm_ys, &bars->st_full[s], hh * 64, c0,
+                                bh);
+                }
+                issued = j + 1;
+            }
+            // Loads already issued must land before shared memory is released.
+            volatile int no_abort = 0;
+            mbar_wait(&bars->x_full, 0, kSiteDrain, &no_abort);
+            for (int j = max(0, issued - 2); j < issued; ++j)
+                mbar_wait(&bars->st_full[j & 1], (j >> 1) & 1, kSiteDrain, &no_abort);
+        }
+    } else if (warp == kMmaWarpB) {
+        // ------------------------------- MMA issuer -------------------------------
+        constexpr uint32_t idS = idesc_bf16_f32(128, kColsB, 0, 0);   // both operands K-major
+        constexpr uint32_t idAcc = idesc_bf16_f32(128, D, 0, 1);      // A from TMEM, B MN-major
+        bool ok = n > 0, issued = false;
+        if (ok) ok = wwait(&bars->x_full, 0, kSiteQFull);
+        const uint32_t sx = smem_u32(base + C::kX), sy = smem_u32(base + C::kY);
+        for (int j = 0; ok && j < n; ++j) {
+            const int s = j & 1;
+            ok = wwait(&bars->st_full[s], (j >> 1) & 1, kSiteKFull);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t sxs = smem_u32(base + C::kStage + s * 2 * C::kTileS);
+            const uint32_t sys = sxs + C::kTileS;
+            // S = X Xs^T and dP = Y Ys^T, 128 x 64 each (K = D).
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                if (elect_one())
+                    umma_ss(tmem + kColSB, desc_k(sx, kk, C::kHalfX), desc_k(sxs, kk, C::kHalfS), idS,
+                            kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                if (elect_one())
+                    umma_ss(tmem + kColDpB, desc_k(sy, kk, C::kHalfX), desc_k(sys, kk, C::kHalfS), idS,
+                            kk > 0);
+            if (elect_one()) umma_commit(&bars->s_full);
+            __syncwarp();
+            issued = true;
+            ok = wwait(&bars->p_full, j & 1, kSitePFull);
+            if (!ok) break;
+            tc_fence_after();
+            // Accumulating products over the tile's 64 rows (4 K-steps of 16;
+            // P / dS as packed bf16 pairs, 8 TMEM columns per K-step).
+            if (KV) {
+#pragma unroll
+                for (int kk = 0; kk < kColsB / 16; ++kk)
+                    if (elect_one())   // dV += P^T dout
+                        umma_ts(tmem + kColAccB, tmem + kColSB + kk * 8, desc_mn(sys, kk, C::kHalfS), idAcc,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < kColsB / 16; ++kk)
+                    if (elect_one())   // dK += dS^T Q
+                        umma_ts(tmem + kColAccB + D, tmem + kColDpB + kk * 8, desc_mn(sxs, kk, C::kHalfS),
+                                idAcc, (j > 0 || kk > 0) ? 1u : 0u);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < kColsB / 16; ++kk)
+                    if (elect_one())   // dQ += dS K
+                        umma_ts(tmem + kColAccB, tmem + kColSB + kk * 8, desc_mn(sxs, kk, C::kHalfS), idAcc,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (elect_one()) {
+                umma_commit(&bars->st_empty[s]);
+                if (j == n - 1) umma_commit(&bars->acc_full);
+            }
+            __syncwarp();
+        }
+        if (issued) {
+            volatile int no_abort = 0;
+            if (elect_one()) umma_commit(&bars->drain);
+            __syncwarp();
+            mbar_wait(&bars->drain, 0, kSiteDrain, &no_abort);
+            __syncwarp();
+        }
+    } else {
+        // --------------------------------- softmax --------------------------------
+        const int t = threadIdx.x;   // stationary row within the tile = TMEM lane
+        const int row = r0 + t;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const float *lse_bh = p.lse + (size_t)bh * p.Lq;
+        const float *dl_bh = p.delta + (size_t)bh * p.Lq;
+        constexpr float kLog2e = 1.4426950408889634f;
+        // dQ kernel: the row's own statistics.
+        float lse2_row = 0.f, dl_row = 0.f;
+        if (!KV && row < p.Lq) {
+            lse2_row = lse_bh[row] * kLog2e;
+            dl_row = dl_bh[row];
+        }
+        // KV: this warp's copy of the 64 query columns' statistics.
+        float *stw = reinterpret_cast<float *>(base + C::kStat) + warp * 128;
+        bool ok = true;
+        for (int j = 0; ok && j < n; ++j) {
+            const int c0 = (j0 + j) * kColsB;
+            if (KV) {
+                __syncwarp();   // every lane is done with the previous tile's copy
+                for (int c = lane; c < kColsB; c += 32) {
+                    const int qc = c0 + c;
+                    stw[c] = qc < p.Lq ? lse_bh[qc] * kLog2e : 0.f;
+                    stw[kColsB + c] = qc < p.Lq ? dl_bh[qc] : 0.f;
+                }
+                __syncwarp();
+            }
+            ok = wwait(&bars->s_full, j & 1, kSiteSFull);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t pk[kColsB / 2], dk[kColsB / 2];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_off + kColSB + half * 32, sr);
+                tmem_ld32(tmem + lane_off + kColDpB + half * 32, dr);
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int cc = half * 32 + c + u;
+                        bool vis;
+                        float l2, dl;
+                        if (KV) {   // row = key, column = query
+                            const int qc = c0 + cc;
+                            vis = row < len && qc < p.Lq && (!p.causal || row <= qc);
+                            l2 = stw[cc];
+                            dl = stw[kColsB + cc];
+                        } else {    // row = query, column = key
+                            const int key = c0 + cc;
+                            vis = key < len && row < p.Lq && (!p.causal || key <= row);
+                            l2 = lse2_row;
+                            dl = dl_row;
+                        }
+                        const float pr =
+                            vis ? ex2_approx(fmaf(__uint_as_float(sr[c + u]), p.scale_log2, -l2)) : 0.f;
+                        pv[u] = pr;
+                        dv[u] = pr * (__uint_as_float(dr[c + u]) - dl);
+                    }
+                    pk[(half * 32 + c) >> 1] = pack_bf16x2(pv[0], pv[1]);
+                    dk[(half * 32 + c) >> 1] = pack_bf16x2(dv[0], dv[1]);
+                }
+            }
+            if (KV) {
+                tmem_st32(tmem + lane_off + kColSB, pk);    // P^T over S
+                tmem_st32(tmem + lane_off + kColDpB, dk);   // dS^T over dP
+            } else {
+                tmem_st32(tmem + lane_off + kColSB, dk);    // dS over S
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full);
+        }
+        // Epilogue: the accumulators (scaled) as bf16, one row per thread.  The
+        // wait and the TMEM loads are warp-collective, so every lane runs them;
+        // only the stores depend on the row.
+        const int rows_valid = KV ? p.Lk : p.Lq;
+        bool have = false;
+        if (ok && n > 0) {
+            have = wwait(&bars->acc_full, 0, kSitePvDone);   // warp-uniform
+            if (have) tc_fence_after();
+        }
+        if (ok && (n == 0 || have)) {
+            const bool store = row < rows_valid;
+#pragma unroll
+            for (int gi = 0; gi < (KV ? 2 : 1); ++gi) {
+                // KV: gi 0 = dV (accumulator at 128), gi 1 = dK (at 128 + D,
+                // scaled); else dQ (scaled).
+                __nv_bfloat16 *dst = (KV && gi == 0 ? p.g2 : p.g1) +
+                                     ((size_t)bh * rows_valid + (store ? row : 0)) * D;
+                const float sc = (KV && gi == 0) ? 1.f : p.scale;
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t a[32];
+                    if (have) {
+                        tmem_ld32(tmem + lane_off + kColAccB + (KV && gi == 1 ? D : 0) + ch * 32, a);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) a[e] = 0u;
+                    }
+                    if (store) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(a[e]) * sc, __uint_as_float(a[e + 1]) * sc);
+                            w.y = pack_bf16x2(__uint_as_float(a[e + 2]) * sc, __uint_as_float(a[e + 3]) * sc);
+                            w.z = pack_bf16x2(__uint_as_float(a[e + 4]) * sc, __uint_as_float(a[e + 5]) * sc);
+                            w.w = pack_bf16x2(__uint_as_float(a[e + 6]) * sc, __uint_as_float(a[e + 7]) * sc);
+                            *reinterpret_cast<uint4 *>(dst + ch * 32 + e) = w;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarpB) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D, bool KV>
+cudaError_t launch_bwd_bf16_tc(const BwdBf16Params &p, int grid_x, cudaStream_t stream) {
+    // Shared memory requested so that the CTAs resident on one SM never ask
+    // for more than its 512 TMEM columns together (an allocation would
+    // otherwise wait for another CTA to finish): 512 / columns per CTA.
+    constexpr uint32_t per_sm = 512u / bwd_tmem_cols<D, KV>();
+    constexpr size_t floor_smem = (228u * 1024u) / (per_sm + 1) + 1024u;
+    constexpr size_t smem = BwdBf16Cfg<D>::kSmem > floor_smem ? BwdBf16Cfg<D>::kSmem : floor_smem;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(attn_bwd_bf16_kernel<D, KV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const dim3 grid((unsigned)grid_x, (unsigned)p.H, (unsigned)p.B);
+    attn_bwd_bf16_kernel<D, KV><<<grid, kThreadsB, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16_tensor(const void *q, const void *k, const void *v, const void *dout,
+                                   const float *lse, const float *delta, const int32_t *kv_lengths,
+                                   void *dq, void *dk, void *dv, int B, int H, int Lq, int Lk, int D,
+                                   int mask_kind, float scale, cudaStream_t stream, int *driver_err) {
+    *driver_err = 0;
+    const uint64_t BH = (uint64_t)B * H;
+    BwdBf16Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.lse = lse;
+    p.delta = delta;
+    p.kv_lengths = (mask_kind & 2) ? kv_lengths : nullptr;
+    p.B = B;
+    p.H = H;
+    p.Lq = Lq;
+    p.Lk = Lk;
+    p.causal = (mask_kind & 1) ? 1 : 0;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaError_t e = cudaSuccess;
+    CUresult r = CUDA_SUCCESS;
+    // Key-stationary: dK, dV (every key row written, zeros where no query sees it).
+    if (Lk > 0) {
+        const bool has_q = Lq > 0;
+        r = encode_bf16_3d(&p.tm_x, k, D, Lk, BH, kRowsB);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_y, v, D, Lk, BH, kRowsB);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_xs, has_q ? q : k, D, has_q ? Lq : Lk, BH, kColsB);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_ys, has_q ? dout : v, D, has_q ? Lq : Lk, BH, kColsB);
+        if (r != CUDA_SUCCESS) {
+            *driver_err = (int)r;
+            return cudaErrorInvalidValue;
+        }
+        p.g1 = static_cast<__nv_bfloat16 *>(dk);
+        p.g2 = static_cast<__nv_bfloat16 *>(dv);
+        const int gx = (Lk + kRowsB - 1) / kRowsB;
+        e = D == 64 ? launch_bwd_bf16_tc<64, true>(p, gx, stream) : launch_bwd_bf16_tc<128, true>(p, gx, stream);
+        if (e != cudaSuccess) return e;
+    }
+    // Query-stationary: dQ.
+    if (Lq > 0) {
+        const bool has_k = Lk > 0;
+        r = encode_bf16_3d(&p.tm_x, q, D, Lq, BH, kRowsB);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_y, dout, D, Lq, BH, kRowsB);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_xs, has_k ? k : q, D, has_k ? Lk : Lq, BH, kColsB);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_ys, has_k ? v : dout, D, has_k ? Lk : Lq, BH, kColsB);
+        if (r != CUDA_SUCCESS) {
+            *driver_err = (int)r;
+            return cudaErrorInvalidValue;
+        }
+        p.g1 = static_cast<__nv_bfloat16 *>(dq);
+        p.g2 = nullptr;
+        const int gx = (Lq + kRowsB - 1) / kRowsB;
+        e = D == 64 ? launch_bwd_bf16_tc<64, false>(p, gx, stream) : launch_bwd_bf16_tc<128, false>(p, gx, stream);
+    }
+    return e;
+}
+
+}  // namespace mha

@@ -899,7 +899,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // box and the 128-byte swizzle; rows outside the array read as zero (loads)
 // or are not written (stores).
 CUresult encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
-                        uint64_t d2, uint32_t box_rows = 128) {
+                        uint64_t d2, uint32_t box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return CUDA_ERROR_NOT_SUPPORTED;
     const cuuint64_t dims[3] = {d0, d1, d2};
@@ -1020,15 +1020,15 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     const uint64_t BH = (uint64_t)c.B * c.H;
     CUresult r;
     if (prenorm)
-        r = encode_bf16_3d(&p.tm_q, c.x, (uint64_t)c.H * c.D, c.Lq, c.B);
+        r = encode_bf16_3d(&p.tm_q, c.x, (uint64_t)c.H * c.D, c.Lq, c.B, 128);
     else
-        r = encode_bf16_3d(&p.tm_q, c.q, c.D, c.Lq, BH);
+        r = encode_bf16_3d(&p.tm_q, c.q, c.D, c.Lq, BH, 128);
     if (r == CUDA_SUCCESS) {
         // With no keys the K/V maps are never used; point them at a valid array.
         const bool has_k = c.Lk > 0;
-        r = encode_bf16_3d(&p.tm_k, has_k ? c.k : c.out, c.D, has_k ? c.Lk : 1, has_k ? BH : 1);
+        r = encode_bf16_3d(&p.tm_k, has_k ? c.k : c.out, c.D, has_k ? c.Lk : 1, has_k ? BH : 1, 128);
         if (r == CUDA_SUCCESS)
-            r = encode_bf16_3d(&p.tm_v, has_k ? c.v : c.out, c.D, has_k ? c.Lk : 1, has_k ? BH : 1);
+            r = encode_bf16_3d(&p.tm_v, has_k ? c.v : c.out, c.D, has_k ? c.Lk : 1, has_k ? BH : 1, 128);
     }
     if (r == CUDA_SUCCESS) {
         if (prenorm)
@@ -1080,11 +1080,11 @@ cudaError_t launch_selftest_umma(int variant, int kn, const void *a, const void 
     std::memset(&p, 0, sizeof(p));
     CUresult r = CUDA_SUCCESS;
     if (variant == 0) {
-        r = encode_bf16_3d(&p.tm_a, a, kn, 128, 1);
-        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_b, b, kn, 128, 1);
+        r = encode_bf16_3d(&p.tm_a, a, kn, 128, 1, 128);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_b, b, kn, 128, 1, 128);
     } else {
-        if (variant == 1) r = encode_bf16_3d(&p.tm_a, a, 128, 128, 1);
-        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_b, b, kn, 128, 1);
+        if (variant == 1) r = encode_bf16_3d(&p.tm_a, a, 128, 128, 1, 128);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_b, b, kn, 128, 1, 128);
     }
     if (r != CUDA_SUCCESS) {
         *driver_err = (int)r;

@@ -46,6 +46,21 @@ cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const
                            const float *dout, const float *lse, const int32_t *kv_lengths,
                            float *dq, float *dk, float *dv, float *delta, int B, int H, int Lq,
                            int Lk, int D, int mask_kind, float scale, cudaStream_t stream);
+// bf16 backward on the tensor cores (bwd_bf16.cu): dK, dV by a key-stationary
+// kernel and dQ by a query-stationary one, from the forward's log-sum-exp and
+// Delta (B*H*Lq floats each).  Every gradient element written once.
+cudaError_t launch_bwd_bf16_tensor(const void *q, const void *k, const void *v, const void *dout,
+                                   const float *lse, const float *delta, const int32_t *kv_lengths,
+                                   void *dq, void *dk, void *dv, int B, int H, int Lq, int Lk, int D,
+                                   int mask_kind, float scale, cudaStream_t stream, int *driver_err);
+// The row pass alone (Delta = dout . o), for the tensor-core backward.
+cudaError_t launch_bwd_row_delta_bf16(const void *o, const void *dout, float *delta, int64_t rows,
+                                      int D, cudaStream_t stream);
+// 3-D bf16 tensor map over a dense [d2][d1][d0] array, {64, box_rows, 1} box,
+// 128-byte swizzle (fwd_bf16.cu).
+CUresult encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
+                        uint64_t d2, uint32_t box_rows);
+
 cudaError_t launch_bwd_bf16(const void *q, const void *k, const void *v, const void *o,
                             const void *dout, const float *lse, const int32_t *kv_lengths,
                             void *dq, void *dk, void *dv, float *dq_acc, float *delta, int B,

@@ -85,6 +85,11 @@ WORKLOADS = {
     "b3_causal_f32_bwd": Workload(
         "b3_causal_f32_bwd", "mha_bwd", "f32", B=2, H=16, Lq=1024, Lk=1024, D=128,
         mask=MASK_CAUSAL, note="backward of causal self-attention, fp32, D=128; dout iid N(0,1)"),
+    "b5_causal_bf16_bwd": Workload(
+        "b5_causal_bf16_bwd", "mha_bwd", "bf16", B=1, H=32, Lq=2048, Lk=2048, D=128,
+        mask=MASK_CAUSAL, qk_std=math.sqrt(2.5),
+        note="backward of the c3 causal bf16 workload (fp32 arithmetic, bf16 gradients); "
+             "dout iid N(0,1)"),
 }
 
 

@@ -180,9 +180,17 @@ def check_grad_bf16(got, want, what):
     return float(err.max() / s), float(err.mean() / s)
 
 
+@pytest.fixture
+def bwd_kernel(request):
+    mha.set_bwd_kernel(request.param)
+    yield request.param
+    mha.set_bwd_kernel(0)
+
+
 @pytest.mark.gpu
+@pytest.mark.parametrize("bwd_kernel", [0, 1], indirect=True, ids=["tensor", "cudacore"])
 @pytest.mark.parametrize("case", BF16_CASES, ids=lambda c: "B%dH%dLq%dLk%dD%dm%d" % c[:6])
-def test_backward_parity_bf16(case):
+def test_backward_parity_bf16(case, bwd_kernel):
     B, H, Lq, Lk, D, mask, lens = case
     q = randn((B, H, Lq, D), 121, 1.0, torch.bfloat16)
     k = randn((B, H, Lk, D), 122, 1.0, torch.bfloat16)
@@ -203,6 +211,59 @@ def test_backward_parity_bf16(case):
     wq, wk, wv = oracle.mha_bwd(qn, kn, vn, gn, mask, lens)
     r = [check_grad_bf16(as_np(t), w, "%s %s" % (n, case))
          for n, t, w in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv))]
-    print(case, "relative max/mean: dq %.1e/%.1e dk %.1e/%.1e dv %.1e/%.1e" % (
+    print(case, bwd_kernel, "relative max/mean: dq %.1e/%.1e dk %.1e/%.1e dv %.1e/%.1e" % (
         r[0] + r[1] + r[2]))
+    assert mha.device_status() == 0
+
+
+@pytest.mark.gpu
+def test_backward_bf16_tensor_deterministic_and_hidden_keys():
+    """The tensor-core bf16 backward writes every element once: two runs are
+    bit-identical, keys past the length get exactly zero dk and dv, and
+    changing their values changes no gradient bit of the visible keys."""
+    B, H, Lq, Lk, D = 2, 2, 200, 300, 128
+    lens = [130, 300]
+    q = randn((B, H, Lq, D), 141, 1.0, torch.bfloat16)
+    k = randn((B, H, Lk, D), 142, 1.0, torch.bfloat16)
+    v = randn((B, H, Lk, D), 143, 1.0, torch.bfloat16)
+    g = randn((B, H, Lq, D), 144, 1.0, torch.bfloat16)
+    lt = dev(lens_tensor(lens))
+
+    def run(kk, vv):
+        out, lse = mha.mha_fwd_lse(dev(q), dev(kk), dev(vv), 3, lt)
+        return mha.mha_bwd(dev(q), dev(kk), dev(vv), out, dev(g), lse, 3, lt)
+
+    a = run(k, v)
+    b = run(k, v)
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(a, b))
+    assert torch.count_nonzero(a[1][0, :, 130:]) == 0 and torch.count_nonzero(a[2][0, :, 130:]) == 0
+    k2, v2 = k.clone(), v.clone()
+    k2[0, :, 130:] = randn((H, Lk - 130, D), 145, 20.0, torch.bfloat16)
+    v2[0, :, 130:] = randn((H, Lk - 130, D), 146, 20.0, torch.bfloat16)
+    c = run(k2, v2)
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(a, c))
+    assert mha.device_status() == 0
+
+
+@pytest.mark.gpu
+def test_backward_bf16_workload_sampled_heads():
+    """The bf16 backward workload of the benchmark (B1 H32 L2048 D128 causal):
+    every gradient element of three heads (first, middle, last) against the
+    oracle run on those heads alone (heads are independent problems)."""
+    w = synthetic.WORKLOADS["b5_causal_bf16_bwd"]
+    x = synthetic.make(w, seed=0)
+    out, lse = mha.mha_fwd_lse(dev(x["q"]), dev(x["k"]), dev(x["v"]), w.mask, None, scale=w.scale)
+    dq, dk, dv = mha.mha_bwd(dev(x["q"]), dev(x["k"]), dev(x["v"]), out, dev(x["dout"]), lse,
+                             w.mask, None, scale=w.scale)
+    torch.cuda.synchronize()
+    for h in (0, w.H // 2, w.H - 1):
+        sl = lambda t: t[:, h:h + 1].float().numpy()
+        wq, wk, wv = oracle.mha_bwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["dout"]), w.mask,
+                                    None, w.scale)
+        r = [check_grad_bf16(as_np(t[:, h:h + 1]), ww, "%s head %d" % (n, h))
+             for n, t, ww in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv))]
+        print(w.name, "head", h, "relative max/mean: dq %.1e/%.1e dk %.1e/%.1e dv %.1e/%.1e" % (
+            r[0] + r[1] + r[2]))
     assert mha.device_status() == 0

@@ -39,6 +39,11 @@ def test_backward_accounting():
     assert bench.kernel_of(w) == "mha_bwd_f32_kernel"
     small = synthetic.small(kind="mha_bwd", Lq=64, Lk=64)
     assert bench.kernel_of(small) == "mha_bwd_f32_kernel"
+    b5 = synthetic.WORKLOADS["b5_causal_bf16_bwd"]
+    assert bench.kernel_of(b5) == "attn_bwd_bf16_kernel"
+    r = bench.roofline_for(b5, None, 1.0, {"bf16_tflops": 2000.0, "hbm_gbs": 7000.0,
+                                           "_source": "test"}, 152)
+    assert r["bound"] == "tensor" and r["peak"] == 2000.0   # bf16 backward: tensor cores
 
 
 def test_kernel_choice_and_tf32_roofline():
