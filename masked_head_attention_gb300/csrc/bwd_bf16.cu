@@ -23,8 +23,11 @@
 // S(j) and dP(j), waits for the softmax's P / dS, then the accumulating
 // products, which read the stage and the P / dS columns before S(j + 1)
 // overwrites them (the tensor pipe executes one thread's MMAs in order).
-// TMEM: S 0-63 (P / dS packed bf16 pairs over its first 32 columns), dP
-// 64-127 (dS over its first 32 columns for KV), accumulators from 128.
+// TMEM: per S/dP buffer (two for D = 128, one for D = 64) S in its first 64
+// columns (P / dS packed bf16 pairs over the first 32 of them) and dP in the
+// next 64 (dS over its first 32 for KV); the accumulators after the buffers.
+// With two buffers S(j + 1) and dP(j + 1) are issued before the products of
+// tile j, so the softmax of a tile overlaps the products of its neighbours.
 // All hand-offs are mbarriers; every wait is bounded.
 #include <cstdint>
 #include <cstring>
@@ -45,7 +48,8 @@ constexpr int kColsB = 64;     // rows of a stream tile
 constexpr int kThreadsB = 192;
 constexpr int kProdWarpB = 4;
 constexpr int kMmaWarpB = 5;
-constexpr uint32_t kColSB = 0, kColDpB = 64, kColAccB = 128;
+// TMEM per S/dP buffer: S in columns [0, 64), dP in [64, 128) of the buffer.
+constexpr uint32_t kColDpOff = 64;
 
 struct BwdBf16Params {
     CUtensorMap tm_x, tm_y;     // stationary: KV: K, V; else Q, dout   (box rows 128)
@@ -63,7 +67,7 @@ struct BwdBf16Params {
 struct __align__(8) BwdBars {
     uint64_t x_full;
     uint64_t st_full[2], st_empty[2];
-    uint64_t s_full, p_full, acc_full, drain;
+    uint64_t s_full[2], p_full[2], acc_full, drain;   // s_full, p_full: per S/dP buffer
     uint32_t tmem_base;
     int abort;
 };
@@ -77,16 +81,24 @@ struct BwdBf16Cfg {
     static constexpr uint32_t kTileS = NH * kHalfS;
     static constexpr uint32_t kX = 0, kY = kTileX;
     static constexpr uint32_t kStage = 2 * kTileX;          // stage s: xs at kStage + s*2*kTileS
-    static constexpr uint32_t kStat = kStage + 4 * kTileS;  // per softmax warp: 64 lse2 + 64 Delta
-    static constexpr uint32_t kBars = kStat + 4 * 128 * 4;
+    // Per softmax warp, two slots of 64 (lse2, Delta) pairs (the current and
+    // the next stream tile's query columns).
+    static constexpr uint32_t kStat = kStage + 4 * kTileS;
+    static constexpr uint32_t kBars = kStat + 4 * 2 * 64 * 8;
     static constexpr size_t kSmem = 1024 + kBars + sizeof(BwdBars);
 };
 
-// TMEM columns: S and dP (128), then one (dQ) or two (dV, dK) accumulators
-// of D columns; a power of two.
+// S/dP buffers in TMEM: two for D = 128 (the softmax of one stream tile
+// overlaps the products of the next), one for D = 64 (two CTAs share an SM).
+template <int D>
+constexpr int bwd_sdp_buffers() {
+    return D == 128 ? 2 : 1;
+}
+// TMEM columns: the S/dP buffers (128 each), then one (dQ) or two (dV, dK)
+// accumulators of D columns; a power of two.
 template <int D, bool KV>
 constexpr uint32_t bwd_tmem_cols() {
-    return (128 + (KV ? 2 : 1) * D) <= 256 ? 256u : 512u;
+    return (128 * bwd_sdp_buffers<D>() + (KV ? 2 : 1) * D) <= 256 ? 256u : 512u;
 }
 
 // K-major descriptor of K-step kk (16 bf16 along the row) of a tile stored as
@@ -114,9 +126,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     volatile int *abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // This CTA's stationary tile and the stream tiles it visits.
-    const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int bh = b * p.H + h;
+    // This CTA's stationary tile and the stream tiles it visits.  The grid is
+    // one-dimensional, heaviest tiles first: under the causal rule the first
+    // key tiles see the most queries, the last query tiles the most keys.
+    const int n_tiles = (int)(gridDim.x / (unsigned)(p.B * p.H));
+    const int tr = (int)blockIdx.x / (p.B * p.H);
+    const int bh = (int)blockIdx.x % (p.B * p.H);
+    const int tile = (KV || !p.causal) ? tr : n_tiles - 1 - tr;
+    const int b = bh / p.H;
     const int r0 = tile * kRowsB;
     int len = p.Lk;
     if (p.kv_lengths) len = max(0, min((int)p.kv_lengths[b], p.Lk));
@@ -140,8 +157,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             mbar_init(&bars->st_full[s], 1);
             mbar_init(&bars->st_empty[s], 1);
         }
-        mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->p_full, 4);   // one arrival per softmax warp
+        for (int bb = 0; bb < 2; ++bb) {
+            mbar_init(&bars->s_full[bb], 1);
+            mbar_init(&bars->p_full[bb], 4);   // one arrival per softmax warp
+        }
         mbar_init(&bars->acc_full, 1);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -196,58 +215,77 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         // ------------------------------- MMA issuer -------------------------------
         constexpr uint32_t idS = idesc_bf16_f32(128, kColsB, 0, 0);   // both operands K-major
         constexpr uint32_t idAcc = idesc_bf16_f32(128, D, 0, 1);      // A from TMEM, B MN-major
+        constexpr int NB = bwd_sdp_buffers<D>();
+        constexpr uint32_t kAcc = 128 * NB;                           // first accumulator column
         bool ok = n > 0, issued = false;
         if (ok) ok = wwait(&bars->x_full, 0, kSiteQFull);
         const uint32_t sx = smem_u32(base + C::kX), sy = smem_u32(base + C::kY);
-        for (int j = 0; ok && j < n; ++j) {
-            const int s = j & 1;
-            ok = wwait(&bars->st_full[s], (j >> 1) & 1, kSiteKFull);
-            if (!ok) break;
+        // S(j) = X Xs^T and dP(j) = Y Ys^T (128 x 64 each, K = D) into buffer j % NB.
+        auto issue_sdp = [&](int j) -> bool {
+            if (!wwait(&bars->st_full[j & 1], (j >> 1) & 1, kSiteKFull)) return false;
             tc_fence_after();
-            const uint32_t sxs = smem_u32(base + C::kStage + s * 2 * C::kTileS);
+            const uint32_t sxs = smem_u32(base + C::kStage + (j & 1) * 2 * C::kTileS);
             const uint32_t sys = sxs + C::kTileS;
-            // S = X Xs^T and dP = Y Ys^T, 128 x 64 each (K = D).
+            const uint32_t cs = (uint32_t)(j % NB) * 128;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 if (elect_one())
-                    umma_ss(tmem + kColSB, desc_k(sx, kk, C::kHalfX), desc_k(sxs, kk, C::kHalfS), idS,
-                            kk > 0);
+                    umma_ss(tmem + cs, desc_k(sx, kk, C::kHalfX), desc_k(sxs, kk, C::kHalfS), idS, kk > 0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 if (elect_one())
-                    umma_ss(tmem + kColDpB, desc_k(sy, kk, C::kHalfX), desc_k(sys, kk, C::kHalfS), idS,
+                    umma_ss(tmem + cs + kColDpOff, desc_k(sy, kk, C::kHalfX), desc_k(sys, kk, C::kHalfS), idS,
                             kk > 0);
-            if (elect_one()) umma_commit(&bars->s_full);
+            if (elect_one()) umma_commit(&bars->s_full[j % NB]);
             __syncwarp();
             issued = true;
-            ok = wwait(&bars->p_full, j & 1, kSitePFull);
-            if (!ok) break;
+            return true;
+        };
+        // Accumulating products of tile j over its 64 rows (4 K-steps of 16;
+        // P / dS as packed bf16 pairs, 8 TMEM columns per K-step), once the
+        // softmax has written them; then the stage is released.
+        auto issue_acc = [&](int j) -> bool {
+            if (!wwait(&bars->p_full[j % NB], (j / NB) & 1, kSitePFull)) return false;
             tc_fence_after();
-            // Accumulating products over the tile's 64 rows (4 K-steps of 16;
-            // P / dS as packed bf16 pairs, 8 TMEM columns per K-step).
+            const uint32_t sxs = smem_u32(base + C::kStage + (j & 1) * 2 * C::kTileS);
+            const uint32_t sys = sxs + C::kTileS;
+            const uint32_t cs = (uint32_t)(j % NB) * 128;
             if (KV) {
 #pragma unroll
                 for (int kk = 0; kk < kColsB / 16; ++kk)
                     if (elect_one())   // dV += P^T dout
-                        umma_ts(tmem + kColAccB, tmem + kColSB + kk * 8, desc_mn(sys, kk, C::kHalfS), idAcc,
+                        umma_ts(tmem + kAcc, tmem + cs + kk * 8, desc_mn(sys, kk, C::kHalfS), idAcc,
                                 (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < kColsB / 16; ++kk)
                     if (elect_one())   // dK += dS^T Q
-                        umma_ts(tmem + kColAccB + D, tmem + kColDpB + kk * 8, desc_mn(sxs, kk, C::kHalfS),
+                        umma_ts(tmem + kAcc + D, tmem + cs + kColDpOff + kk * 8, desc_mn(sxs, kk, C::kHalfS),
                                 idAcc, (j > 0 || kk > 0) ? 1u : 0u);
             } else {
 #pragma unroll
                 for (int kk = 0; kk < kColsB / 16; ++kk)
                     if (elect_one())   // dQ += dS K
-                        umma_ts(tmem + kColAccB, tmem + kColSB + kk * 8, desc_mn(sxs, kk, C::kHalfS), idAcc,
+                        umma_ts(tmem + kAcc, tmem + cs + kk * 8, desc_mn(sxs, kk, C::kHalfS), idAcc,
                                 (j > 0 || kk > 0) ? 1u : 0u);
             }
             if (elect_one()) {
-                umma_commit(&bars->st_empty[s]);
+                umma_commit(&bars->st_empty[j & 1]);
                 if (j == n - 1) umma_commit(&bars->acc_full);
             }
             __syncwarp();
+            return true;
+        };
+        // Two buffers: S/dP(j + 1) goes out before the products of tile j (the
+        // buffer it overwrites was read by the products of tile j - 1, issued
+        // earlier).  One buffer: strictly alternating.
+        if (ok && NB == 2) ok = issue_sdp(0);
+        for (int j = 0; ok && j < n; ++j) {
+            if (NB == 2) {
+                if (j + 1 < n) ok = issue_sdp(j + 1);
+            } else {
+                ok = issue_sdp(j);
+            }
+            if (ok) ok = issue_acc(j);
         }
         if (issued) {
             volatile int no_abort = 0;
@@ -270,29 +308,43 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             lse2_row = lse_bh[row] * kLog2e;
             dl_row = dl_bh[row];
         }
-        // KV: this warp's copy of the 64 query columns' statistics.
-        float *stw = reinterpret_cast<float *>(base + C::kStat) + warp * 128;
+        // KV: this warp's copies of the query columns' (lse2, Delta) pairs, two
+        // slots: the next tile's are fetched while the current one is used.
+        float2 *stw = reinterpret_cast<float2 *>(base + C::kStat) + warp * 2 * kColsB;
+        auto fetch_stats = [&](int jj, float2 (&v)[kColsB / 32]) {
+            const int cb = (j0 + jj) * kColsB;
+#pragma unroll
+            for (int u = 0; u < kColsB / 32; ++u) {
+                const int qc = cb + lane + 32 * u;
+                v[u] = qc < p.Lq ? make_float2(lse_bh[qc] * kLog2e, dl_bh[qc]) : make_float2(0.f, 0.f);
+            }
+        };
+        float2 nxt[kColsB / 32];
+        if (KV && n > 0) fetch_stats(0, nxt);
         bool ok = true;
         for (int j = 0; ok && j < n; ++j) {
             const int c0 = (j0 + j) * kColsB;
+            float2 *cur = stw + (j & 1) * kColsB;
             if (KV) {
-                __syncwarp();   // every lane is done with the previous tile's copy
-                for (int c = lane; c < kColsB; c += 32) {
-                    const int qc = c0 + c;
-                    stw[c] = qc < p.Lq ? lse_bh[qc] * kLog2e : 0.f;
-                    stw[kColsB + c] = qc < p.Lq ? dl_bh[qc] : 0.f;
-                }
+                // Slot j & 1 was last read for tile j - 2, before this warp's
+                // tile j - 1 work; the lanes are converged here.
                 __syncwarp();
+#pragma unroll
+                for (int u = 0; u < kColsB / 32; ++u) cur[lane + 32 * u] = nxt[u];
+                __syncwarp();
+                if (j + 1 < n) fetch_stats(j + 1, nxt);   // in flight during this tile
             }
-            ok = wwait(&bars->s_full, j & 1, kSiteSFull);
+            constexpr int NB = bwd_sdp_buffers<D>();
+            const uint32_t cs = (uint32_t)(j % NB) * 128;   // this tile's S/dP buffer
+            ok = wwait(&bars->s_full[j % NB], (j / NB) & 1, kSiteSFull);
             if (!ok) break;
             tc_fence_after();
             uint32_t pk[kColsB / 2], dk[kColsB / 2];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + kColSB + half * 32, sr);
-                tmem_ld32(tmem + lane_off + kColDpB + half * 32, dr);
+                tmem_ld32(tmem + lane_off + cs + half * 32, sr);
+                tmem_ld32(tmem + lane_off + cs + kColDpOff + half * 32, dr);
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
                     float pv[2], dv[2];
@@ -304,8 +356,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                         if (KV) {   // row = key, column = query
                             const int qc = c0 + cc;
                             vis = row < len && qc < p.Lq && (!p.causal || row <= qc);
-                            l2 = stw[cc];
-                            dl = stw[kColsB + cc];
+                            const float2 st = cur[cc];
+                            l2 = st.x;
+                            dl = st.y;
                         } else {    // row = query, column = key
                             const int key = c0 + cc;
                             vis = key < len && row < p.Lq && (!p.causal || key <= row);
@@ -322,15 +375,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 }
             }
             if (KV) {
-                tmem_st32(tmem + lane_off + kColSB, pk);    // P^T over S
-                tmem_st32(tmem + lane_off + kColDpB, dk);   // dS^T over dP
+                tmem_st32(tmem + lane_off + cs, pk);               // P^T over S
+                tmem_st32(tmem + lane_off + cs + kColDpOff, dk);   // dS^T over dP
             } else {
-                tmem_st32(tmem + lane_off + kColSB, dk);    // dS over S
+                tmem_st32(tmem + lane_off + cs, dk);               // dS over S
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full);
+            if (lane == 0) mbar_arrive(&bars->p_full[j % NB]);
         }
         // Epilogue: the accumulators (scaled) as bf16, one row per thread.  The
         // wait and the TMEM loads are warp-collective, so every lane runs them;
@@ -354,7 +407,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t a[32];
                     if (have) {
-                        tmem_ld32(tmem + lane_off + kColAccB + (KV && gi == 1 ? D : 0) + ch * 32, a);
+                        tmem_ld32(tmem + lane_off + 128 * bwd_sdp_buffers<D>() + (KV && gi == 1 ? D : 0) +
+                                      ch * 32, a);
                     } else {
 #pragma unroll
                         for (int e = 0; e < 32; ++e) a[e] = 0u;
@@ -398,8 +452,11 @@ cudaError_t launch_bwd_bf16_tc(const BwdBf16Params &p, int grid_x, cudaStream_t 
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const dim3 grid((unsigned)grid_x, (unsigned)p.H, (unsigned)p.B);
-    attn_bwd_bf16_kernel<D, KV><<<grid, kThreadsB, smem, stream>>>(p);
+    // One-dimensional grid: tiles x (b, h); the kernel orders the tiles.
+    const uint64_t blocks = (uint64_t)grid_x * (uint64_t)p.B * (uint64_t)p.H;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+    attn_bwd_bf16_kernel<D, KV><<<(unsigned)blocks, kThreadsB, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
