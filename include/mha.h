@@ -8,7 +8,8 @@
  *     O[b,h,i,:] = sum_j softmax_j(s over visible j) * V[b,h,j,:]
  * with the softmax taken after subtracting the running row maximum (online
  * softmax), masked keys contributing exactly zero, and a row with no visible
- * key returning zeros.  Sources, cited by page title and section:
+ * key returning zeros.  mha_fwd_lse also returns each row's log-sum-exp, and
+ * mha_bwd the gradients dq, dk, dv of sum(dout * O) from it.  Sources, cited by page title and section:
  *  - "How to fuse cross-attention and layer-norm into a single CUDA kernel?"
  *    (cms365.cn), knowledge points: S = QK^T -> P = softmax(S) -> O = PV;
  *    answer steps two to five: Pre-LayerNorm on the query rows and the
