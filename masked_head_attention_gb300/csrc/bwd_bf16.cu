@@ -339,6 +339,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             ok = wwait(&bars->s_full[j % NB], (j / NB) & 1, kSiteSFull);
             if (!ok) break;
             tc_fence_after();
+            // A tile every position of which is visible (inside the length, the
+            // query range and the causal triangle) skips the element test.
+            const bool interior =
+                KV ? (r0 + kRowsB <= len && c0 + kColsB <= p.Lq && (!p.causal || r0 + kRowsB - 1 <= c0))
+                   : (c0 + kColsB <= len && r0 + kRowsB <= p.Lq && (!p.causal || c0 + kColsB - 1 <= r0));
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
             uint32_t pk[kColsB / 2], dk[kColsB / 2];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -347,31 +353,39 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 tmem_ld32(tmem + lane_off + cs + kColDpOff + half * 32, dr);
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int cc = half * 32 + c + u;
-                        bool vis;
-                        float l2, dl;
-                        if (KV) {   // row = key, column = query
-                            const int qc = c0 + cc;
-                            vis = row < len && qc < p.Lq && (!p.causal || row <= qc);
-                            const float2 st = cur[cc];
-                            l2 = st.x;
-                            dl = st.y;
-                        } else {    // row = query, column = key
-                            const int key = c0 + cc;
-                            vis = key < len && row < p.Lq && (!p.causal || key <= row);
-                            l2 = lse2_row;
-                            dl = dl_row;
-                        }
-                        const float pr =
-                            vis ? ex2_approx(fmaf(__uint_as_float(sr[c + u]), p.scale_log2, -l2)) : 0.f;
-                        pv[u] = pr;
-                        dv[u] = pr * (__uint_as_float(dr[c + u]) - dl);
+                    const int cc = half * 32 + c;
+                    // Statistics of the two columns (KV: per query column; else the row's).
+                    float2 nl2, ndl;
+                    if (KV) {
+                        const float4 st = *reinterpret_cast<const float4 *>(cur + cc);   // (l2, dl) x 2
+                        nl2 = make_float2(-st.x, -st.z);
+                        ndl = make_float2(-st.y, -st.w);
+                    } else {
+                        nl2 = make_float2(-lse2_row, -lse2_row);
+                        ndl = make_float2(-dl_row, -dl_row);
                     }
-                    pk[(half * 32 + c) >> 1] = pack_bf16x2(pv[0], pv[1]);
-                    dk[(half * 32 + c) >> 1] = pack_bf16x2(dv[0], dv[1]);
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                                sc2, nl2);
+                    float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    if (!interior) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            bool vis;
+                            if (KV) {   // row = key, column = query
+                                const int qc = c0 + cc + u;
+                                vis = row < len && qc < p.Lq && (!p.causal || row <= qc);
+                            } else {    // row = query, column = key
+                                const int key = c0 + cc + u;
+                                vis = key < len && row < p.Lq && (!p.causal || key <= row);
+                            }
+                            if (!vis) (u == 0 ? pr.x : pr.y) = 0.f;
+                        }
+                    }
+                    const float2 dd =
+                        __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), ndl);
+                    const float2 ds = __fmul2_rn(pr, dd);
+                    pk[cc >> 1] = pack_bf16x2(pr.x, pr.y);
+                    dk[cc >> 1] = pack_bf16x2(ds.x, ds.y);
                 }
             }
             if (KV) {
