@@ -19,7 +19,7 @@
 //
 // CTA = 6 warps: warps 0-3 softmax (thread t owns row t, TMEM lane t),
 // warp 4 TMA producer, warp 5 MMA issuer and TMEM owner.  Stream tiles go
-// through two shared-memory stages.  Per stream tile j the MMA warp issues
+// through four shared-memory stages.  Per stream tile j the MMA warp issues
 // S(j) and dP(j), waits for the softmax's P / dS, then the accumulating
 // products, which read the stage and the P / dS columns before S(j + 1)
 // overwrites them (the tensor pipe executes one thread's MMAs in order).
@@ -48,6 +48,7 @@ constexpr int kColsB = 64;     // rows of a stream tile
 constexpr int kThreadsB = 192;
 constexpr int kProdWarpB = 4;
 constexpr int kMmaWarpB = 5;
+constexpr int kStagesB = 4;    // stream-tile stages (TMA runs up to three tiles ahead)
 // TMEM per S/dP buffer: S in columns [0, 64), dP in [64, 128) of the buffer.
 constexpr uint32_t kColDpOff = 64;
 
@@ -66,7 +67,7 @@ struct BwdBf16Params {
 
 struct __align__(8) BwdBars {
     uint64_t x_full;
-    uint64_t st_full[2], st_empty[2];
+    uint64_t st_full[kStagesB], st_empty[kStagesB];
     uint64_t s_full[2], p_full[2], acc_full, drain;   // s_full, p_full: per S/dP buffer
     uint32_t tmem_base;
     int abort;
@@ -80,10 +81,10 @@ struct BwdBf16Cfg {
     static constexpr uint32_t kTileX = NH * kHalfX;
     static constexpr uint32_t kTileS = NH * kHalfS;
     static constexpr uint32_t kX = 0, kY = kTileX;
-    static constexpr uint32_t kStage = 2 * kTileX;          // stage s: xs at kStage + s*2*kTileS
+    static constexpr uint32_t kStage = 2 * kTileX;          // stage s: xs at kStage + s*2*kTileS, ys after it
     // Per softmax warp, two slots of 64 (lse2, Delta) pairs (the current and
     // the next stream tile's query columns).
-    static constexpr uint32_t kStat = kStage + 4 * kTileS;
+    static constexpr uint32_t kStat = kStage + 2 * kStagesB * kTileS;
     static constexpr uint32_t kBars = kStat + 4 * 2 * 64 * 8;
     static constexpr size_t kSmem = 1024 + kBars + sizeof(BwdBars);
 };
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->x_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kStagesB; ++s) {
             mbar_init(&bars->st_full[s], 1);
             mbar_init(&bars->st_empty[s], 1);
         }
@@ -192,10 +193,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             }
             int issued = 0;
             for (int j = 0; ok && j < n; ++j) {
-                const int s = j & 1;
-                if (j >= 2) ok = mbar_wait(&bars->st_empty[s], ((j >> 1) - 1) & 1, kSiteKvEmpty, abort);
+                const int s = j % kStagesB;
+                if (j >= kStagesB)
+                    ok = mbar_wait(&bars->st_empty[s], ((j / kStagesB) - 1) & 1, kSiteKvEmpty, abort);
                 if (!ok) break;
-                uint8_t *st = base + C::kStage + s * 2 * C::kTileS;
+                uint8_t *st = base + C::kStage + s * 2 * C::kTileS;   // s = j % kStagesB
                 const int c0 = (j0 + j) * kColsB;
                 mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::kTileS);
                 for (int hh = 0; hh < NH; ++hh) {
@@ -208,8 +210,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             // Loads already issued must land before shared memory is released.
             volatile int no_abort = 0;
             mbar_wait(&bars->x_full, 0, kSiteDrain, &no_abort);
-            for (int j = max(0, issued - 2); j < issued; ++j)
-                mbar_wait(&bars->st_full[j & 1], (j >> 1) & 1, kSiteDrain, &no_abort);
+            for (int j = max(0, issued - kStagesB); j < issued; ++j)
+                mbar_wait(&bars->st_full[j % kStagesB], (j / kStagesB) & 1, kSiteDrain, &no_abort);
         }
     } else if (warp == kMmaWarpB) {
         // ------------------------------- MMA issuer -------------------------------
@@ -222,9 +224,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const uint32_t sx = smem_u32(base + C::kX), sy = smem_u32(base + C::kY);
         // S(j) = X Xs^T and dP(j) = Y Ys^T (128 x 64 each, K = D) into buffer j % NB.
         auto issue_sdp = [&](int j) -> bool {
-            if (!wwait(&bars->st_full[j & 1], (j >> 1) & 1, kSiteKFull)) return false;
+            if (!wwait(&bars->st_full[j % kStagesB], (j / kStagesB) & 1, kSiteKFull)) return false;
             tc_fence_after();
-            const uint32_t sxs = smem_u32(base + C::kStage + (j & 1) * 2 * C::kTileS);
+            const uint32_t sxs = smem_u32(base + C::kStage + (j % kStagesB) * 2 * C::kTileS);
             const uint32_t sys = sxs + C::kTileS;
             const uint32_t cs = (uint32_t)(j % NB) * 128;
 #pragma unroll
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         auto issue_acc = [&](int j) -> bool {
             if (!wwait(&bars->p_full[j % NB], (j / NB) & 1, kSitePFull)) return false;
             tc_fence_after();
-            const uint32_t sxs = smem_u32(base + C::kStage + (j & 1) * 2 * C::kTileS);
+            const uint32_t sxs = smem_u32(base + C::kStage + (j % kStagesB) * 2 * C::kTileS);
             const uint32_t sys = sxs + C::kTileS;
             const uint32_t cs = (uint32_t)(j % NB) * 128;
             if (KV) {
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                 (j > 0 || kk > 0) ? 1u : 0u);
             }
             if (elect_one()) {
-                umma_commit(&bars->st_empty[j & 1]);
+                umma_commit(&bars->st_empty[j % kStagesB]);
                 if (j == n - 1) umma_commit(&bars->acc_full);
             }
             __syncwarp();
