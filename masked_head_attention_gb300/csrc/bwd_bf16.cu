@@ -14,6 +14,10 @@
 //              dV += P^T dout, dK += dS^T Q  (dK scaled at the end).
 //   KV = false (query-stationary): rows = queries, stream key tiles.
 //              S = Q K^T, dP = dout V^T; dS into TMEM; dQ += dS K.
+//              Q and dout sit in TMEM as the A operands of S and dP, so
+//              those products read only the 64-row K / V tiles from shared
+//              memory (with both operands in shared memory a 128 x 64 x 16
+//              product is bound by the shared-memory port, not the math).
 // No atomics: every gradient element is written once, the same on every run.
 // The price is forming S and dP twice (seven products instead of five).
 //
@@ -25,12 +29,14 @@
 // overwrites them (the tensor pipe executes one thread's MMAs in order).
 // TMEM: per S/dP buffer (two for D = 128, one for D = 64) S in its first 64
 // columns (P / dS packed bf16 pairs over the first 32 of them) and dP in the
-// next 64 (dS over its first 32 for KV); the accumulators after the buffers.
+// next 64 (dS over its first 32 for KV); the accumulators after the buffers,
+// then (query-stationary) Q and dout.
 // With two buffers S(j + 1) and dP(j + 1) are issued before the products of
 // tile j, so the softmax of a tile overlaps the products of its neighbours.
 // All hand-offs are mbarriers; every wait is bounded.
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -48,7 +54,10 @@ constexpr int kColsB = 64;     // rows of a stream tile
 constexpr int kThreadsB = 192;
 constexpr int kProdWarpB = 4;
 constexpr int kMmaWarpB = 5;
-constexpr int kStagesB = 4;    // stream-tile stages (TMA runs up to three tiles ahead)
+// Stream-tile stages (TMA runs up to three tiles ahead; a stage is released
+// when the accumulating products of its tile have finished).  More stages
+// (five, seven) measured no faster.
+constexpr int kStagesB = 4;
 // TMEM per S/dP buffer: S in columns [0, 64), dP in [64, 128) of the buffer.
 constexpr uint32_t kColDpOff = 64;
 
@@ -58,6 +67,7 @@ struct BwdBf16Params {
     const float *lse;           // [B*H][Lq] natural log
     const float *delta;         // [B*H][Lq]
     const int32_t *kv_lengths;  // null unless the kv-length mask is on
+    const __nv_bfloat16 *xa, *ya;   // query-stationary: Q and dout rows [B*H][Lq][D] (TMEM operands)
     __nv_bfloat16 *g1;          // KV: dK; else dQ     [B*H][rows][D]
     __nv_bfloat16 *g2;          // KV: dV; else unused
     int B, H, Lq, Lk;
@@ -66,26 +76,29 @@ struct BwdBf16Params {
 };
 
 struct __align__(8) BwdBars {
-    uint64_t x_full;
+    uint64_t x_full, xa_full;   // stationary tile in shared memory (KV) / in TMEM (else)
     uint64_t st_full[kStagesB], st_empty[kStagesB];
     uint64_t s_full[2], p_full[2], acc_full, drain;   // s_full, p_full: per S/dP buffer
     uint32_t tmem_base;
     int abort;
 };
 
-template <int D>
+template <int D, bool KV>
 struct BwdBf16Cfg {
     static constexpr int NH = D / 64;                      // 64-column halves
     static constexpr uint32_t kHalfX = kRowsB * 128;       // 16 KB
     static constexpr uint32_t kHalfS = kColsB * 128;       // 8 KB
     static constexpr uint32_t kTileX = NH * kHalfX;
     static constexpr uint32_t kTileS = NH * kHalfS;
+    // The key-stationary kernel keeps K and V in shared memory (the S and dP
+    // products read both operands from there); the query-stationary kernel
+    // keeps Q and dout in TMEM and needs no stationary tile here.
     static constexpr uint32_t kX = 0, kY = kTileX;
-    static constexpr uint32_t kStage = 2 * kTileX;          // stage s: xs at kStage + s*2*kTileS, ys after it
-    // Per softmax warp, two slots of 64 (lse2, Delta) pairs (the current and
-    // the next stream tile's query columns).
+    static constexpr uint32_t kStage = KV ? 2 * kTileX : 0;  // stage s: xs at kStage + s*2*kTileS, ys after it
+    // KV: per softmax warp, two slots of 64 (lse2, Delta) pairs (the current
+    // and the next stream tile's query columns).
     static constexpr uint32_t kStat = kStage + 2 * kStagesB * kTileS;
-    static constexpr uint32_t kBars = kStat + 4 * 2 * 64 * 8;
+    static constexpr uint32_t kBars = kStat + (KV ? 4 * 2 * 64 * 8 : 0);
     static constexpr size_t kSmem = 1024 + kBars + sizeof(BwdBars);
 };
 
@@ -95,11 +108,13 @@ template <int D>
 constexpr int bwd_sdp_buffers() {
     return D == 128 ? 2 : 1;
 }
-// TMEM columns: the S/dP buffers (128 each), then one (dQ) or two (dV, dK)
-// accumulators of D columns; a power of two.
+// TMEM columns: the S/dP buffers (128 each), then the accumulators: dV, dK
+// (D columns each) for KV; else dQ (D columns) followed by Q and dout as MMA
+// A operands (D / 2 columns each, bf16 pairs).  2D after the buffers either
+// way; a power of two.
 template <int D, bool KV>
 constexpr uint32_t bwd_tmem_cols() {
-    return (128 * bwd_sdp_buffers<D>() + (KV ? 2 : 1) * D) <= 256 ? 256u : 512u;
+    return (128 * bwd_sdp_buffers<D>() + 2 * D) <= 256 ? 256u : 512u;
 }
 
 // K-major descriptor of K-step kk (16 bf16 along the row) of a tile stored as
@@ -116,8 +131,9 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk, uint32_t half
 template <int D, bool KV>
 __global__ void __launch_bounds__(kThreadsB, 1)
     attn_bwd_bf16_kernel(const __grid_constant__ BwdBf16Params p) {
-    using C = BwdBf16Cfg<D>;
+    using C = BwdBf16Cfg<D, KV>;
     constexpr int NH = C::NH;
+    constexpr int NS = kStagesB;
     if (*reinterpret_cast<volatile unsigned int *>(&g_status) != 0u) return;
 
     extern __shared__ uint8_t smem_raw[];
@@ -154,7 +170,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->x_full, 1);
-        for (int s = 0; s < kStagesB; ++s) {
+        mbar_init(&bars->xa_full, 4);   // one arrival per softmax warp
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&bars->st_full[s], 1);
             mbar_init(&bars->st_empty[s], 1);
         }
@@ -186,18 +203,20 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0 && n > 0) {
             bool ok = true;
-            mbar_arrive_expect_tx(&bars->x_full, 2 * C::kTileX);
-            for (int hh = 0; hh < NH; ++hh) {
-                tma_load_3d(base + C::kX + hh * C::kHalfX, &p.tm_x, &bars->x_full, hh * 64, r0, bh);
-                tma_load_3d(base + C::kY + hh * C::kHalfX, &p.tm_y, &bars->x_full, hh * 64, r0, bh);
+            if (KV) {
+                mbar_arrive_expect_tx(&bars->x_full, 2 * C::kTileX);
+                for (int hh = 0; hh < NH; ++hh) {
+                    tma_load_3d(base + C::kX + hh * C::kHalfX, &p.tm_x, &bars->x_full, hh * 64, r0, bh);
+                    tma_load_3d(base + C::kY + hh * C::kHalfX, &p.tm_y, &bars->x_full, hh * 64, r0, bh);
+                }
             }
             int issued = 0;
             for (int j = 0; ok && j < n; ++j) {
-                const int s = j % kStagesB;
-                if (j >= kStagesB)
-                    ok = mbar_wait(&bars->st_empty[s], ((j / kStagesB) - 1) & 1, kSiteKvEmpty, abort);
+                const int s = j % NS;
+                if (j >= NS)
+                    ok = mbar_wait(&bars->st_empty[s], ((j / NS) - 1) & 1, kSiteKvEmpty, abort);
                 if (!ok) break;
-                uint8_t *st = base + C::kStage + s * 2 * C::kTileS;   // s = j % kStagesB
+                uint8_t *st = base + C::kStage + s * 2 * C::kTileS;   // s = j % NS
                 const int c0 = (j0 + j) * kColsB;
                 mbar_arrive_expect_tx(&bars->st_full[s], 2 * C::kTileS);
                 for (int hh = 0; hh < NH; ++hh) {
@@ -209,9 +228,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             }
             // Loads already issued must land before shared memory is released.
             volatile int no_abort = 0;
-            mbar_wait(&bars->x_full, 0, kSiteDrain, &no_abort);
-            for (int j = max(0, issued - kStagesB); j < issued; ++j)
-                mbar_wait(&bars->st_full[j % kStagesB], (j / kStagesB) & 1, kSiteDrain, &no_abort);
+            if (KV) mbar_wait(&bars->x_full, 0, kSiteDrain, &no_abort);
+            for (int j = max(0, issued - NS); j < issued; ++j)
+                mbar_wait(&bars->st_full[j % NS], (j / NS) & 1, kSiteDrain, &no_abort);
         }
     } else if (warp == kMmaWarpB) {
         // ------------------------------- MMA issuer -------------------------------
@@ -219,37 +238,45 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         constexpr uint32_t idAcc = idesc_bf16_f32(128, D, 0, 1);      // A from TMEM, B MN-major
         constexpr int NB = bwd_sdp_buffers<D>();
         constexpr uint32_t kAcc = 128 * NB;                           // first accumulator column
+        constexpr uint32_t kXa = kAcc + D, kYa = kXa + D / 2;         // query-stationary: Q, dout
         bool ok = n > 0, issued = false;
-        if (ok) ok = wwait(&bars->x_full, 0, kSiteQFull);
+        if (ok) ok = KV ? wwait(&bars->x_full, 0, kSiteQFull) : wwait(&bars->xa_full, 0, kSiteQFull);
         const uint32_t sx = smem_u32(base + C::kX), sy = smem_u32(base + C::kY);
-        // S(j) = X Xs^T and dP(j) = Y Ys^T (128 x 64 each, K = D) into buffer j % NB.
-        auto issue_sdp = [&](int j) -> bool {
-            if (!wwait(&bars->st_full[j % kStagesB], (j / kStagesB) & 1, kSiteKFull)) return false;
-            tc_fence_after();
-            const uint32_t sxs = smem_u32(base + C::kStage + (j % kStagesB) * 2 * C::kTileS);
+        // S(j) = X Xs^T and dP(j) = Y Ys^T (128 x 64 each, K = D) into buffer
+        // j % NB; the caller has waited for stage j.
+        auto issue_sdp = [&](int j) {
+            const uint32_t sxs = smem_u32(base + C::kStage + (j % NS) * 2 * C::kTileS);
             const uint32_t sys = sxs + C::kTileS;
             const uint32_t cs = (uint32_t)(j % NB) * 128;
+            if (KV) {   // K and V from shared memory
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                if (elect_one())
-                    umma_ss(tmem + cs, desc_k(sx, kk, C::kHalfX), desc_k(sxs, kk, C::kHalfS), idS, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    if (elect_one())
+                        umma_ss(tmem + cs, desc_k(sx, kk, C::kHalfX), desc_k(sxs, kk, C::kHalfS), idS, kk > 0);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                if (elect_one())
-                    umma_ss(tmem + cs + kColDpOff, desc_k(sy, kk, C::kHalfX), desc_k(sys, kk, C::kHalfS), idS,
-                            kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    if (elect_one())
+                        umma_ss(tmem + cs + kColDpOff, desc_k(sy, kk, C::kHalfX), desc_k(sys, kk, C::kHalfS),
+                                idS, kk > 0);
+            } else {    // Q and dout from TMEM (8 columns per K-step of 16)
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    if (elect_one()) umma_ts(tmem + cs, tmem + kXa + kk * 8, desc_k(sxs, kk, C::kHalfS), idS, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    if (elect_one())
+                        umma_ts(tmem + cs + kColDpOff, tmem + kYa + kk * 8, desc_k(sys, kk, C::kHalfS), idS,
+                                kk > 0);
+            }
             if (elect_one()) umma_commit(&bars->s_full[j % NB]);
             __syncwarp();
             issued = true;
-            return true;
         };
         // Accumulating products of tile j over its 64 rows (4 K-steps of 16;
-        // P / dS as packed bf16 pairs, 8 TMEM columns per K-step), once the
-        // softmax has written them; then the stage is released.
-        auto issue_acc = [&](int j) -> bool {
-            if (!wwait(&bars->p_full[j % NB], (j / NB) & 1, kSitePFull)) return false;
-            tc_fence_after();
-            const uint32_t sxs = smem_u32(base + C::kStage + (j % kStagesB) * 2 * C::kTileS);
+        // P / dS as packed bf16 pairs, 8 TMEM columns per K-step); the caller
+        // has waited for the softmax.  Then the stage is released.
+        auto issue_acc = [&](int j) {
+            const uint32_t sxs = smem_u32(base + C::kStage + (j % NS) * 2 * C::kTileS);
             const uint32_t sys = sxs + C::kTileS;
             const uint32_t cs = (uint32_t)(j % NB) * 128;
             if (KV) {
@@ -271,23 +298,34 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                 (j > 0 || kk > 0) ? 1u : 0u);
             }
             if (elect_one()) {
-                umma_commit(&bars->st_empty[j % kStagesB]);
+                umma_commit(&bars->st_empty[j % NS]);
                 if (j == n - 1) umma_commit(&bars->acc_full);
             }
             __syncwarp();
-            return true;
         };
-        // Two buffers: S/dP(j + 1) goes out before the products of tile j (the
-        // buffer it overwrites was read by the products of tile j - 1, issued
-        // earlier).  One buffer: strictly alternating.
-        if (ok && NB == 2) ok = issue_sdp(0);
-        for (int j = 0; ok && j < n; ++j) {
-            if (NB == 2) {
-                if (j + 1 < n) ok = issue_sdp(j + 1);
-            } else {
-                ok = issue_sdp(j);
+        // Tensor-pipe order: S/dP(0) (and S/dP(1) with two buffers), then per
+        // tile j its products followed by S/dP(j + NB), which overwrites the
+        // buffer those products read just before it (one thread's MMAs execute
+        // in order).  With two buffers the softmax of tile j + 1 overlaps the
+        // products of j and S/dP(j + 2).  Both waits of a tile come before its
+        // issues: a wait placed right after a commit returns only once the
+        // committed products have finished, which would leave the pipe idle
+        // while this warp waits.
+        for (int j = 0; ok && j < NB && j < n; ++j) {
+            ok = wwait(&bars->st_full[j % NS], (j / NS) & 1, kSiteKFull);
+            if (ok) {
+                tc_fence_after();
+                issue_sdp(j);
             }
-            if (ok) ok = issue_acc(j);
+        }
+        for (int j = 0; ok && j < n; ++j) {
+            const int jn = j + NB;
+            ok = wwait(&bars->p_full[j % NB], (j / NB) & 1, kSitePFull);
+            if (ok && jn < n) ok = wwait(&bars->st_full[jn % NS], (jn / NS) & 1, kSiteKFull);
+            if (!ok) break;
+            tc_fence_after();
+            issue_acc(j);
+            if (jn < n) issue_sdp(jn);
         }
         if (issued) {
             volatile int no_abort = 0;
@@ -312,6 +350,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
         // KV: this warp's copies of the query columns' (lse2, Delta) pairs, two
         // slots: the next tile's are fetched while the current one is used.
+        // (One copy shared by the four warps needs a barrier per tile, which
+        // measured slower.)
         float2 *stw = reinterpret_cast<float2 *>(base + C::kStat) + warp * 2 * kColsB;
         auto fetch_stats = [&](int jj, float2 (&v)[kColsB / 32]) {
             const int cb = (j0 + jj) * kColsB;
@@ -321,6 +361,40 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 v[u] = qc < p.Lq ? make_float2(lse_bh[qc] * kLog2e, dl_bh[qc]) : make_float2(0.f, 0.f);
             }
         };
+        // Query-stationary: the row's Q and dout into TMEM (bf16 pairs, the
+        // A-operand layout of the S and dP products; zeros past Lq).
+        if (!KV && n > 0) {
+            constexpr uint32_t kXa = 128 * bwd_sdp_buffers<D>() + D;
+            const bool have_row = row < p.Lq;
+            const size_t off = ((size_t)bh * p.Lq + (have_row ? row : 0)) * D;
+            // Every load is issued before the first store (one memory round trip).
+            uint32_t w[2][D / 2];
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const uint4 *src = reinterpret_cast<const uint4 *>((g == 0 ? p.xa : p.ya) + off);
+#pragma unroll
+                for (int u = 0; u < D / 8; ++u) {
+                    const uint4 v = have_row ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+                    w[g][4 * u] = v.x;
+                    w[g][4 * u + 1] = v.y;
+                    w[g][4 * u + 2] = v.z;
+                    w[g][4 * u + 3] = v.w;
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const uint32_t dst = tmem + lane_off + kXa + g * (D / 2);
+                if constexpr (D == 128) {
+                    tmem_st64(dst, *reinterpret_cast<uint32_t(*)[64]>(w[g]));
+                } else {
+                    tmem_st32(dst, *reinterpret_cast<uint32_t(*)[32]>(w[g]));
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->xa_full);
+        }
         float2 nxt[kColsB / 32];
         if (KV && n > 0) fetch_stats(0, nxt);
         bool ok = true;
@@ -347,55 +421,68 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 KV ? (r0 + kRowsB <= len && c0 + kColsB <= p.Lq && (!p.causal || r0 + kRowsB - 1 <= c0))
                    : (c0 + kColsB <= len && r0 + kRowsB <= p.Lq && (!p.causal || c0 + kColsB - 1 <= r0));
             const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-            uint32_t pk[kColsB / 2], dk[kColsB / 2];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + cs + half * 32, sr);
-                tmem_ld32(tmem + lane_off + cs + kColDpOff + half * 32, dr);
-#pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const int cc = half * 32 + c;
-                    // Statistics of the two columns (KV: per query column; else the row's).
-                    float2 nl2, ndl;
-                    if (KV) {
-                        const float4 st = *reinterpret_cast<const float4 *>(cur + cc);   // (l2, dl) x 2
-                        nl2 = make_float2(-st.x, -st.z);
-                        ndl = make_float2(-st.y, -st.w);
-                    } else {
-                        nl2 = make_float2(-lse2_row, -lse2_row);
-                        ndl = make_float2(-dl_row, -dl_row);
-                    }
-                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
-                                                sc2, nl2);
-                    float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    if (!interior) {
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            bool vis;
-                            if (KV) {   // row = key, column = query
-                                const int qc = c0 + cc + u;
-                                vis = row < len && qc < p.Lq && (!p.causal || row <= qc);
-                            } else {    // row = query, column = key
-                                const int key = c0 + cc + u;
-                                vis = key < len && row < p.Lq && (!p.causal || key <= row);
-                            }
-                            if (!vis) (u == 0 ? pr.x : pr.y) = 0.f;
-                        }
-                    }
-                    const float2 dd =
-                        __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), ndl);
-                    const float2 ds = __fmul2_rn(pr, dd);
-                    pk[cc >> 1] = pack_bf16x2(pr.x, pr.y);
-                    dk[cc >> 1] = pack_bf16x2(ds.x, ds.y);
-                }
-            }
+            // The visible columns of this row form one range [vlo, vhi) relative
+            // to the tile: KV (row = key): queries from the key on (causal) up to
+            // Lq, none for a key past the length; else (row = query): keys
+            // below the length and up to the query (causal), none past Lq.
+            int vlo, vhi;
             if (KV) {
-                tmem_st32(tmem + lane_off + cs, pk);               // P^T over S
-                tmem_st32(tmem + lane_off + cs + kColDpOff, dk);   // dS^T over dP
+                vlo = (p.causal ? row : 0) - c0;
+                vhi = row < len ? p.Lq - c0 : vlo;
             } else {
-                tmem_st32(tmem + lane_off + cs, dk);               // dS over S
+                vlo = -c0;
+                vhi = row < p.Lq ? (p.causal ? min(len, row + 1) : len) - c0 : vlo;
             }
+            // The element loop in two compiled forms, chosen by a warp-uniform
+            // test: without the visibility test (a straight line the compiler
+            // schedules across columns) and with it.  Half h covers columns
+            // [32h, 32h + 32) of S and dP; its P and dS (packed bf16 pairs) go to
+            // the first 32 columns of S and of dP, which were read at half 0.
+            auto tile_math = [&](auto masked_tag) {
+                constexpr bool kMasked = decltype(masked_tag)::value;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sr[32], dr[32], pk[16], dk[16];
+                    tmem_ld32_pair(tmem + lane_off + cs + half * 32, sr,
+                                   tmem + lane_off + cs + kColDpOff + half * 32, dr);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const int cc = half * 32 + c;
+                        // Statistics of the two columns (KV: per query column; else the row's).
+                        float2 nl2, ndl;
+                        if (KV) {
+                            const float4 st = *reinterpret_cast<const float4 *>(cur + cc);   // (l2, dl) x 2
+                            nl2 = make_float2(-st.x, -st.z);
+                            ndl = make_float2(-st.y, -st.w);
+                        } else {
+                            nl2 = make_float2(-lse2_row, -lse2_row);
+                            ndl = make_float2(-dl_row, -dl_row);
+                        }
+                        const float2 x =
+                            __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nl2);
+                        float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        if (kMasked) {
+                            pr.x = (cc >= vlo && cc < vhi) ? pr.x : 0.f;
+                            pr.y = (cc + 1 >= vlo && cc + 1 < vhi) ? pr.y : 0.f;
+                        }
+                        const float2 dd =
+                            __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), ndl);
+                        const float2 ds = __fmul2_rn(pr, dd);
+                        pk[c >> 1] = pack_bf16x2(pr.x, pr.y);
+                        dk[c >> 1] = pack_bf16x2(ds.x, ds.y);
+                    }
+                    if (KV) {
+                        tmem_st16(tmem + lane_off + cs + half * 16, pk);               // P^T over S
+                        tmem_st16(tmem + lane_off + cs + kColDpOff + half * 16, dk);   // dS^T over dP
+                    } else {
+                        tmem_st16(tmem + lane_off + cs + half * 16, dk);               // dS over S
+                    }
+                }
+            };
+            if (interior)
+                tile_math(std::false_type{});
+            else
+                tile_math(std::true_type{});
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -460,7 +547,8 @@ cudaError_t launch_bwd_bf16_tc(const BwdBf16Params &p, int grid_x, cudaStream_t 
     // otherwise wait for another CTA to finish): 512 / columns per CTA.
     constexpr uint32_t per_sm = 512u / bwd_tmem_cols<D, KV>();
     constexpr size_t floor_smem = (228u * 1024u) / (per_sm + 1) + 1024u;
-    constexpr size_t smem = BwdBf16Cfg<D>::kSmem > floor_smem ? BwdBf16Cfg<D>::kSmem : floor_smem;
+    constexpr size_t smem =
+        BwdBf16Cfg<D, KV>::kSmem > floor_smem ? BwdBf16Cfg<D, KV>::kSmem : floor_smem;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(attn_bwd_bf16_kernel<D, KV>,
@@ -518,9 +606,10 @@ cudaError_t launch_bwd_bf16_tensor(const void *q, const void *k, const void *v, 
     // Query-stationary: dQ.
     if (Lq > 0) {
         const bool has_k = Lk > 0;
-        r = encode_bf16_3d(&p.tm_x, q, D, Lq, BH, kRowsB);
-        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_y, dout, D, Lq, BH, kRowsB);
-        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_xs, has_k ? k : q, D, has_k ? Lk : Lq, BH, kColsB);
+        // Q and dout go to TMEM row by row (plain loads); K and V stream by TMA.
+        p.xa = static_cast<const __nv_bfloat16 *>(q);
+        p.ya = static_cast<const __nv_bfloat16 *>(dout);
+        r = encode_bf16_3d(&p.tm_xs, has_k ? k : q, D, has_k ? Lk : Lq, BH, kColsB);
         if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_ys, has_k ? v : dout, D, has_k ? Lk : Lq, BH, kColsB);
         if (r != CUDA_SUCCESS) {
             *driver_err = (int)r;
