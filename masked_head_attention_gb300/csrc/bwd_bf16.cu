@@ -21,15 +21,17 @@
 // No atomics: every gradient element is written once, the same on every run.
 // The price is forming S and dP twice (seven products instead of five).
 //
-// CTA = 6 warps: warps 0-3 softmax (thread t owns row t, TMEM lane t),
-// warp 4 TMA producer, warp 5 MMA issuer and TMEM owner.  Stream tiles go
-// through four shared-memory stages.  Per stream tile j the MMA warp issues
-// S(j) and dP(j), waits for the softmax's P / dS, then the accumulating
-// products, which read the stage and the P / dS columns before S(j + 1)
-// overwrites them (the tensor pipe executes one thread's MMAs in order).
+// CTA: the softmax warps (8 for D = 128: two per TMEM lane quadrant, each
+// taking one 32-column half of a stream tile; 4 for D = 64), then a TMA
+// producer warp and the MMA issuer / TMEM owner.  Stream tiles go through
+// four shared-memory stages.  Per stream tile j the MMA warp issues S(j) and
+// dP(j), waits for the softmax's P / dS, then the accumulating products,
+// which read the stage and the P / dS columns before S(j + 2) overwrites
+// them (the tensor pipe executes one thread's MMAs in order).
 // TMEM: per S/dP buffer (two for D = 128, one for D = 64) S in its first 64
-// columns (P / dS packed bf16 pairs over the first 32 of them) and dP in the
-// next 64 (dS over its first 32 for KV); the accumulators after the buffers,
+// columns and dP in the next 64; the packed bf16 pairs of P (KV) and dS
+// overwrite the first 16 columns of each 32-column half of S and dP (KV: P
+// over S, dS over dP; else dS over S).  The accumulators follow the buffers,
 // then (query-stationary) Q and dout.
 // With two buffers S(j + 1) and dP(j + 1) are issued before the products of
 // tile j, so the softmax of a tile overlaps the products of its neighbours.
@@ -51,9 +53,18 @@ namespace {
 
 constexpr int kRowsB = 128;    // stationary rows per CTA
 constexpr int kColsB = 64;     // rows of a stream tile
-constexpr int kThreadsB = 192;
-constexpr int kProdWarpB = 4;
-constexpr int kMmaWarpB = 5;
+// Softmax warps: two per TMEM lane quadrant for D = 128 (each takes one
+// 32-column half of a stream tile), one for D = 64 (both halves; two CTAs
+// share an SM, which 320 threads of this size would not).  Then the TMA
+// producer warp and the MMA warp.
+template <int D>
+constexpr int bwd_soft_warps() {
+    return D == 128 ? 8 : 4;
+}
+template <int D>
+constexpr int bwd_threads() {
+    return 32 * (bwd_soft_warps<D>() + 2);
+}
 // Stream-tile stages (TMA runs up to three tiles ahead; a stage is released
 // when the accumulating products of its tile have finished).  More stages
 // (five, seven) measured no faster.
@@ -98,7 +109,7 @@ struct BwdBf16Cfg {
     // KV: per softmax warp, two slots of 64 (lse2, Delta) pairs (the current
     // and the next stream tile's query columns).
     static constexpr uint32_t kStat = kStage + 2 * kStagesB * kTileS;
-    static constexpr uint32_t kBars = kStat + (KV ? 4 * 2 * 64 * 8 : 0);
+    static constexpr uint32_t kBars = kStat + (KV ? 4 * 2 * 64 * 8 : 0);   // SW warps x 2 x (256 / SW) pairs
     static constexpr size_t kSmem = 1024 + kBars + sizeof(BwdBars);
 };
 
@@ -129,11 +140,13 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk, uint32_t half
 }
 
 template <int D, bool KV>
-__global__ void __launch_bounds__(kThreadsB, 1)
+__global__ void __launch_bounds__(bwd_threads<D>(), 1)
     attn_bwd_bf16_kernel(const __grid_constant__ BwdBf16Params p) {
     using C = BwdBf16Cfg<D, KV>;
     constexpr int NH = C::NH;
     constexpr int NS = kStagesB;
+    constexpr int SW = bwd_soft_warps<D>();
+    constexpr int kProdWarpB = SW, kMmaWarpB = SW + 1;
     if (*reinterpret_cast<volatile unsigned int *>(&g_status) != 0u) return;
 
     extern __shared__ uint8_t smem_raw[];
@@ -170,14 +183,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->x_full, 1);
-        mbar_init(&bars->xa_full, 4);   // one arrival per softmax warp
+        mbar_init(&bars->xa_full, SW);   // one arrival per softmax warp
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bars->st_full[s], 1);
             mbar_init(&bars->st_empty[s], 1);
         }
         for (int bb = 0; bb < 2; ++bb) {
             mbar_init(&bars->s_full[bb], 1);
-            mbar_init(&bars->p_full[bb], 4);   // one arrival per softmax warp
+            mbar_init(&bars->p_full[bb], SW);   // one arrival per softmax warp
         }
         mbar_init(&bars->acc_full, 1);
         mbar_init(&bars->drain, 1);
@@ -243,7 +256,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         if (ok) ok = KV ? wwait(&bars->x_full, 0, kSiteQFull) : wwait(&bars->xa_full, 0, kSiteQFull);
         const uint32_t sx = smem_u32(base + C::kX), sy = smem_u32(base + C::kY);
         // S(j) = X Xs^T and dP(j) = Y Ys^T (128 x 64 each, K = D) into buffer
-        // j % NB; the caller has waited for stage j.
+        // j % NB; the caller has waited for stage j and commits s_full.
         auto issue_sdp = [&](int j) {
             const uint32_t sxs = smem_u32(base + C::kStage + (j % NS) * 2 * C::kTileS);
             const uint32_t sys = sxs + C::kTileS;
@@ -268,13 +281,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                         umma_ts(tmem + cs + kColDpOff, tmem + kYa + kk * 8, desc_k(sys, kk, C::kHalfS), idS,
                                 kk > 0);
             }
-            if (elect_one()) umma_commit(&bars->s_full[j % NB]);
-            __syncwarp();
             issued = true;
         };
+        auto commit_s = [&](int j) {
+            if (elect_one()) umma_commit(&bars->s_full[j % NB]);
+            __syncwarp();
+        };
         // Accumulating products of tile j over its 64 rows (4 K-steps of 16;
-        // P / dS as packed bf16 pairs, 8 TMEM columns per K-step); the caller
+        // P / dS as packed bf16 pairs, 8 TMEM columns per K-step, the pairs of
+        // each 32-row half at the start of that half's 32 columns); the caller
         // has waited for the softmax.  Then the stage is released.
+        auto pcol = [](int kk) -> uint32_t { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); };
         auto issue_acc = [&](int j) {
             const uint32_t sxs = smem_u32(base + C::kStage + (j % NS) * 2 * C::kTileS);
             const uint32_t sys = sxs + C::kTileS;
@@ -283,18 +300,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
                 for (int kk = 0; kk < kColsB / 16; ++kk)
                     if (elect_one())   // dV += P^T dout
-                        umma_ts(tmem + kAcc, tmem + cs + kk * 8, desc_mn(sys, kk, C::kHalfS), idAcc,
+                        umma_ts(tmem + kAcc, tmem + cs + pcol(kk), desc_mn(sys, kk, C::kHalfS), idAcc,
                                 (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < kColsB / 16; ++kk)
                     if (elect_one())   // dK += dS^T Q
-                        umma_ts(tmem + kAcc + D, tmem + cs + kColDpOff + kk * 8, desc_mn(sxs, kk, C::kHalfS),
+                        umma_ts(tmem + kAcc + D, tmem + cs + kColDpOff + pcol(kk), desc_mn(sxs, kk, C::kHalfS),
                                 idAcc, (j > 0 || kk > 0) ? 1u : 0u);
             } else {
 #pragma unroll
                 for (int kk = 0; kk < kColsB / 16; ++kk)
                     if (elect_one())   // dQ += dS K
-                        umma_ts(tmem + kAcc, tmem + cs + kk * 8, desc_mn(sxs, kk, C::kHalfS), idAcc,
+                        umma_ts(tmem + kAcc, tmem + cs + pcol(kk), desc_mn(sxs, kk, C::kHalfS), idAcc,
                                 (j > 0 || kk > 0) ? 1u : 0u);
             }
             if (elect_one()) {
@@ -307,15 +324,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         // tile j its products followed by S/dP(j + NB), which overwrites the
         // buffer those products read just before it (one thread's MMAs execute
         // in order).  With two buffers the softmax of tile j + 1 overlaps the
-        // products of j and S/dP(j + 2).  Both waits of a tile come before its
-        // issues: a wait placed right after a commit returns only once the
-        // committed products have finished, which would leave the pipe idle
-        // while this warp waits.
+        // products of j and S/dP(j + 2).
+        // A wait of this warp placed after a commit returns only once every
+        // product issued before that commit has finished, so the waits of a
+        // tile come before its issues.  (Holding the S/dP commit back past the
+        // next wait keeps the pipe busier but delays the softmax by this
+        // warp's reaction time; measured slower.)
         for (int j = 0; ok && j < NB && j < n; ++j) {
             ok = wwait(&bars->st_full[j % NS], (j / NS) & 1, kSiteKFull);
             if (ok) {
                 tc_fence_after();
                 issue_sdp(j);
+                commit_s(j);
             }
         }
         for (int j = 0; ok && j < n; ++j) {
@@ -325,7 +345,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             if (!ok) break;
             tc_fence_after();
             issue_acc(j);
-            if (jn < n) issue_sdp(jn);
+            if (jn < n) {
+                issue_sdp(jn);
+                commit_s(jn);
+            }
         }
         if (issued) {
             volatile int no_abort = 0;
@@ -336,9 +359,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
     } else {
         // --------------------------------- softmax --------------------------------
-        const int t = threadIdx.x;   // stationary row within the tile = TMEM lane
+        // Warp w owns TMEM lane quadrant w % 4 (rows 32 (w % 4) + lane) and,
+        // with two warps per quadrant, the 32-column half w / 4 of each tile.
+        constexpr int G = SW / 4;          // warps per quadrant
+        constexpr int HPW = 2 / G;         // 32-column halves per warp
+        const int gi = warp >> 2;          // this warp's group within the quadrant
+        const int h0 = gi * HPW;           // first half this warp handles
+        const int t = 32 * (warp & 3) + lane;   // stationary row within the tile = TMEM lane
         const int row = r0 + t;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         const float *lse_bh = p.lse + (size_t)bh * p.Lq;
         const float *dl_bh = p.delta + (size_t)bh * p.Lq;
         constexpr float kLog2e = 1.4426950408889634f;
@@ -348,30 +377,33 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             lse2_row = lse_bh[row] * kLog2e;
             dl_row = dl_bh[row];
         }
-        // KV: this warp's copies of the query columns' (lse2, Delta) pairs, two
-        // slots: the next tile's are fetched while the current one is used.
-        // (One copy shared by the four warps needs a barrier per tile, which
+        // KV: this warp's copies of its query columns' (lse2, Delta) pairs,
+        // two slots: the next tile's are fetched while the current one is
+        // used.  (One copy shared by all warps needs a barrier per tile, which
         // measured slower.)
-        float2 *stw = reinterpret_cast<float2 *>(base + C::kStat) + warp * 2 * kColsB;
-        auto fetch_stats = [&](int jj, float2 (&v)[kColsB / 32]) {
-            const int cb = (j0 + jj) * kColsB;
+        constexpr int kWCols = 32 * HPW;   // columns per warp
+        float2 *stw = reinterpret_cast<float2 *>(base + C::kStat) + warp * 2 * kWCols;
+        auto fetch_stats = [&](int jj, float2 (&v)[HPW]) {
+            const int cb = (j0 + jj) * kColsB + 32 * h0;
 #pragma unroll
-            for (int u = 0; u < kColsB / 32; ++u) {
+            for (int u = 0; u < HPW; ++u) {
                 const int qc = cb + lane + 32 * u;
                 v[u] = qc < p.Lq ? make_float2(lse_bh[qc] * kLog2e, dl_bh[qc]) : make_float2(0.f, 0.f);
             }
         };
         // Query-stationary: the row's Q and dout into TMEM (bf16 pairs, the
-        // A-operand layout of the S and dP products; zeros past Lq).
+        // A-operand layout of the S and dP products; zeros past Lq); with two
+        // warps per quadrant each writes one of the two.
         if (!KV && n > 0) {
             constexpr uint32_t kXa = 128 * bwd_sdp_buffers<D>() + D;
+            constexpr int NG = 2 / G;   // operands per warp
             const bool have_row = row < p.Lq;
             const size_t off = ((size_t)bh * p.Lq + (have_row ? row : 0)) * D;
             // Every load is issued before the first store (one memory round trip).
-            uint32_t w[2][D / 2];
+            uint32_t w[NG][D / 2];
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const uint4 *src = reinterpret_cast<const uint4 *>((g == 0 ? p.xa : p.ya) + off);
+            for (int g = 0; g < NG; ++g) {
+                const uint4 *src = reinterpret_cast<const uint4 *>((gi * NG + g == 0 ? p.xa : p.ya) + off);
 #pragma unroll
                 for (int u = 0; u < D / 8; ++u) {
                     const uint4 v = have_row ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
@@ -382,8 +414,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 }
             }
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const uint32_t dst = tmem + lane_off + kXa + g * (D / 2);
+            for (int g = 0; g < NG; ++g) {
+                const uint32_t dst = tmem + lane_off + kXa + (gi * NG + g) * (D / 2);
                 if constexpr (D == 128) {
                     tmem_st64(dst, *reinterpret_cast<uint32_t(*)[64]>(w[g]));
                 } else {
@@ -395,18 +427,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->xa_full);
         }
-        float2 nxt[kColsB / 32];
+        float2 nxt[HPW];
         if (KV && n > 0) fetch_stats(0, nxt);
         bool ok = true;
         for (int j = 0; ok && j < n; ++j) {
             const int c0 = (j0 + j) * kColsB;
-            float2 *cur = stw + (j & 1) * kColsB;
+            float2 *cur = stw + (j & 1) * kWCols;
             if (KV) {
                 // Slot j & 1 was last read for tile j - 2, before this warp's
                 // tile j - 1 work; the lanes are converged here.
                 __syncwarp();
 #pragma unroll
-                for (int u = 0; u < kColsB / 32; ++u) cur[lane + 32 * u] = nxt[u];
+                for (int u = 0; u < HPW; ++u) cur[lane + 32 * u] = nxt[u];
                 __syncwarp();
                 if (j + 1 < n) fetch_stats(j + 1, nxt);   // in flight during this tile
             }
@@ -437,21 +469,22 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             // test: without the visibility test (a straight line the compiler
             // schedules across columns) and with it.  Half h covers columns
             // [32h, 32h + 32) of S and dP; its P and dS (packed bf16 pairs) go to
-            // the first 32 columns of S and of dP, which were read at half 0.
+            // the first 16 of those columns of S and of dP, read by this warp.
             auto tile_math = [&](auto masked_tag) {
                 constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int hu = 0; hu < HPW; ++hu) {
+                    const int half = h0 + hu;
+                    const uint32_t hc = (uint32_t)(32 * half);
+                    const int lo = vlo - 32 * half, hi = vhi - 32 * half;   // relative to the half
                     uint32_t sr[32], dr[32], pk[16], dk[16];
-                    tmem_ld32_pair(tmem + lane_off + cs + half * 32, sr,
-                                   tmem + lane_off + cs + kColDpOff + half * 32, dr);
+                    tmem_ld32_pair(tmem + lane_off + cs + hc, sr, tmem + lane_off + cs + kColDpOff + hc, dr);
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
-                        const int cc = half * 32 + c;
                         // Statistics of the two columns (KV: per query column; else the row's).
                         float2 nl2, ndl;
                         if (KV) {
-                            const float4 st = *reinterpret_cast<const float4 *>(cur + cc);   // (l2, dl) x 2
+                            const float4 st = *reinterpret_cast<const float4 *>(cur + 32 * hu + c);   // (l2, dl) x 2
                             nl2 = make_float2(-st.x, -st.z);
                             ndl = make_float2(-st.y, -st.w);
                         } else {
@@ -462,8 +495,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                             __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nl2);
                         float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                         if (kMasked) {
-                            pr.x = (cc >= vlo && cc < vhi) ? pr.x : 0.f;
-                            pr.y = (cc + 1 >= vlo && cc + 1 < vhi) ? pr.y : 0.f;
+                            pr.x = (c >= lo && c < hi) ? pr.x : 0.f;
+                            pr.y = (c + 1 >= lo && c + 1 < hi) ? pr.y : 0.f;
                         }
                         const float2 dd =
                             __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), ndl);
@@ -472,10 +505,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                         dk[c >> 1] = pack_bf16x2(ds.x, ds.y);
                     }
                     if (KV) {
-                        tmem_st16(tmem + lane_off + cs + half * 16, pk);               // P^T over S
-                        tmem_st16(tmem + lane_off + cs + kColDpOff + half * 16, dk);   // dS^T over dP
+                        tmem_st16(tmem + lane_off + cs + hc, pk);               // P^T over S
+                        tmem_st16(tmem + lane_off + cs + kColDpOff + hc, dk);   // dS^T over dP
                     } else {
-                        tmem_st16(tmem + lane_off + cs + half * 16, dk);               // dS over S
+                        tmem_st16(tmem + lane_off + cs + hc, dk);               // dS over S
                     }
                 }
             };
@@ -488,9 +521,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->p_full[j % NB]);
         }
-        // Epilogue: the accumulators (scaled) as bf16, one row per thread.  The
-        // wait and the TMEM loads are warp-collective, so every lane runs them;
-        // only the stores depend on the row.
+        // Epilogue: the accumulators (scaled) as bf16, one row per thread (its
+        // share of the 32-column chunks).  The wait and the TMEM loads are
+        // warp-collective, so every lane runs them; only the stores depend on
+        // the row.
         const int rows_valid = KV ? p.Lk : p.Lq;
         bool have = false;
         if (ok && n > 0) {
@@ -499,18 +533,20 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
         if (ok && (n == 0 || have)) {
             const bool store = row < rows_valid;
+            constexpr int kChunks = (D / 32) / G;   // 32-column chunks per warp and accumulator
 #pragma unroll
-            for (int gi = 0; gi < (KV ? 2 : 1); ++gi) {
-                // KV: gi 0 = dV (accumulator at 128), gi 1 = dK (at 128 + D,
-                // scaled); else dQ (scaled).
-                __nv_bfloat16 *dst = (KV && gi == 0 ? p.g2 : p.g1) +
+            for (int ai = 0; ai < (KV ? 2 : 1); ++ai) {
+                // KV: ai 0 = dV (first accumulator), ai 1 = dK (after it, scaled);
+                // else dQ (scaled).
+                __nv_bfloat16 *dst = (KV && ai == 0 ? p.g2 : p.g1) +
                                      ((size_t)bh * rows_valid + (store ? row : 0)) * D;
-                const float sc = (KV && gi == 0) ? 1.f : p.scale;
+                const float sc = (KV && ai == 0) ? 1.f : p.scale;
 #pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
+                for (int cu = 0; cu < kChunks; ++cu) {
+                    const int ch = gi * kChunks + cu;
                     uint32_t a[32];
                     if (have) {
-                        tmem_ld32(tmem + lane_off + 128 * bwd_sdp_buffers<D>() + (KV && gi == 1 ? D : 0) +
+                        tmem_ld32(tmem + lane_off + 128 * bwd_sdp_buffers<D>() + (KV && ai == 1 ? D : 0) +
                                       ch * 32, a);
                     } else {
 #pragma unroll
@@ -560,7 +596,7 @@ cudaError_t launch_bwd_bf16_tc(const BwdBf16Params &p, int grid_x, cudaStream_t 
     const uint64_t blocks = (uint64_t)grid_x * (uint64_t)p.B * (uint64_t)p.H;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-    attn_bwd_bf16_kernel<D, KV><<<(unsigned)blocks, kThreadsB, smem, stream>>>(p);
+    attn_bwd_bf16_kernel<D, KV><<<(unsigned)blocks, bwd_threads<D>(), smem, stream>>>(p);
     return cudaGetLastError();
 }
 
