@@ -181,7 +181,39 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1)
     }
     const int n = max(0, j1 - j0);
 
-    if (threadIdx.x == 0) {
+    // Start-up work that needs no other role goes out before the CTA-wide
+    // barrier: the query-stationary softmax threads issue their row loads of
+    // Q and dout (stored to TMEM after it), and the producer lane prefetches
+    // the tensor maps, sets up the barriers (nothing else touches them before
+    // the CTA-wide barrier) and starts the stationary tile and the first
+    // stream stages.
+    constexpr int NG = 2 / (SW / 4);   // query-stationary: operands per softmax warp (Q, dout)
+    uint32_t xa_w[KV ? 1 : NG][KV ? 1 : D / 2];
+    if (!KV && warp < SW && n > 0) {
+        const int row = r0 + 32 * (warp & 3) + lane;
+        const bool have_row = row < p.Lq;
+        const size_t off = ((size_t)bh * p.Lq + (have_row ? row : 0)) * D;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(((warp >> 2) * NG + g == 0 ? p.xa : p.ya) + off);
+#pragma unroll
+            for (int u = 0; u < (KV ? 0 : D / 8); ++u) {
+                const uint4 v = have_row ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+                xa_w[g][4 * u] = v.x;
+                xa_w[g][4 * u + 1] = v.y;
+                xa_w[g][4 * u + 2] = v.z;
+                xa_w[g][4 * u + 3] = v.w;
+            }
+        }
+    }
+    int pre_issued = 0;   // stream stages the producer lane started before the barrier
+    if (warp == kProdWarpB && lane == 0) {
+        tma_prefetch_desc(&p.tm_xs);
+        tma_prefetch_desc(&p.tm_ys);
+        if (KV) {
+            tma_prefetch_desc(&p.tm_x);
+            tma_prefetch_desc(&p.tm_y);
+        }
         mbar_init(&bars->x_full, 1);
         mbar_init(&bars->xa_full, SW);   // one arrival per softmax warp
         for (int s = 0; s < NS; ++s) {
@@ -196,6 +228,25 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1)
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         mbar_fence_init();
+        if (n > 0) {
+            if (KV) {
+                mbar_arrive_expect_tx(&bars->x_full, 2 * C::kTileX);
+                for (int hh = 0; hh < NH; ++hh) {
+                    tma_load_3d(base + C::kX + hh * C::kHalfX, &p.tm_x, &bars->x_full, hh * 64, r0, bh);
+                    tma_load_3d(base + C::kY + hh * C::kHalfX, &p.tm_y, &bars->x_full, hh * 64, r0, bh);
+                }
+            }
+            for (; pre_issued < NS && pre_issued < n; ++pre_issued) {
+                uint8_t *st = base + C::kStage + pre_issued * 2 * C::kTileS;
+                const int c0 = (j0 + pre_issued) * kColsB;
+                mbar_arrive_expect_tx(&bars->st_full[pre_issued], 2 * C::kTileS);
+                for (int hh = 0; hh < NH; ++hh) {
+                    tma_load_3d(st + hh * C::kHalfS, &p.tm_xs, &bars->st_full[pre_issued], hh * 64, c0, bh);
+                    tma_load_3d(st + C::kTileS + hh * C::kHalfS, &p.tm_ys, &bars->st_full[pre_issued], hh * 64,
+                                c0, bh);
+                }
+            }
+        }
     }
     constexpr uint32_t kTmemCols = bwd_tmem_cols<D, KV>();
     if (warp == kMmaWarpB) {
@@ -216,15 +267,8 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1)
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0 && n > 0) {
             bool ok = true;
-            if (KV) {
-                mbar_arrive_expect_tx(&bars->x_full, 2 * C::kTileX);
-                for (int hh = 0; hh < NH; ++hh) {
-                    tma_load_3d(base + C::kX + hh * C::kHalfX, &p.tm_x, &bars->x_full, hh * 64, r0, bh);
-                    tma_load_3d(base + C::kY + hh * C::kHalfX, &p.tm_y, &bars->x_full, hh * 64, r0, bh);
-                }
-            }
-            int issued = 0;
-            for (int j = 0; ok && j < n; ++j) {
+            int issued = pre_issued;   // the stationary tile and stages [0, pre_issued) went out above
+            for (int j = pre_issued; ok && j < n; ++j) {
                 const int s = j % NS;
                 if (j >= NS)
                     ok = mbar_wait(&bars->st_empty[s], ((j / NS) - 1) & 1, kSiteKvEmpty, abort);
@@ -393,39 +437,26 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1)
         };
         // Query-stationary: the row's Q and dout into TMEM (bf16 pairs, the
         // A-operand layout of the S and dP products; zeros past Lq); with two
-        // warps per quadrant each writes one of the two.
-        if (!KV && n > 0) {
+        // warps per quadrant each writes one of the two.  One memory round
+        // trip: every load was issued before the first store.
+        if constexpr (!KV) {
+          if (n > 0) {
             constexpr uint32_t kXa = 128 * bwd_sdp_buffers<D>() + D;
-            constexpr int NG = 2 / G;   // operands per warp
-            const bool have_row = row < p.Lq;
-            const size_t off = ((size_t)bh * p.Lq + (have_row ? row : 0)) * D;
-            // Every load is issued before the first store (one memory round trip).
-            uint32_t w[NG][D / 2];
-#pragma unroll
-            for (int g = 0; g < NG; ++g) {
-                const uint4 *src = reinterpret_cast<const uint4 *>((gi * NG + g == 0 ? p.xa : p.ya) + off);
-#pragma unroll
-                for (int u = 0; u < D / 8; ++u) {
-                    const uint4 v = have_row ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-                    w[g][4 * u] = v.x;
-                    w[g][4 * u + 1] = v.y;
-                    w[g][4 * u + 2] = v.z;
-                    w[g][4 * u + 3] = v.w;
-                }
-            }
+            // The rows were loaded before the CTA-wide barrier (xa_w).
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
                 const uint32_t dst = tmem + lane_off + kXa + (gi * NG + g) * (D / 2);
                 if constexpr (D == 128) {
-                    tmem_st64(dst, *reinterpret_cast<uint32_t(*)[64]>(w[g]));
+                    tmem_st64(dst, *reinterpret_cast<uint32_t(*)[64]>(xa_w[g]));
                 } else {
-                    tmem_st32(dst, *reinterpret_cast<uint32_t(*)[32]>(w[g]));
+                    tmem_st32(dst, *reinterpret_cast<uint32_t(*)[32]>(xa_w[g]));
                 }
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->xa_full);
+          }
         }
         float2 nxt[HPW];
         if (KV && n > 0) fetch_stats(0, nxt);
