@@ -25,7 +25,7 @@
  *    Jacobian d p_j / d s_k = p_j (delta_jk - p_k), used by the backward
  *    pass (oracle_mha_bwd) together with the row log-sum-exp (oracle_mha_lse).
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *  - scale is passed explicitly (the kernels' default is 1/sqrt(D));
  *  - causal alignment is top-left: key j is visible to query i iff j <= i;
  *  - the padding mask hides keys j >= len_b; query rows are all computed;
