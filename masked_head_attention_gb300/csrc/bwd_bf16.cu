@@ -139,9 +139,10 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk, uint32_t half
     return sdesc_sw128(tile + kk * 2048, half, 1024);
 }
 
+// One 128-row stationary tile: rank tr of n_tiles on its side (heaviest
+// first), problem bh.
 template <int D, bool KV>
-__global__ void __launch_bounds__(bwd_threads<D>(), 1)
-    attn_bwd_bf16_kernel(const __grid_constant__ BwdBf16Params p) {
+__device__ __forceinline__ void bwd_tile(const BwdBf16Params &p, int tr, int n_tiles, int bh) {
     using C = BwdBf16Cfg<D, KV>;
     constexpr int NH = C::NH;
     constexpr int NS = kStagesB;
@@ -156,12 +157,9 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1)
     volatile int *abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // This CTA's stationary tile and the stream tiles it visits.  The grid is
-    // one-dimensional, heaviest tiles first: under the causal rule the first
-    // key tiles see the most queries, the last query tiles the most keys.
-    const int n_tiles = (int)(gridDim.x / (unsigned)(p.B * p.H));
-    const int tr = (int)blockIdx.x / (p.B * p.H);
-    const int bh = (int)blockIdx.x % (p.B * p.H);
+    // This CTA's stationary tile and the stream tiles it visits.  Ranks run
+    // heaviest first: under the causal rule the first key tiles see the most
+    // queries, the last query tiles the most keys.
     const int tile = (KV || !p.causal) ? tr : n_tiles - 1 - tr;
     const int b = bh / p.H;
     const int r0 = tile * kRowsB;
@@ -607,27 +605,64 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1)
     }
 }
 
-template <int D, bool KV>
-cudaError_t launch_bwd_bf16_tc(const BwdBf16Params &p, int grid_x, cudaStream_t stream) {
+// Both halves of the backward in one launch: the key-stationary tiles (dK,
+// dV) and the query-stationary tiles (dQ) are independent, so one grid holds
+// both, interleaved by rank (key tile rank r, then query tile rank r, each
+// for every (b, h)), heaviest first.  Neither half's last wave then leaves
+// SMs idle while the other waits to start.
+struct BwdBf16Launch {
+    BwdBf16Params kv, q;   // key-stationary and query-stationary parameters
+    int n_kv, n_q;         // 128-row tiles on each side (0: that half is absent)
+    int BH;
+};
+
+template <int D>
+__global__ void __launch_bounds__(bwd_threads<D>(), 1)
+    attn_bwd_bf16_kernel(const __grid_constant__ BwdBf16Launch L) {
+    const int idx = (int)blockIdx.x, BH = L.BH;
+    const int m = min(L.n_kv, L.n_q);
+    int r, bh;
+    bool kv;
+    if (idx < 2 * m * BH) {
+        r = idx / (2 * BH);
+        kv = ((idx / BH) & 1) == 0;
+        bh = idx % BH;
+    } else {
+        const int i2 = idx - 2 * m * BH;
+        r = m + i2 / BH;
+        kv = L.n_kv > L.n_q;
+        bh = i2 % BH;
+    }
+    if (kv)
+        bwd_tile<D, true>(L.kv, r, L.n_kv, bh);
+    else
+        bwd_tile<D, false>(L.q, r, L.n_q, bh);
+}
+
+template <int D>
+cudaError_t launch_bwd_bf16_tc(const BwdBf16Launch &L, cudaStream_t stream) {
     // Shared memory requested so that the CTAs resident on one SM never ask
     // for more than its 512 TMEM columns together (an allocation would
-    // otherwise wait for another CTA to finish): 512 / columns per CTA.
-    constexpr uint32_t per_sm = 512u / bwd_tmem_cols<D, KV>();
+    // otherwise wait for another CTA to finish): 512 / columns per CTA (the
+    // same for both halves).
+    static_assert(bwd_tmem_cols<D, true>() == bwd_tmem_cols<D, false>(), "one TMEM size");
+    constexpr uint32_t per_sm = 512u / bwd_tmem_cols<D, true>();
     constexpr size_t floor_smem = (228u * 1024u) / (per_sm + 1) + 1024u;
-    constexpr size_t smem =
-        BwdBf16Cfg<D, KV>::kSmem > floor_smem ? BwdBf16Cfg<D, KV>::kSmem : floor_smem;
+    constexpr size_t need = BwdBf16Cfg<D, true>::kSmem > BwdBf16Cfg<D, false>::kSmem
+                                ? BwdBf16Cfg<D, true>::kSmem
+                                : BwdBf16Cfg<D, false>::kSmem;
+    constexpr size_t smem = need > floor_smem ? need : floor_smem;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_bwd_bf16_kernel<D, KV>,
+        cudaError_t e = cudaFuncSetAttribute(attn_bwd_bf16_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    // One-dimensional grid: tiles x (b, h); the kernel orders the tiles.
-    const uint64_t blocks = (uint64_t)grid_x * (uint64_t)p.B * (uint64_t)p.H;
+    const uint64_t blocks = ((uint64_t)L.n_kv + (uint64_t)L.n_q) * (uint64_t)L.BH;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-    attn_bwd_bf16_kernel<D, KV><<<(unsigned)blocks, bwd_threads<D>(), smem, stream>>>(p);
+    attn_bwd_bf16_kernel<D><<<(unsigned)blocks, bwd_threads<D>(), smem, stream>>>(L);
     return cudaGetLastError();
 }
 
@@ -639,54 +674,55 @@ cudaError_t launch_bwd_bf16_tensor(const void *q, const void *k, const void *v, 
                                    int mask_kind, float scale, cudaStream_t stream, int *driver_err) {
     *driver_err = 0;
     const uint64_t BH = (uint64_t)B * H;
-    BwdBf16Params p;
-    std::memset(&p, 0, sizeof(p));
-    p.lse = lse;
-    p.delta = delta;
-    p.kv_lengths = (mask_kind & 2) ? kv_lengths : nullptr;
-    p.B = B;
-    p.H = H;
-    p.Lq = Lq;
-    p.Lk = Lk;
-    p.causal = (mask_kind & 1) ? 1 : 0;
-    p.scale = scale;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    cudaError_t e = cudaSuccess;
+    if (BH > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+    BwdBf16Launch L;
+    std::memset(&L, 0, sizeof(L));
+    L.BH = (int)BH;
+    BwdBf16Params &pk = L.kv, &pq = L.q;
+    pk.lse = lse;
+    pk.delta = delta;
+    pk.kv_lengths = (mask_kind & 2) ? kv_lengths : nullptr;
+    pk.B = B;
+    pk.H = H;
+    pk.Lq = Lq;
+    pk.Lk = Lk;
+    pk.causal = (mask_kind & 1) ? 1 : 0;
+    pk.scale = scale;
+    pk.scale_log2 = scale * 1.4426950408889634f;
+    pq = pk;
     CUresult r = CUDA_SUCCESS;
     // Key-stationary: dK, dV (every key row written, zeros where no query sees it).
     if (Lk > 0) {
         const bool has_q = Lq > 0;
-        r = encode_bf16_3d(&p.tm_x, k, D, Lk, BH, kRowsB);
-        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_y, v, D, Lk, BH, kRowsB);
-        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_xs, has_q ? q : k, D, has_q ? Lq : Lk, BH, kColsB);
-        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_ys, has_q ? dout : v, D, has_q ? Lq : Lk, BH, kColsB);
+        r = encode_bf16_3d(&pk.tm_x, k, D, Lk, BH, kRowsB);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&pk.tm_y, v, D, Lk, BH, kRowsB);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&pk.tm_xs, has_q ? q : k, D, has_q ? Lq : Lk, BH, kColsB);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&pk.tm_ys, has_q ? dout : v, D, has_q ? Lq : Lk, BH, kColsB);
         if (r != CUDA_SUCCESS) {
             *driver_err = (int)r;
             return cudaErrorInvalidValue;
         }
-        p.g1 = static_cast<__nv_bfloat16 *>(dk);
-        p.g2 = static_cast<__nv_bfloat16 *>(dv);
-        const int gx = (Lk + kRowsB - 1) / kRowsB;
-        e = D == 64 ? launch_bwd_bf16_tc<64, true>(p, gx, stream) : launch_bwd_bf16_tc<128, true>(p, gx, stream);
-        if (e != cudaSuccess) return e;
+        pk.g1 = static_cast<__nv_bfloat16 *>(dk);
+        pk.g2 = static_cast<__nv_bfloat16 *>(dv);
+        L.n_kv = (Lk + kRowsB - 1) / kRowsB;
     }
     // Query-stationary: dQ.
     if (Lq > 0) {
         const bool has_k = Lk > 0;
         // Q and dout go to TMEM row by row (plain loads); K and V stream by TMA.
-        p.xa = static_cast<const __nv_bfloat16 *>(q);
-        p.ya = static_cast<const __nv_bfloat16 *>(dout);
-        r = encode_bf16_3d(&p.tm_xs, has_k ? k : q, D, has_k ? Lk : Lq, BH, kColsB);
-        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&p.tm_ys, has_k ? v : dout, D, has_k ? Lk : Lq, BH, kColsB);
+        pq.xa = static_cast<const __nv_bfloat16 *>(q);
+        pq.ya = static_cast<const __nv_bfloat16 *>(dout);
+        r = encode_bf16_3d(&pq.tm_xs, has_k ? k : q, D, has_k ? Lk : Lq, BH, kColsB);
+        if (r == CUDA_SUCCESS) r = encode_bf16_3d(&pq.tm_ys, has_k ? v : dout, D, has_k ? Lk : Lq, BH, kColsB);
         if (r != CUDA_SUCCESS) {
             *driver_err = (int)r;
             return cudaErrorInvalidValue;
         }
-        p.g1 = static_cast<__nv_bfloat16 *>(dq);
-        p.g2 = nullptr;
-        const int gx = (Lq + kRowsB - 1) / kRowsB;
-        e = D == 64 ? launch_bwd_bf16_tc<64, false>(p, gx, stream) : launch_bwd_bf16_tc<128, false>(p, gx, stream);
+        pq.g1 = static_cast<__nv_bfloat16 *>(dq);
+        pq.g2 = nullptr;
+        L.n_q = (Lq + kRowsB - 1) / kRowsB;
     }
+    const cudaError_t e = D == 64 ? launch_bwd_bf16_tc<64>(L, stream) : launch_bwd_bf16_tc<128>(L, stream);
     return e;
 }
 
