@@ -7,8 +7,9 @@
 // Jacobian of "Why attention must compute the max first" (gsyq.cn, section
 // 3.3) is applied as dS_ij = p_ij (dP_ij - Delta_i), dP_ij = dout_i . v_j,
 // Delta_i = dout_i . o_i (one row pass, shared with the CUDA-core backward).
-// Two kernels of one template, each holding 128 rows of one (b, h) in TMEM
-// lanes and streaming 64-row tiles of the other side:
+// Two kinds of tile (bwd_tile<D, KV>), both run by one kernel launch, each
+// CTA holding 128 rows of one (b, h) in TMEM lanes and streaming 64-row
+// tiles of the other side:
 //   KV = true  (key-stationary): rows = keys, stream query tiles.
 //              S^T = K Q^T, dP^T = V dout^T; P^T and dS^T into TMEM;
 //              dV += P^T dout, dK += dS^T Q  (dK scaled at the end).
@@ -26,8 +27,9 @@
 // producer warp and the MMA issuer / TMEM owner.  Stream tiles go through
 // four shared-memory stages.  Per stream tile j the MMA warp issues S(j) and
 // dP(j), waits for the softmax's P / dS, then the accumulating products,
-// which read the stage and the P / dS columns before S(j + 2) overwrites
-// them (the tensor pipe executes one thread's MMAs in order).
+// which read the stage and the P / dS columns before S(j + NB) overwrites
+// them (NB = the number of S/dP buffers; the tensor pipe executes one
+// thread's MMAs in order).
 // TMEM: per S/dP buffer (two for D = 128, one for D = 64) S in its first 64
 // columns and dP in the next 64; the packed bf16 pairs of P (KV) and dS
 // overwrite the first 16 columns of each 32-column half of S and dP (KV: P
