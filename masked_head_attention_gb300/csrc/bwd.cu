@@ -355,13 +355,8 @@ cudaError_t launch_bwd(const T *q, const T *k, const T *v, const T *o, const T *
     }
     if (e != cudaSuccess || Lk == 0) return e;
     constexpr size_t smem = BwdCfg<D>::kSmem;
-    static bool configured = false;
-    if (!configured) {
-        e = cudaFuncSetAttribute(mha_bwd_f32_kernel<D, T>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    e = set_smem_limit(reinterpret_cast<const void *>(mha_bwd_f32_kernel<D, T>), smem);
+    if (e != cudaSuccess) return e;
     const dim3 grid((Lk + kBwdBN - 1) / kBwdBN, H, B);
     mha_bwd_f32_kernel<D, T><<<grid, kBwdThreads, smem, stream>>>(
         q, k, v, dout, lse, delta, kv, dq_acc, dk, dv, H, Lq, Lk, mask_kind, scale,

@@ -654,13 +654,8 @@ cudaError_t launch_bwd_bf16_tc(const BwdBf16Launch &L, cudaStream_t stream) {
                                 ? BwdBf16Cfg<D, true>::kSmem
                                 : BwdBf16Cfg<D, false>::kSmem;
     constexpr size_t smem = need > floor_smem ? need : floor_smem;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_bwd_bf16_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_bwd_bf16_kernel<D>), smem);
+    if (e != cudaSuccess) return e;
     const uint64_t blocks = ((uint64_t)L.n_kv + (uint64_t)L.n_q) * (uint64_t)L.BH;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;

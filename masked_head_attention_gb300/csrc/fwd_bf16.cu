@@ -43,6 +43,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -929,6 +930,24 @@ DeviceInfo device_info() {
     return info[dev];
 }
 
+cudaError_t set_smem_limit(const void *func, size_t bytes) {
+    struct Done {
+        const void *func;
+        int dev;
+    };
+    static std::mutex lock;
+    static std::vector<Done> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> guard(lock);
+    for (const Done &d : done)
+        if (d.func == func && d.dev == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done.push_back({func, dev});
+    return e;
+}
+
 namespace {
 
 int g_grid_override = 0;
@@ -936,13 +955,8 @@ int g_grid_override = 0;
 template <int D, bool PRENORM>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
     constexpr size_t smem = Cfg<D>::kSmem;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<D, PRENORM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_fwd_bf16_kernel<D, PRENORM>), smem);
+    if (e != cudaSuccess) return e;
     // Persistent grid: one CTA per SM (one fits per SM), unless overridden.
     int grid = g_grid_override > 0 ? g_grid_override : device_info().sms;
     if (grid > p.n_items) grid = p.n_items;
@@ -1095,13 +1109,8 @@ cudaError_t launch_selftest_umma(int variant, int kn, const void *a, const void 
     p.variant = variant;
     p.kn = kn;
     const size_t smem = 1024 + 4 * kHalfBytes + 64;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(selftest_umma_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(selftest_umma_kernel), smem);
+    if (e != cudaSuccess) return e;
     selftest_umma_kernel<<<1, 128, smem, stream>>>(p);
     return cudaGetLastError();
 }

@@ -511,14 +511,8 @@ cudaError_t launch_small(const float *q, const float *k, const float *v, const i
     using C = SmallCfg<D>;
     const int keys_cap = ((Lk + 31) / 32) * 32;
     const size_t smem = C::smem(keys_cap);
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(mha_fwd_f32_small_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C::smem(C::kMaxKeys));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(mha_fwd_f32_small_kernel<D>), C::smem(C::kMaxKeys));
+    if (e != cudaSuccess) return e;
     const dim3 grid((Lq + kSmallRows - 1) / kSmallRows, H, B);
     mha_fwd_f32_small_kernel<D><<<grid, kSmallThreads, smem, stream>>>(
         q, k, v, kv, out, lse, H, Lq, Lk, mask_kind, scale * 1.4426950408889634f, keys_cap);
@@ -530,13 +524,8 @@ cudaError_t launch(const float *q, const float *k, const float *v, const int32_t
                    float *out, float *lse, int B, int H, int Lq, int Lk, int mask_kind, float scale,
                    cudaStream_t stream) {
     constexpr size_t smem = F32Cfg<D>::kSmem;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(mha_fwd_f32_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(mha_fwd_f32_kernel<D>), smem);
+    if (e != cudaSuccess) return e;
     const dim3 grid((Lq + kBM - 1) / kBM, H, B);
     const float scale_log2 = scale * 1.4426950408889634f;
     mha_fwd_f32_kernel<D><<<grid, kThreads, smem, stream>>>(q, k, v, kv, out, lse, H, Lq, Lk,

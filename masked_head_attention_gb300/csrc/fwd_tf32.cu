@@ -702,13 +702,8 @@ cudaError_t launch_fwd_tf32x3(const float *q, const float *k, const float *v,
     p.scale_log2 = scale * 1.4426950408889634f;
     p.n_qt = (Lq + kRows - 1) / kRows;
     p.n_items = (int)(BH * (uint64_t)p.n_qt);
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_tf32x3_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_fwd_tf32x3_kernel), kSmem);
+    if (e != cudaSuccess) return e;
     int grid = device_info().sms;
     if (grid > p.n_items) grid = p.n_items;
     if (grid < 1) return cudaSuccess;

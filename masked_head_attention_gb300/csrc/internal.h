@@ -15,6 +15,11 @@ struct DeviceInfo {
     int l2 = 0;
 };
 DeviceInfo device_info();
+// Raises `func`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (function, device); thread-safe.  Function attributes
+// belong to a device's context, so a process that launches on several GPUs
+// sets each one.
+cudaError_t set_smem_limit(const void *func, size_t bytes);
 
 // cuTensorMapEncodeTiled from the driver (null if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
