@@ -234,22 +234,10 @@ __device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint
 }
 
 // D[tmem] (+)= A[tmem] * B[smem desc] with tf32 operands (kind::tf32: K = 8
-// per instruction, one 32-bit element per TMEM column / 4 bytes of a row).
-__device__ __forceinline__ void umma_ts_tf32_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                               uint32_t b_hi, uint32_t idesc,
-                                               uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
-        "mov.b64 bd, {%2, %3};\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// The same MMA issued by one elected lane of a converged warp (every lane
-// executes the call; elect.sync picks the lowest active lane, so the same
-// lane issues every time and its later tcgen05.commit covers these MMAs).
+// per instruction, one 32-bit element per TMEM column / 4 bytes of a row),
+// issued by one elected lane of a converged warp (every lane executes the
+// call; elect.sync picks the lowest active lane, so the same lane issues
+// every time and its later tcgen05.commit covers these MMAs).
 __device__ __forceinline__ void umma_ts_tf32_elect(uint32_t d_tmem, uint32_t a_tmem,
                                                    uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                                    uint32_t accumulate) {
@@ -426,14 +414,6 @@ __device__ __forceinline__ bool elect_one() {
         "selp.u32 %0, 1, 0, P;\n\t}"
         : "=r"(pred));
     return pred != 0;
-}
-
-// fp32 -> tf32 (10 explicit mantissa bits, round to nearest, ties away from
-// zero), returned as the 32-bit pattern with the low 13 bits zero.
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
 }
 
 // Pack two floats to bf16x2 (round to nearest even): `lo` goes to bits 0-15.
