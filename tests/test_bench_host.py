@@ -54,10 +54,38 @@ def test_kernel_choice_and_tf32_roofline():
     peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 7000.0, "_source": "test"}
     lens = [512] * 16
     flops = bench.mask_aware_flops(c2, lens)
+    nbytes = bench.algorithmic_bytes(c2, lens)
+    tf32 = 2000.0 * 1.1 / 2.25
+    # Only the method's work counts: 4*D FLOP per (row, key), not the three
+    # tf32 MMAs of the emulation.  At these sizes HBM binds.
+    assert flops / (tf32 * 1e12) < nbytes / 7000e9
     r = bench.roofline_for(c2, lens, 0.05, peaks, 152)
-    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
-    assert abs(r["peak"] - 2000.0 * 1.1 / 2.25) < 0.1
-    assert abs(r["achieved"] - 3 * flops / 0.05e-3 / 1e12) < 1e-3
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 7000.0
+    assert abs(r["achieved"] - nbytes / 0.05e-3 / 1e9) < 1e-2
+    assert abs(r["tensor_issue_frac"] - 3 * flops / 0.05e-3 / 1e12 / tf32) < 1e-4
+    # A long fp32 problem on the same kernel is bound by the tf32 pipe.
+    long = synthetic.small(dtype="f32", D=64, B=1, H=8, Lq=8192, Lk=8192, mask=0)
+    r2 = bench.roofline_for(long, None, 1.0, peaks, 152)
+    assert r2["bound"] == "tensor" and abs(r2["peak"] - tf32) < 0.1
+    assert abs(r2["achieved"] - bench.mask_aware_flops(long, None) / 1e-3 / 1e12) < 1e-3
+
+
+def test_headline_is_the_largest_config():
+    assert bench.DEFAULT_WORKLOAD == "c5_long_causal_bf16"
+
+
+def test_even_row_sample_accounts_exact_flops():
+    for name in ("c1_causal_f32", "c2_padding_f32", "c4_prenorm_bf16"):
+        w = synthetic.WORKLOADS[name]
+        lens = None if w.len_range is None else list(range(w.len_range[0], w.len_range[0] + w.B))
+        rows, f = bench.sample_rows_even(w, lens, 1.0)   # tiny target: stride covers all rows
+        total = bench.mask_aware_flops(w, lens)
+        rows1, f1 = bench.sample_rows_even(w, lens, total * 10)   # stride 1: every row
+        assert len(rows1) == w.B * w.H * w.Lq and abs(f1 - total) <= 1e-9 * total
+        rows4, f4 = bench.sample_rows_even(w, lens, total / 4, offset=1)
+        assert abs(len(rows4) - len(rows1) / 4) <= 1
+        assert 0.2 * total < f4 < 0.3 * total
+        assert set(map(tuple, rows4)) <= set(map(tuple, rows1))
 
 
 def test_fp32_alu_peak():
