@@ -239,6 +239,9 @@ class GpuWorkload:
                                                    scale=w.scale)
                 s["dk"] = torch.empty_like(s["k"])
                 s["dv"] = torch.empty_like(s["v"])
+                need = mha.mha_bwd_workspace_size(w.B, w.H, w.Lq, w.D,
+                                                  mha.F32 if w.dtype == "f32" else mha.BF16)
+                s["ws"] = torch.empty((max(need, 1),), dtype=torch.uint8, device=device)
             torch.cuda.synchronize()
 
     def step(self, s=None):
@@ -250,7 +253,8 @@ class GpuWorkload:
             self.mha.mha_fwd(s["q"], s["k"], s["v"], w.mask, self.kv, out=s["out"], scale=w.scale)
         elif w.kind == "mha_bwd":   # s["out"] receives dq
             self.mha.mha_bwd(s["q"], s["k"], s["v"], s["o"], s["dout"], s["lse"], w.mask, self.kv,
-                             dq=s["out"], dk=s["dk"], dv=s["dv"], scale=w.scale)
+                             dq=s["out"], dk=s["dk"], dv=s["dv"], scale=w.scale,
+                             workspace=s["ws"])
         elif w.kind == "prenorm":
             self.mha.prenorm_cross_attn_fwd(s["x"], s["gamma"], s["beta"], w.eps, s["k"], s["v"],
                                             self.kv, out=s["out"], scale=w.scale)
@@ -607,10 +611,17 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--extra-steps", type=int, default=0,
                     help="fixed timed steps for the other workloads (0 = about 0.3 s each)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload with this batch size instead (profiling captures "
+                         "of a smaller case of the same kernel); 0 = the workload's own")
     ap.add_argument("--settle-s", type=float, default=1.0,
                     help="untimed back-to-back steps before the timed region (clock settling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.batch > 0:
+        import dataclasses
+        w0 = synthetic.WORKLOADS[args.workload]
+        synthetic.WORKLOADS[args.workload] = dataclasses.replace(w0, B=args.batch)
 
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -25,8 +25,8 @@
  *  - Pointers are DEVICE pointers owned by the caller; the library keeps no
  *    per-call state.  mha_fwd and mha_fwd_lse allocate no device memory;
  *    prenorm_cross_attn_fwd takes a stream-ordered workspace of 8*B*Lq bytes
- *    and mha_bwd one of 4*B*H*Lq bytes (cudaMallocAsync / cudaFreeAsync on
- *    `stream`) for per-row statistics.
+ *    (cudaMallocAsync / cudaFreeAsync on `stream`) for per-row statistics;
+ *    mha_bwd uses a workspace the caller passes in (mha_bwd_workspace_size).
  *  - Layouts are dense and row-major: q, out [B,H,Lq,D]; k, v [B,H,Lk,D];
  *    kv_lengths int32 [B].  Every tensor pointer must be 16-byte aligned.
  *  - Work is enqueued on `stream` (0 = legacy default stream); no entry
@@ -41,6 +41,7 @@
 #ifndef MHA_GB300_H
 #define MHA_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -129,29 +130,42 @@ MHA_API int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_ki
  *   dout        dL/dO [B,H,Lq,D].
  *   lse         the forward's row log-sum-exp [B,H,Lq] (mha_fwd_lse).
  *   dq          [B,H,Lq,D]; dk, dv [B,H,Lk,D]: outputs of `dtype`, fully
- *               written (dq is accumulated in fp32 with atomic adds, so its
- *               last bits can differ between runs).  Must not alias any
+ *               written (for fp32, dq is accumulated with atomic adds, so
+ *               its last bits can differ between runs).  Must not alias any
  *               input.
  *   dtype       MHA_F32 or MHA_BF16: q, k, v, out, dout and the gradients
  *               all of that type, rounded once (to nearest even) for bf16.
- * Kernels.  fp32: CUDA-core FFMA, a row pass (Delta, dq = 0) and a key-tile
- * kernel adding dq with fp32 atomics (its last bits can differ between
- * runs).  bf16 (default): the tensor cores, fp32 accumulation in TMEM, P and
- * dS rounded to bf16 for the products; the row pass (Delta), a key-
- * stationary kernel writing dk and dv and a query-stationary kernel writing
- * dq -- every element written once, the same on every run.  bf16 with
- * mha_set_bwd_kernel(1): the CUDA-core kernels (fp32 arithmetic, dq through
- * an fp32 accumulator and a conversion pass).
- * Memory: a stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on
- * `stream`) of 4*B*H*Lq bytes (rounded up to 256) for Delta, plus, for bf16
- * on CUDA cores, 4*B*H*Lq*D bytes for the fp32 dq accumulator.  Lq == 0
- * with Lk > 0 writes zero dk and dv.  Returns MHA_OK or a negative
- * mha_status.
+ *   workspace   device scratch of at least mha_bwd_workspace_size(...) bytes,
+ *               16-byte aligned, owned by the caller; its contents on entry
+ *               do not matter and on return are unspecified.  It must not be
+ *               used by anything else until the call's kernels have run.
+ *   workspace_bytes  its size; too small (or a null workspace when a
+ *               nonzero size is needed) returns MHA_ERR_INVALID_ARG.
+ * Kernels.  fp32: CUDA-core FFMA, a row pass (Delta into the workspace, dq =
+ * 0) and a key-tile kernel adding dq with fp32 atomics (its last bits can
+ * differ between runs).  bf16 (default): the tensor cores, fp32 accumulation
+ * in TMEM, P and dS rounded to bf16 for the products; the row pass (Delta)
+ * and one launch holding two kinds of tile, interleaved heaviest first:
+ * key-stationary tiles that write dk and dv, and query-stationary tiles that
+ * write dq -- every element written once, the same on every run.  bf16 with
+ * the CUDA-core test hook (mha_testing.h): fp32 arithmetic, dq through an
+ * fp32 accumulator in the workspace and a conversion pass.
+ * The library allocates no device memory.  Lq == 0 with Lk > 0 writes zero
+ * dk and dv.  Returns MHA_OK or a negative mha_status.
  */
 MHA_API int mha_bwd(const void *q, const void *k, const void *v, const void *out,
                     const void *dout, const float *lse, int mask_kind,
                     const int32_t *kv_lengths, void *dq, void *dk, void *dv, int B, int H,
-                    int Lq, int Lk, int D, float scale, int dtype, cudaStream_t stream);
+                    int Lq, int Lk, int D, float scale, int dtype, void *workspace,
+                    size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * mha_bwd_workspace_size -- bytes of workspace mha_bwd needs for these sizes
+ * on the calling thread's kernel choice: 4*B*H*Lq (rounded up to 256) for
+ * the per-row Delta, plus 4*B*H*Lq*D for bf16 on the CUDA-core test path.
+ * Returns 0 for an empty problem or invalid sizes.
+ */
+MHA_API size_t mha_bwd_workspace_size(int B, int H, int Lq, int D, int dtype);
 
 /*
  * prenorm_cross_attn_fwd -- Pre-LayerNorm cross-attention forward
@@ -230,71 +244,6 @@ MHA_API const char *mha_strerror(int status);
  * copies from the current device.  Returns MHA_OK or MHA_ERR_CUDA.
  */
 MHA_API int mha_device_status(uint32_t *bits, int clear);
-
-/*
- * mha_selftest_umma -- diagnostic: one 128-row tcgen05 GEMM tile built
- * with exactly the shared-memory/TMEM descriptors the bf16 attention kernel
- * uses, so the descriptor encoding can be checked against a host matmul.
- *   variant 0: C[128,128] = A[128,K] * B[128,K]^T, both K-major in shared
- *              memory (the S = Q K^T step); K = 64 or 128.
- *   variant 1: C[128,N] = A[128,128] * B[128,N], A K-major and B N-major in
- *              shared memory (the P V step with P staged in shared memory).
- *   variant 2: as variant 1 but A is first written to tensor memory and the
- *              MMA reads it from there (the P V step the kernel uses).
- *   a, b bf16 row-major device buffers; c fp32 [128, N or 128] row-major.
- * Returns MHA_OK or a negative mha_status.
- */
-MHA_API int mha_selftest_umma(int variant, int K_or_N, const void *a, const void *b,
-                      float *c, cudaStream_t stream);
-
-/*
- * mha_set_bf16_grid -- launch-shape hook for tests and benchmarks: run the
- * persistent bf16 kernels on `ctas` CTAs (each loops over its share of the
- * work items); 0 restores the default of one CTA per SM.  Affects later
- * calls from any thread of the process.
- */
-MHA_API void mha_set_bf16_grid(int ctas);
-
-/*
- * mha_set_f32_kernel -- kernel-choice hook for tests and benchmarks of the
- * fp32 path.  0 = automatic: for D = 64 the tensor-core kernel (three TF32
- * MMAs per product: hi*hi + lo*hi + hi*lo of the operands split as
- * x = tf32(x) + tf32(x - tf32(x)), fp32 accumulation in TMEM); for D = 128
- * the CUDA-core kernels: the short-key-range kernel (every visible K/V row
- * of a 16-row query block staged in shared memory at once) when
- * Lk * D <= 16384, else the tiled kernel (64-row query tiles, 64-key K/V
- * tiles).  1 = always the tiled CUDA-core kernel; 2 = the short-key-range
- * kernel whenever Lk * D <= 16384, else the tiled one; 3 = as 0.  Other
- * values act as 0.  Affects later calls from any thread of the process.
- */
-MHA_API void mha_set_f32_kernel(int which);
-
-/*
- * mha_set_bf16_decode -- kernel-choice hook for tests and benchmarks of the
- * bf16 path.  0 = automatic: mha_fwd calls with at most 8 query rows run the
- * decode kernel (the keys of each (b, h) split over a thread-block cluster of
- * up to 8 CTAs, partial results combined in distributed shared memory);
- * 1 = never (always the tensor-core kernel).  Other values act as 0.
- * Affects later calls from any thread of the process.
- */
-MHA_API void mha_set_bf16_decode(int mode);
-
-/*
- * mha_set_bf16_decode_splits -- launch-shape hook for tests and benchmarks of
- * the decode kernel: split the keys of every (b, h) over `splits` CTAs (one
- * cluster; values above 8 act as 8); 0 restores the automatic choice (about
- * one CTA per SM in total, at least 256 keys per CTA).  Affects later calls
- * from any thread of the process.
- */
-MHA_API void mha_set_bf16_decode_splits(int splits);
-
-/*
- * mha_set_bwd_kernel -- kernel-choice hook for tests and benchmarks of
- * mha_bwd: 0 = automatic (bf16 on the tensor cores, fp32 on CUDA cores);
- * 1 = CUDA cores for both.  Other values act as 0.  Affects later calls from
- * any thread of the process.
- */
-MHA_API void mha_set_bwd_kernel(int which);
 
 #ifdef __cplusplus
 }

@@ -52,8 +52,15 @@ def lib():
         L.prenorm_cross_attn_residual_fwd.restype = i
         L.mha_fwd_lse.argtypes = [P, P, P, i, P, P, P, i, i, i, i, i, f, i, P]
         L.mha_fwd_lse.restype = i
-        L.mha_bwd.argtypes = [P, P, P, P, P, P, i, P, P, P, P, i, i, i, i, i, f, i, P]
+        L.mha_bwd.argtypes = [P, P, P, P, P, P, i, P, P, P, P, i, i, i, i, i, f, i, P,
+                              ctypes.c_size_t, P]
         L.mha_bwd.restype = i
+        L.mha_bwd_workspace_size.argtypes = [i, i, i, i, i]
+        L.mha_bwd_workspace_size.restype = ctypes.c_size_t
+        L.mha_test_set_device_status.argtypes = [i, ctypes.c_uint32]
+        L.mha_test_set_device_status.restype = i
+        L.mha_test_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.mha_test_set_wait_limit_ns.restype = i
         L.mha_strerror.argtypes = [i]
         L.mha_strerror.restype = ctypes.c_char_p
         L.mha_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
@@ -183,13 +190,21 @@ def mha_fwd_lse(q, k, v, mask_kind=MASK_NONE, kv_lengths=None, out=None, lse=Non
     return out, lse
 
 
+def mha_bwd_workspace_size(B, H, Lq, D, dtype):
+    """Bytes of device workspace mha_bwd needs (dtype: F32 or BF16 code)."""
+    return int(lib().mha_bwd_workspace_size(int(B), int(H), int(Lq), int(D), int(dtype)))
+
+
 def mha_bwd(q, k, v, out, dout, lse, mask_kind=MASK_NONE, kv_lengths=None, dq=None, dk=None,
-            dv=None, scale=None, stream=None):
+            dv=None, scale=None, stream=None, workspace=None):
     """Gradients (dq, dk, dv) of sum(dout * out) for out, lse = mha_fwd_lse(q, k, v, ...).
 
     fp32 or bf16 (q, k, v, out, dout and the gradients of one dtype; lse fp32);
     every tensor contiguous on the same device.  q, k, v, mask_kind,
-    kv_lengths and scale must be those of the forward call."""
+    kv_lengths and scale must be those of the forward call.  `workspace` is
+    a device uint8 tensor of at least mha_bwd_workspace_size(...) bytes; when
+    omitted, one is taken from torch's allocator for this call (the library
+    itself never allocates)."""
     torch = _torch()
     _dev(q, "q")
     for t, n in ((k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
@@ -208,11 +223,18 @@ def mha_bwd(q, k, v, out, dout, lse, mask_kind=MASK_NONE, kv_lengths=None, dq=No
     dq = torch.empty_like(q) if dq is None else _dev(dq, "dq", q.dtype)
     dk = torch.empty_like(k) if dk is None else _dev(dk, "dk", q.dtype)
     dv = torch.empty_like(v) if dv is None else _dev(dv, "dv", q.dtype)
+    dt = _dtype_code(q)
+    need = mha_bwd_workspace_size(B, H, Lq, D, dt)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
+    else:
+        _dev(workspace, "workspace")
+    wbytes = workspace.numel() * workspace.element_size()
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     _check(lib().mha_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
                          int(mask_kind), _ptr(kv_lengths), _ptr(dq), _ptr(dk), _ptr(dv),
-                         B, H, Lq, Lk, D, scale, _dtype_code(q), _stream(stream, q.get_device())),
-           "mha_bwd")
+                         B, H, Lq, Lk, D, scale, dt, _ptr(workspace), wbytes,
+                         _stream(stream, q.get_device())), "mha_bwd")
     return dq, dk, dv
 
 
@@ -287,6 +309,17 @@ def device_status(clear=False):
     bits = ctypes.c_uint32(0)
     _check(lib().mha_device_status(ctypes.byref(bits), 1 if clear else 0), "mha_device_status")
     return bits.value
+
+
+def test_set_device_status(unit, bits):
+    """Test hook: OR `bits` into kernel unit `unit`'s device status word
+    (0 bf16 forward, 1 fp32 tensor-core forward, 2 bf16 backward)."""
+    _check(lib().mha_test_set_device_status(int(unit), int(bits)), "mha_test_set_device_status")
+
+
+def test_set_wait_limit_ns(ns):
+    """Test hook: limit of every bounded device wait (0 restores 2 s)."""
+    _check(lib().mha_test_set_wait_limit_ns(int(ns)), "mha_test_set_wait_limit_ns")
 
 
 def selftest_umma(variant, kn, a, b, c, stream=None):

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/mha.h"
+#include "../../include/mha_testing.h"
 #include "internal.h"
 
 namespace {
@@ -15,9 +16,19 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA; }
 
+// The units with bounded waits, in the numbering of mha_test_set_device_status.
+cudaError_t status_ctl(int unit, int op, uint64_t value, uint32_t *bits) {
+    switch (unit) {
+        case 0: return mha::status_ctl_fwd_bf16(op, value, bits);
+        case 1: return mha::status_ctl_fwd_tf32(op, value, bits);
+        case 2: return mha::status_ctl_bwd_bf16(op, value, bits);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 // Backward kernel choice: 0 automatic (bf16 on the tensor cores, fp32 on CUDA
 // cores), 1 CUDA cores for both.
-int g_bwd_kernel = 0;
+thread_local int g_bwd_kernel = 0;
 
 // Shared checks of the shape arguments; 1 means "nothing to do".
 int check_shape(int B, int H, int Lq, int Lk, int D, float scale, int *empty) {
@@ -117,10 +128,19 @@ int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_kind,
     return drv != 0 ? MHA_ERR_CUDA : from_cuda(e);
 }
 
+size_t mha_bwd_workspace_size(int B, int H, int Lq, int D, int dtype) {
+    if (B <= 0 || H <= 0 || Lq <= 0 || (D != 64 && D != 128)) return 0;
+    if (dtype != MHA_F32 && dtype != MHA_BF16) return 0;
+    const size_t rows = (size_t)B * H * Lq;
+    const size_t delta_bytes = (sizeof(float) * rows + 255) & ~(size_t)255;
+    const bool tensor = dtype == MHA_BF16 && g_bwd_kernel != 1;
+    return delta_bytes + (dtype == MHA_BF16 && !tensor ? sizeof(float) * rows * D : 0);
+}
+
 int mha_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
             const float *lse, int mask_kind, const int32_t *kv_lengths, void *dq, void *dk,
             void *dv, int B, int H, int Lq, int Lk, int D, float scale, int dtype,
-            cudaStream_t stream) {
+            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     int empty = 0;
     int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
     if (st != MHA_OK) return st;
@@ -132,22 +152,20 @@ int mha_bwd(const void *q, const void *k, const void *v, const void *out, const 
     if ((Lq > 0 && (!q || !out || !dout || !lse || !dq)) || (Lk > 0 && (!k || !v || !dk || !dv)))
         return MHA_ERR_INVALID_ARG;
     if ((mask_kind & MHA_MASK_KV_LEN) && !kv_lengths) return MHA_ERR_INVALID_ARG;
+    // Per-row Delta = dout . o (and, for bf16 on CUDA cores, the fp32 dq
+    // accumulator) live in the caller's workspace.
+    const size_t need = mha_bwd_workspace_size(B, H, Lq, D, dtype);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MHA_ERR_INVALID_ARG;
     if ((Lq > 0 && (!aligned16(q) || !aligned16(out) || !aligned16(dout) || !aligned16(lse) ||
                     !aligned16(dq))) ||
-        (Lk > 0 && (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))))
+        (Lk > 0 && (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))) ||
+        (need > 0 && !aligned16(workspace)))
         return MHA_ERR_MISALIGNED;
-    // Per-row Delta = dout . o (and, for bf16 on CUDA cores, the fp32 dq
-    // accumulator) live in a stream-ordered workspace for this call.
     const bool tensor = dtype == MHA_BF16 && g_bwd_kernel != 1;
     const size_t rows = (size_t)B * H * Lq;
     const size_t delta_bytes = (sizeof(float) * rows + 255) & ~(size_t)255;
-    const size_t ws_bytes =
-        delta_bytes + (dtype == MHA_BF16 && !tensor ? sizeof(float) * rows * D : 0);
-    char *ws = nullptr;
-    if (ws_bytes > 0 &&
-        cudaMallocAsync(reinterpret_cast<void **>(&ws), ws_bytes, stream) != cudaSuccess)
-        return MHA_ERR_CUDA;
-    float *delta = reinterpret_cast<float *>(ws);
+    char *ws = static_cast<char *>(workspace);
+    float *delta = need > 0 ? reinterpret_cast<float *>(ws) : nullptr;
     cudaError_t e;
     int drv = 0;
     if (tensor) {
@@ -164,12 +182,8 @@ int mha_bwd(const void *q, const void *k, const void *v, const void *out, const 
                                 stream);
     else
         e = mha::launch_bwd_bf16(q, k, v, out, dout, lse, kv_lengths, dq, dk, dv,
-                                 reinterpret_cast<float *>(ws + delta_bytes), delta, B, H, Lq, Lk,
-                                 D, mask_kind, scale, stream);
-    if (ws != nullptr) {
-        const cudaError_t ef = cudaFreeAsync(ws, stream);
-        if (e == cudaSuccess) e = ef;
-    }
+                                 need > 0 ? reinterpret_cast<float *>(ws + delta_bytes) : nullptr,
+                                 delta, B, H, Lq, Lk, D, mask_kind, scale, stream);
     if (drv != 0) return MHA_ERR_CUDA;
     return from_cuda(e);
 }
@@ -299,11 +313,26 @@ const char *mha_strerror(int status) {
 }
 
 int mha_device_status(uint32_t *bits, int clear) {
-    // Each tensor-core translation unit keeps its own word; report their union.
-    uint32_t a = 0, b = 0;
-    cudaError_t e = mha::read_device_status(&a, clear != 0);
-    if (e == cudaSuccess) e = mha::read_device_status_tf32(&b, clear != 0);
-    if (bits) *bits = a | b;
+    // Each unit with bounded waits keeps its own word; report their union.
+    uint32_t all = 0;
+    cudaError_t e = cudaSuccess;
+    for (int u = 0; u < mha::kStatusUnits && e == cudaSuccess; ++u) {
+        uint32_t w = 0;
+        e = status_ctl(u, 0, clear != 0 ? 1 : 0, &w);
+        all |= w;
+    }
+    if (bits) *bits = all;
+    return from_cuda(e);
+}
+
+int mha_test_set_device_status(int unit, uint32_t bits) {
+    if (unit < 0 || unit >= mha::kStatusUnits) return MHA_ERR_INVALID_ARG;
+    return from_cuda(status_ctl(unit, 1, bits, nullptr));
+}
+
+int mha_test_set_wait_limit_ns(uint64_t ns) {
+    cudaError_t e = cudaSuccess;
+    for (int u = 0; u < mha::kStatusUnits && e == cudaSuccess; ++u) e = status_ctl(u, 2, ns, nullptr);
     return from_cuda(e);
 }
 
@@ -319,8 +348,7 @@ int mha_selftest_umma(int variant, int K_or_N, const void *a, const void *b, flo
     return from_cuda(e);
 }
 
-// Benchmark hook: cap the bf16 grid at `ctas` CTAs (persistent scheduling);
-// 0 restores one CTA per work item.
+// Test and benchmark hooks (mha_testing.h); thread-local state.
 void mha_set_bf16_grid(int ctas) { mha::set_bf16_grid_override(ctas); }
 
 void mha_set_f32_kernel(int which) { mha::set_f32_kernel_override(which); }

@@ -723,4 +723,8 @@ cudaError_t launch_bwd_bf16_tensor(const void *q, const void *k, const void *v, 
     return e;
 }
 
+cudaError_t status_ctl_bwd_bf16(int op, uint64_t value, uint32_t *bits) {
+    return unit_status_ctl(op, value, bits);
+}
+
 }  // namespace mha

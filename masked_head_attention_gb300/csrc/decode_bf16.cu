@@ -264,8 +264,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     cluster_sync_all();
 }
 
-int g_decode_override = 0;   // 0 automatic, 1 never
-int g_decode_splits = 0;     // 0 automatic, else CTAs per (b, h) (at most 8)
+thread_local int g_decode_override = 0;  // 0 automatic, 1 never
+thread_local int g_decode_splits = 0;   // 0 automatic, else CTAs per (b, h) (at most 8)
 
 template <int D, int R>
 cudaError_t launch_dec(const Bf16Call &c, int splits, int chunk, cudaStream_t stream) {

@@ -950,7 +950,7 @@ cudaError_t set_smem_limit(const void *func, size_t bytes) {
 
 namespace {
 
-int g_grid_override = 0;
+thread_local int g_grid_override = 0;
 
 template <int D, bool PRENORM>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
@@ -968,16 +968,8 @@ cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
 
 void set_bf16_grid_override(int ctas) { g_grid_override = ctas; }
 
-cudaError_t read_device_status(uint32_t *bits, bool clear) {
-    unsigned int v = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
-    if (e != cudaSuccess) return e;
-    if (bits) *bits = v;
-    if (clear && v != 0) {
-        const unsigned int z = 0;
-        e = cudaMemcpyToSymbol(g_status, &z, sizeof(z));
-    }
-    return e;
+cudaError_t status_ctl_fwd_bf16(int op, uint64_t value, uint32_t *bits) {
+    return unit_status_ctl(op, value, bits);
 }
 
 // ---------------------------------------------------------------------------

@@ -535,7 +535,7 @@ cudaError_t launch(const float *q, const float *k, const float *v, const int32_t
 
 // 0 automatic, 1 tiled only, 2 short-key kernel where it applies, 3 the
 // tensor-core (3xTF32) kernel where it applies (D = 64).
-int g_f32_kernel = 0;
+thread_local int g_f32_kernel = 0;
 
 }  // namespace
 

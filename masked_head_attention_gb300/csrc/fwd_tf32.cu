@@ -711,16 +711,8 @@ cudaError_t launch_fwd_tf32x3(const float *q, const float *k, const float *v,
     return cudaGetLastError();
 }
 
-cudaError_t read_device_status_tf32(uint32_t *bits, bool clear) {
-    unsigned int v = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
-    if (e != cudaSuccess) return e;
-    if (bits) *bits = v;
-    if (clear && v != 0) {
-        const unsigned int z = 0;
-        e = cudaMemcpyToSymbol(g_status, &z, sizeof(z));
-    }
-    return e;
+cudaError_t status_ctl_fwd_tf32(int op, uint64_t value, uint32_t *bits) {
+    return unit_status_ctl(op, value, bits);
 }
 
 }  // namespace mha

@@ -41,7 +41,6 @@ cudaError_t launch_fwd_tf32x3(const float *q, const float *k, const float *v,
                               const int32_t *kv_lengths, float *out, float *lse, int B, int H,
                               int Lq, int Lk, int D, int mask_kind, float scale,
                               cudaStream_t stream, int *driver_err);
-cudaError_t read_device_status_tf32(uint32_t *bits, bool clear);
 
 // Backward (bwd.cu): dq, dk, dv from q, k, v, the forward output o, its row
 // log-sum-exp and dout.  `delta` is device scratch of B*H*Lq floats.  fp32:
@@ -115,8 +114,15 @@ cudaError_t launch_selftest_umma(int variant, int K_or_N, const void *a, const v
 constexpr int64_t kNoAllocMaxRows = 262144;
 cudaError_t noalloc_ln_stats(int64_t rows, float2 **ptr);
 
-// Device status word of the bf16 translation unit.
-cudaError_t read_device_status(uint32_t *bits, bool clear);
+// Device status word and wait limit of each unit with bounded waits
+// (fwd_bf16.cu, fwd_tf32.cu, bwd_bf16.cu; each keeps its own):
+//   op 0: *bits = the word, cleared afterwards when value != 0;
+//   op 1: OR `value` into the word;
+//   op 2: wait limit = `value` ns (0 restores the default of 2 s).
+cudaError_t status_ctl_fwd_bf16(int op, uint64_t value, uint32_t *bits);
+cudaError_t status_ctl_fwd_tf32(int op, uint64_t value, uint32_t *bits);
+cudaError_t status_ctl_bwd_bf16(int op, uint64_t value, uint32_t *bits);
+constexpr int kStatusUnits = 3;
 
 // Launch-configuration overrides used by tests and benchmark sweeps (0 = default).
 void set_bf16_grid_override(int ctas);

@@ -6,14 +6,19 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 namespace mha {
 
 // ---------------------------------------------------------------------------
 // Device status word.  Bounded waits that expire set bit `site` here and the
 // kernel returns instead of spinning forever; the host reads it with
-// mha_device_status().  Each translation unit including this header has its
-// own copy; only the tensor-core unit (fwd_bf16.cu) has bounded waits.
+// mha_device_status().  A __device__ variable is private to its translation
+// unit (the library is built without relocatable device code), so every unit
+// that includes this header has its own word and its own wait limit; the
+// units with bounded waits (fwd_bf16.cu, fwd_tf32.cu, bwd_bf16.cu) each export
+// a status_ctl_* function built on unit_status_ctl below, and
+// mha_device_status reports the union of their words.
 // ---------------------------------------------------------------------------
 static __device__ unsigned int g_status = 0;
 
@@ -21,10 +26,47 @@ enum WaitSite : uint32_t {
     kSiteQFull = 0, kSiteKFull = 1, kSiteVFull = 2, kSiteKvEmpty = 3,
     kSiteSFull = 4, kSitePFull = 5, kSitePvDone = 6, kSiteQEmpty = 7,
     kSiteOFree = 8, kSiteDrain = 9, kSiteSelftest = 10, kSiteWg = 11,
+    kSiteStats = 12,
 };
 
 // Wall-clock limit for one wait.  Healthy waits last microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// The limit every wait except the teardown drains uses.  Only a test hook
+// changes it (to make waits expire on purpose); the drains, which let copies
+// and products already in flight finish before shared memory or TMEM is
+// released, always keep kWaitLimitNs.
+static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+
+// Host side, on the current device, for this unit's word and limit:
+//   op 0: *bits = the word; cleared afterwards when value != 0;
+//   op 1: OR `value` into the word (a test sets it to check the reporting);
+//   op 2: wait limit = `value` ns, 0 restoring kWaitLimitNs.
+static inline cudaError_t unit_status_ctl(int op, uint64_t value, uint32_t *bits) {
+    if (op == 0) {
+        unsigned int v = 0;
+        cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
+        if (e != cudaSuccess) return e;
+        if (bits) *bits = v;
+        if (value != 0 && v != 0) {
+            const unsigned int z = 0;
+            e = cudaMemcpyToSymbol(g_status, &z, sizeof(z));
+        }
+        return e;
+    }
+    if (op == 1) {
+        unsigned int v = 0;
+        cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
+        if (e != cudaSuccess) return e;
+        v |= (unsigned int)value;
+        return cudaMemcpyToSymbol(g_status, &v, sizeof(v));
+    }
+    if (op == 2) {
+        const unsigned long long ns = value == 0 ? kWaitLimitNs : value;
+        return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns));
+    }
+    return cudaErrorInvalidValue;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -69,18 +111,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed.  Gives up
-// after kWaitLimitNs, or as soon as *abort is set by another role of the
-// CTA; on expiry it records `site` in g_status and sets *abort.  Returns
-// false when it gave up.
+// after the wait limit (g_wait_limit_ns; kWaitLimitNs for the drain site), or
+// as soon as *abort is set by another role of the CTA; on expiry it records
+// `site` in g_status and sets *abort.  Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t site,
                                           volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+    const uint64_t limit =
+        site == kSiteDrain ? kWaitLimitNs
+                           : *reinterpret_cast<volatile unsigned long long *>(&g_wait_limit_ns);
+    // The clock is read every 64 tries; under a limit shorter than 1 ms (a
+    // test's) on every try, so such a wait expires as soon as it has to wait.
+    const uint32_t every = limit < 1000000ull ? 0u : 63u;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if ((it & every) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit) {
                 atomicOr(&g_status, 1u << site);
                 *abort = 1;
                 return false;

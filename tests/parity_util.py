@@ -4,11 +4,14 @@ tolerances written into the tests.
 Tolerances (fixed targets of the method):
   fp32 inputs: max abs error <= 1e-4 against the fp64 oracle.
   bf16 inputs: mean abs error <= 1e-3, and per element
-      |gpu - oracle| <= max(1e-2, ulp_bf16(oracle) + 1e-3).
-  The second term only matters for |oracle| >= 2: rounding the exact result
-  to bf16 alone costs up to half a bf16 ulp (2^-6 = 0.0156 for |O| in [4, 8)),
-  so a literal 1e-2 bound can fail for a perfect kernel.  Tests also report
-  how many elements exceed 1e-2.
+      |gpu - oracle| <= ulp_bf16(oracle) / 2 + 1e-2.
+  The 1e-2 is the method's budget for the arithmetic (fp32 accumulation, P
+  rounded to bf16 before the P.V product).  The half ulp is the one rounding
+  of the result to bf16 that the output format itself imposes: it alone
+  costs up to 2^-7 = 0.0078 for |O| in [2, 4) and 2^-6 = 0.0156 for |O| in
+  [4, 8), so a literal 1e-2 bound can fail for a perfect kernel; below
+  |O| = 0.5 the half ulp is at most 2^-10 and the bound is 1e-2 plus that.
+  Tests also report how many elements exceed 1e-2.
 """
 import math
 
@@ -44,7 +47,7 @@ def check_bf16(got, want, what=""):
     got = np.asarray(got, np.float64)
     err = np.abs(got - want)
     assert np.all(np.isfinite(got)), "%s: non-finite output" % what
-    tol = np.maximum(BF16_MAX_ABS, ulp_bf16(want) + 1e-3)
+    tol = 0.5 * ulp_bf16(want) + BF16_MAX_ABS
     bad = err > tol
     assert not bad.any(), "%s: %d elements over tolerance, worst %.3g at oracle %.3g" % (
         what, bad.sum(), err.max(), want.ravel()[err.argmax()])

@@ -1,6 +1,7 @@
 """The C-ABI library loads and exports every symbol include/mha.h declares,
 and rejects bad arguments on the host, before any CUDA call (CPU only)."""
 import ctypes
+import glob
 import os
 import re
 
@@ -9,7 +10,7 @@ import pytest
 from masked_head_attention_gb300 import build as mbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "mha.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA, DEVICE, TOO_LARGE = 0, -1, -2, -3, -4, -5, -6
 
@@ -24,18 +25,27 @@ def L():
     lib.mha_strerror.restype = ctypes.c_char_p
     lib.mha_selftest_umma.argtypes = [i, i, P, P, P, P]
     lib.mha_fwd_lse.argtypes = [P, P, P, i, P, P, P, i, i, i, i, i, f, i, P]
-    lib.mha_bwd.argtypes = [P, P, P, P, P, P, i, P, P, P, P, i, i, i, i, i, f, i, P]
+    lib.mha_bwd.argtypes = [P, P, P, P, P, P, i, P, P, P, P, i, i, i, i, i, f, i, P,
+                            ctypes.c_size_t, P]
+    lib.mha_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    lib.mha_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.mha_test_set_device_status.argtypes = [i, ctypes.c_uint32]
     return lib
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    return re.findall(r"^MHA_API\s+[\w\s\*]*?\**\s*(\w+)\s*\(", text, re.M)
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        names += re.findall(r"^MHA_API\s+[\w\s\*]*?\**\s*(\w+)\s*\(", text, re.M)
+    return names
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for want in ("mha_fwd", "prenorm_cross_attn_fwd", "mha_strerror", "mha_device_status"):
+    for want in ("mha_fwd", "prenorm_cross_attn_fwd", "mha_strerror", "mha_device_status",
+                 "mha_bwd", "mha_bwd_workspace_size", "mha_set_bf16_grid",
+                 "mha_test_set_device_status", "mha_test_set_wait_limit_ns"):
         assert want in names
 
 
@@ -114,10 +124,13 @@ def test_fwd_lse_host_validation(L, kw, want):
     assert fwd_lse(L, **kw) == want
 
 
+WS = ctypes.c_void_p(0xA0000)
+
+
 def bwd(L, q=A, k=A2, v=A3, o=OUT, g=G, lse=LSE, mask=0, lens=None, dq=DQ, dk=DK, dv=DV,
-        B=2, H=2, Lq=8, Lk=8, D=64, scale=0.125, dtype=0):
+        B=2, H=2, Lq=8, Lk=8, D=64, scale=0.125, dtype=0, ws=WS, ws_bytes=1 << 20):
     return L.mha_bwd(q, k, v, o, g, lse, mask, lens, dq, dk, dv, B, H, Lq, Lk, D, scale, dtype,
-                     None)
+                     ws, ws_bytes, None)
 
 
 @pytest.mark.parametrize("kw,want", [
@@ -129,9 +142,48 @@ def bwd(L, q=A, k=A2, v=A3, o=OUT, g=G, lse=LSE, mask=0, lens=None, dq=DQ, dk=DK
     (dict(B=0), OK), (dict(H=0), OK), (dict(Lq=0, Lk=0), OK),
     # Lq == 0 still writes dk, dv: the query-side pointers are not needed
     (dict(Lq=0, q=None, o=None, g=None, lse=None, dq=None, dk=None), INVALID),
+    # the caller's workspace: present, large enough, aligned
+    (dict(ws=None), INVALID), (dict(ws_bytes=2 * 2 * 8 * 4 - 1), INVALID),
+    (dict(ws=ctypes.c_void_p(0xA0008)), MISALIGNED),
 ])
 def test_bwd_host_validation(L, kw, want):
     assert bwd(L, **kw) == want
+
+
+def test_bwd_workspace_size(L):
+    rows = 3 * 5 * 70
+    delta = (4 * rows + 255) // 256 * 256
+    assert L.mha_bwd_workspace_size(3, 5, 70, 64, 0) == delta       # fp32
+    assert L.mha_bwd_workspace_size(3, 5, 70, 128, 1) == delta      # bf16 on the tensor cores
+    assert L.mha_bwd_workspace_size(0, 5, 70, 64, 0) == 0
+    assert L.mha_bwd_workspace_size(3, 5, 70, 96, 0) == 0
+    L.mha_set_bwd_kernel(1)    # thread-local: this thread only
+    try:
+        assert L.mha_bwd_workspace_size(3, 5, 70, 128, 1) == delta + 4 * rows * 128
+    finally:
+        L.mha_set_bwd_kernel(0)
+    assert L.mha_bwd_workspace_size(3, 5, 70, 128, 1) == delta
+
+
+def test_hooks_are_thread_local(L):
+    import threading
+    rows = 2 * 2 * 8
+    delta = (4 * rows + 255) // 256 * 256
+    seen = []
+    L.mha_set_bwd_kernel(1)
+    try:
+        t = threading.Thread(target=lambda: seen.append(L.mha_bwd_workspace_size(2, 2, 8, 64, 1)))
+        t.start()
+        t.join()
+        assert seen == [delta]    # the other thread still has the automatic choice
+        assert L.mha_bwd_workspace_size(2, 2, 8, 64, 1) == delta + 4 * rows * 64
+    finally:
+        L.mha_set_bwd_kernel(0)
+
+
+def test_status_hook_rejects_unknown_unit(L):
+    assert L.mha_test_set_device_status(3, 1) == INVALID
+    assert L.mha_test_set_device_status(-1, 1) == INVALID
 
 
 def test_selftest_host_validation(L):

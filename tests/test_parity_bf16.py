@@ -86,6 +86,23 @@ def test_bf16_c5_sampled_rows():
 
 
 @pytest.mark.gpu
+def test_bf16_c5_full_workload():
+    """Every element of the long causal workload (B2 H32 L8192 D128, 67 M
+    outputs) against the fp64 oracle, run on all host cores."""
+    w = synthetic.WORKLOADS["c5_long_causal_bf16"]
+    x = synthetic.make(w, seed=0)
+    out = mha.mha_fwd(dev(x["q"]), dev(x["k"]), dev(x["v"]), w.mask, None, scale=w.scale)
+    torch.cuda.synchronize()
+    assert mha.device_status() == 0
+    got = as_np(out)
+    del out
+    want = oracle.mha_fwd(x["q"].float().numpy(), x["k"].float().numpy(), x["v"].float().numpy(),
+                          w.mask, None, w.scale)
+    r = check_bf16(got, want, w.name)
+    print(w.name, r)
+
+
+@pytest.mark.gpu
 def test_bf16_masked_keys_contribute_exactly_zero():
     B, H, L, D = 2, 2, 300, 128
     q = randn((B, H, L, D), 5, dtype=torch.bfloat16)

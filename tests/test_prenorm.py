@@ -59,6 +59,47 @@ def test_prenorm_c4_sampled_rows():
     print(w.name, r)
 
 
+def _c4():
+    w = synthetic.WORKLOADS["c4_prenorm_bf16"]
+    return w, synthetic.make(w, seed=0)
+
+
+def _c4_oracle(fn, w, xs):
+    return fn(xs["x"].float().numpy(), xs["gamma"].numpy(), xs["beta"].numpy(), w.eps,
+              xs["k"].float().numpy(), xs["v"].float().numpy(), xs["kv_lengths"].numpy(), w.scale)
+
+
+@pytest.mark.gpu
+def test_prenorm_c4_full_workload():
+    """Every element of the Pre-LN workload (B32 H16 Lq2048 d_model 1024,
+    67 M outputs) against the fp64 oracle."""
+    w, xs = _c4()
+    out = mha.prenorm_cross_attn_fwd(dev(xs["x"]), dev(xs["gamma"]), dev(xs["beta"]), w.eps,
+                                     dev(xs["k"]), dev(xs["v"]), dev(xs["kv_lengths"]),
+                                     scale=w.scale)
+    torch.cuda.synchronize()
+    assert mha.device_status() == 0
+    got = as_np(out)
+    del out
+    r = check_bf16(got, _c4_oracle(oracle.prenorm_cross_attn, w, xs), w.name)
+    print(w.name, r)
+
+
+@pytest.mark.gpu
+def test_prenorm_residual_c4_full_workload():
+    w, xs = _c4()
+    out = mha.prenorm_cross_attn_residual_fwd(dev(xs["x"]), dev(xs["gamma"]), dev(xs["beta"]),
+                                              w.eps, dev(xs["k"]), dev(xs["v"]),
+                                              dev(xs["kv_lengths"]), scale=w.scale)
+    torch.cuda.synchronize()
+    assert mha.device_status() == 0
+    got = as_np(out)
+    del out
+    r = check_bf16_sum(got, _c4_oracle(oracle.prenorm_cross_attn_residual, w, xs),
+                       w.name + " residual")
+    print(w.name, "residual", r)
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dLq%dLk%dD%d" % c[:5])
 def test_prenorm_residual_small(case):
