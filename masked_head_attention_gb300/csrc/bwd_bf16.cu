@@ -297,6 +297,9 @@ __device__ __forceinline__ void bwd_tile(const BwdBf16Params &p, int tr, int n_t
         constexpr uint32_t kAcc = 128 * NB;                           // first accumulator column
         constexpr uint32_t kXa = kAcc + D, kYa = kXa + D / 2;         // query-stationary: Q, dout
         bool ok = n > 0, issued = false;
+        // Under a test's short wait limit: a wait that must expire (the drain
+        // phase completes only at teardown).
+        if (ok && wait_limit_is_test()) ok = wwait(&bars->drain, 0, kSiteTest);
         if (ok) ok = KV ? wwait(&bars->x_full, 0, kSiteQFull) : wwait(&bars->xa_full, 0, kSiteQFull);
         const uint32_t sx = smem_u32(base + C::kX), sy = smem_u32(base + C::kY);
         // S(j) = X Xs^T and dP(j) = Y Ys^T (128 x 64 each, K = D) into buffer

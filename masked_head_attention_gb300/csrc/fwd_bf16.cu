@@ -433,6 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool r = mbar_wait(bar, parity, site, abort);
             return __all_sync(0xffffffffu, r);
         };
+        // Under a test's short wait limit: a wait that must expire (the drain
+        // phase completes only at teardown).
+        if (wait_limit_is_test()) ok = wwait(&bars->drain, 0, kSiteTest);
         ItemIter iter;
         while (ok && iter.next(p.n_items)) {
             const Item it = decode_item(p, iter.idx);

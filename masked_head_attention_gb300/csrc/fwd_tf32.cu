@@ -331,6 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t g = 0, k = 0;
         bool ok = true;
         bool issued = false;
+        // Under a test's short wait limit: a wait that must expire (the drain
+        // phase completes only at teardown).
+        if (wait_limit_is_test()) ok = wwait(&bars->drain, 0, kSiteTest);
         // Three MMAs per K-step (hi.hi, lo.hi, hi.lo) into `dcol`; A from TMEM
         // columns a_hi / a_lo (8 columns per K-step), B from the K-major tiles
         // b_hi / b_lo (descriptor low words; 64 rows, two 128-byte halves).

@@ -26,7 +26,7 @@ enum WaitSite : uint32_t {
     kSiteQFull = 0, kSiteKFull = 1, kSiteVFull = 2, kSiteKvEmpty = 3,
     kSiteSFull = 4, kSitePFull = 5, kSitePvDone = 6, kSiteQEmpty = 7,
     kSiteOFree = 8, kSiteDrain = 9, kSiteSelftest = 10, kSiteWg = 11,
-    kSiteStats = 12,
+    kSiteStats = 12, kSiteTest = 13,
 };
 
 // Wall-clock limit for one wait.  Healthy waits last microseconds.
@@ -37,6 +37,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // and products already in flight finish before shared memory or TMEM is
 // released, always keep kWaitLimitNs.
 static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+
+// True when a test has shortened the wait limit below 1 ms.  Each kernel's
+// MMA warp then first waits once on a barrier phase that nothing completes
+// before teardown (site kSiteTest), so the expiry path runs on every launch:
+// a hardware-suspending try_wait can otherwise outlast every short wait.
+__device__ __forceinline__ bool wait_limit_is_test() {
+    return *reinterpret_cast<volatile unsigned long long *>(&g_wait_limit_ns) < 1000000ull;
+}
 
 // Host side, on the current device, for this unit's word and limit:
 //   op 0: *bits = the word; cleared afterwards when value != 0;
