@@ -23,10 +23,8 @@
  *
  * Conventions for every entry point.
  *  - Pointers are DEVICE pointers owned by the caller; the library keeps no
- *    per-call state.  mha_fwd and mha_fwd_lse allocate no device memory;
- *    prenorm_cross_attn_fwd takes a stream-ordered workspace of 8*B*Lq bytes
- *    (cudaMallocAsync / cudaFreeAsync on `stream`) for per-row statistics;
- *    mha_bwd uses a workspace the caller passes in (mha_bwd_workspace_size).
+ *    per-call state and allocates no device memory.  (mha_bwd uses a
+ *    workspace the caller passes in, see mha_bwd_workspace_size.)
  *  - Layouts are dense and row-major: q, out [B,H,Lq,D]; k, v [B,H,Lk,D];
  *    kv_lengths int32 [B].  Every tensor pointer must be 16-byte aligned.
  *  - Work is enqueued on `stream` (0 = legacy default stream); no entry
@@ -173,10 +171,12 @@ MHA_API size_t mha_bwd_workspace_size(int B, int H, int Lq, int D, int dtype);
  *     xhat = (x_q[b,i,:] - mean) / sqrt(var + eps) * gamma + beta
  * over the H*D features of the row (biased variance), Q[b,h,i,:] is the
  * head-h slice xhat[h*D:(h+1)*D], and the attention above runs with the
- * padding mask only (kv_lengths, or none when it is NULL).  Two kernels run
- * on `stream`: one pass computes each row's mean and 1/sqrt(var + eps) into
- * the workspace; the attention kernel loads each head's slice of x with TMA
- * and normalises it in shared memory before the first QK^T product.
+ * padding mask only (kv_lengths, or none when it is NULL).  One kernel runs
+ * on `stream` and allocates nothing: it groups the heads of each block of
+ * 256 query rows into chunks, forms each row's mean and 1/sqrt(var + eps)
+ * from the full row of x once per chunk (inside the kernel, in fp32, two
+ * passes), loads each head's slice of x with TMA and normalises it in
+ * shared memory before the first QK^T product.
  *   x_q         [B,Lq,H*D] bf16 (query-side activations)
  *   gamma, beta fp32 [H*D]
  *   eps         finite, >= 0
@@ -199,8 +199,8 @@ MHA_API int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const fl
  *     out[b,i,:] = x_q[b,i,:] + (prenorm_cross_attn_fwd output)[b,i,:]
  * The sum is formed in fp32 inside the attention kernel's epilogue and
  * rounded to bf16 once; a row with no visible key returns x_q's row.
- *   Arguments, layouts, workspace and errors are those of
- *   prenorm_cross_attn_fwd.  out must not overlap x_q.
+ *   Arguments, layouts and errors are those of prenorm_cross_attn_fwd (one
+ *   kernel, no allocation).  out must not overlap x_q.
  */
 MHA_API int prenorm_cross_attn_residual_fwd(const void *x_q, const float *gamma,
                             const float *beta, float eps, const void *k,
@@ -215,7 +215,10 @@ MHA_API int prenorm_cross_attn_residual_fwd(const void *x_q, const float *gamma,
  * for its own pools at start-up and gives libraries only the buffers it
  * planned, or a latency-critical loop in which an allocation could block or
  * fail.  (No counterpart on the pages; this is an interface addition.)
- *   Arguments, layouts and results are those of prenorm_cross_attn_fwd.
+ *   Arguments, layouts and results are those of prenorm_cross_attn_fwd,
+ *   bit for bit.  (prenorm_cross_attn_fwd forms the row statistics inside
+ *   its one kernel and allocates nothing either; this entry point runs them
+ *   as a separate pass first, into the array below.)
  *   Memory: calls no allocator.  The per-row statistics go to a fixed array
  *   of 262144 float2 (2 MiB) that is part of the library's device image and
  *   stays resident on every GPU that loads the library until the process

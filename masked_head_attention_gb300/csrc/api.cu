@@ -192,12 +192,12 @@ int mha_bwd(const void *q, const void *k, const void *v, const void *out, const 
 
 namespace {
 
-// Pre-LN cross-attention with a stream-ordered workspace for the row
-// statistics; `residual` is x_q for the residual variant, else null.
-int prenorm_with_workspace(const void *x_q, const float *gamma, const float *beta, float eps,
-                           const void *k, const void *v, const int32_t *kv_lengths, void *out,
-                           int B, int H, int Lq, int Lk, int D, float scale, int dtype,
-                           cudaStream_t stream, const void *residual) {
+// Pre-LN cross-attention: one kernel, which forms the row statistics of x
+// itself; `residual` is x_q for the residual variant, else null.
+int prenorm_fused(const void *x_q, const float *gamma, const float *beta, float eps,
+                  const void *k, const void *v, const int32_t *kv_lengths, void *out, int B,
+                  int H, int Lq, int Lk, int D, float scale, int dtype, cudaStream_t stream,
+                  const void *residual) {
     int empty = 0;
     int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
     if (st != MHA_OK) return st;
@@ -226,16 +226,9 @@ int prenorm_with_workspace(const void *x_q, const float *gamma, const float *bet
     c.D = D;
     c.mask_kind = kv_lengths ? MHA_MASK_KV_LEN : MHA_MASK_NONE;
     c.scale = scale;
-    // Row statistics of x live in a stream-ordered workspace for this call.
-    float2 *stats = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&stats), sizeof(float2) * (size_t)B * Lq,
-                        stream) != cudaSuccess)
-        return MHA_ERR_CUDA;
     int drv = 0;
-    cudaError_t e = mha::launch_fwd_bf16(c, stream, &drv, stats);
-    const cudaError_t ef = cudaFreeAsync(stats, stream);
+    cudaError_t e = mha::launch_fwd_bf16(c, stream, &drv, nullptr);
     if (drv != 0) return MHA_ERR_CUDA;
-    if (e == cudaSuccess) e = ef;
     return from_cuda(e);
 }
 
@@ -247,16 +240,16 @@ int prenorm_cross_attn_fwd(const void *x_q, const float *gamma, const float *bet
                            const void *k, const void *v, const int32_t *kv_lengths, void *out,
                            int B, int H, int Lq, int Lk, int D, float scale, int dtype,
                            cudaStream_t stream) {
-    return prenorm_with_workspace(x_q, gamma, beta, eps, k, v, kv_lengths, out, B, H, Lq, Lk, D,
-                                  scale, dtype, stream, nullptr);
+    return prenorm_fused(x_q, gamma, beta, eps, k, v, kv_lengths, out, B, H, Lq, Lk, D, scale,
+                         dtype, stream, nullptr);
 }
 
 int prenorm_cross_attn_residual_fwd(const void *x_q, const float *gamma, const float *beta,
                                     float eps, const void *k, const void *v,
                                     const int32_t *kv_lengths, void *out, int B, int H, int Lq,
                                     int Lk, int D, float scale, int dtype, cudaStream_t stream) {
-    return prenorm_with_workspace(x_q, gamma, beta, eps, k, v, kv_lengths, out, B, H, Lq, Lk, D,
-                                  scale, dtype, stream, x_q);
+    return prenorm_fused(x_q, gamma, beta, eps, k, v, kv_lengths, out, B, H, Lq, Lk, D, scale,
+                         dtype, stream, x_q);
 }
 
 int prenorm_cross_attn_fwd_noalloc(const void *x_q, const float *gamma, const float *beta,

@@ -25,8 +25,17 @@
 //                  PV0(j), S0(j+1), PV1(j), S1(j+1)
 //              so while one warpgroup runs its softmax the tensor cores work
 //              on the other query tile.
-//   warps 10-11 idle.  Warpgroup 2 (warps 8-11) hands registers to the two
-//              softmax warpgroups: 384 threads launch with 168 registers each
+//   warps 10-11 Pre-LN with D = 64: row-statistics warps.  A Pre-LN work
+//              chunk is G heads of the same 256 rows of x (consecutive items
+//              of one CTA); these warps compute the chunk's per-row mean and
+//              1/sqrt(var + eps) from the full rows of x into shared memory
+//              while the previous chunk runs, so every row's statistics are
+//              formed once per chunk, inside this kernel, with no scratch in
+//              global memory.  (At D = 128 shared memory has no room for the
+//              statistics buffer; there each softmax warp forms its own 32
+//              rows' statistics when a chunk starts.)  Otherwise idle.
+//              Warpgroup 2 (warps 8-11) hands registers to the two softmax
+//              warpgroups: 384 threads launch with 168 registers each
 //              (64512); after the split 2 x 128 x 200 + 128 x 104 = 64512,
 //              i.e. 504 per lane on each SM sub-partition (limit 512).
 // All hand-offs are mbarriers (TMA transaction counts, tcgen05.commit, thread
@@ -89,6 +98,13 @@ struct AttnParams {
     int n_pairs;          // 256-row query blocks per (b, h)
     int n_items;          // B * H * n_pairs
     int group;            // (b, h) problems per scheduling group (their K/V fit in L2)
+    int G;                // items per chunk: Pre-LN, heads sharing one 256-row block of x; else 1
+    int n_chunks;         // n_items / G
+    int n_hg;             // Pre-LN: head groups per (b, 256-row block) = H / G
+    const __nv_bfloat16 *x;   // Pre-LN: x [B][Lq][N], the rows the statistics are formed from
+    int N;                // Pre-LN: features per row of x (H * D)
+    float eps;
+    int stats_src;        // Pre-LN: 0 = statistics formed in this kernel, 1 = read from ln_stats
 };
 
 struct __align__(8) Bars {
@@ -98,6 +114,8 @@ struct __align__(8) Bars {
     uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];   // p_full, o_free: one arrival per warp
     uint64_t wg_bar[2];   // bounded barrier of each softmax warpgroup
+    uint64_t stats_full;  // Pre-LN (D = 64): a chunk's row statistics are in shared memory
+    uint64_t stats_free;  // ... and every softmax thread has taken its row's
     uint64_t drain;       // teardown after an abort
     uint32_t tmem_base;
     int abort;
@@ -116,7 +134,13 @@ struct Cfg {
     static constexpr uint32_t kStageWarp = 32 * 128;
     static constexpr uint32_t kO = kV + kStages * kTile;
     static constexpr uint32_t kBars = kO + 8 * kStageWarp;
-    static constexpr size_t kSmem = 1024 + kBars + sizeof(Bars);
+    // Pre-LN row statistics of one chunk (256 float2) after the barriers, when
+    // shared memory has room for them (D = 64; D = 128 leaves under 2 KB).
+    static constexpr bool kStatsWarps = D == 64;
+    static constexpr uint32_t kStats = kBars + ((sizeof(Bars) + 15u) & ~15u);
+    static constexpr size_t kSmemSelf = 1024 + kStats;
+    static constexpr size_t kSmemPrenorm = kSmemSelf + (kStatsWarps ? 256 * sizeof(float2) : 0);
+    static_assert(kSmemSelf <= 232448 && kSmemPrenorm <= 232448, "227 KB of shared memory per CTA");
     static constexpr uint32_t kColO0 = 256;                // O_i at 256 + i * D; S_i at i * 128
     // P_i (bf16 pairs, 64 columns): in its own columns when D = 64 leaves
     // room (384 + 64 i); for D = 128 over the first half of S_i, where the
@@ -132,22 +156,39 @@ struct Item {
     int J;        // key tiles loaded = max(n[0], n[1])
 };
 
-// Item order: groups of `group` (b, h) problems whose K/V fit in L2 together;
-// inside a group the latest (for causal masks the heaviest) 256-row query
-// blocks come first and the (b, h) index varies fastest, so CTAs running at
-// the same time share K/V tiles through L2.
+// Item order.  Self-attention: groups of `group` (b, h) problems whose K/V
+// fit in L2 together; inside a group the latest (for causal masks the
+// heaviest) 256-row query blocks come first and the (b, h) index varies
+// fastest, so CTAs running at the same time share K/V tiles through L2.
+// Pre-LN: chunk c (items c*G .. c*G + G - 1) is the head group c % n_hg of
+// 256-row block (c / n_hg) % n_pairs of batch c / (n_pairs * n_hg); its G
+// items are that block's heads in order, so one set of row statistics serves
+// the whole chunk, and the n_hg chunks of one block (which read the same rows
+// of x) run side by side on different SMs.
+template <bool PRENORM>
 __device__ __forceinline__ Item decode_item(const AttnParams &p, int item) {
     Item it;
-    const int BH = p.B * p.H;
-    const int per_group = p.group * p.n_pairs;
-    const int grp = item / per_group;
-    const int within = item - grp * per_group;
-    const int gsize = min(p.group, BH - grp * p.group);
-    const int pr = p.n_pairs - 1 - within / gsize;
-    it.bh = grp * p.group + within % gsize;
-    it.b = it.bh / p.H;
-    it.h = it.bh % p.H;
-    it.q0 = pr * 2 * kTileRows;
+    if (PRENORM) {
+        const int c = item / p.G, sub = item - c * p.G;
+        const int per_b = p.n_pairs * p.n_hg;
+        it.b = c / per_b;
+        const int rem = c - it.b * per_b;
+        const int pr = p.n_pairs - 1 - rem / p.n_hg;
+        it.h = (rem % p.n_hg) * p.G + sub;
+        it.bh = it.b * p.H + it.h;
+        it.q0 = pr * 2 * kTileRows;
+    } else {
+        const int BH = p.B * p.H;
+        const int per_group = p.group * p.n_pairs;
+        const int grp = item / per_group;
+        const int within = item - grp * per_group;
+        const int gsize = min(p.group, BH - grp * p.group);
+        const int pr = p.n_pairs - 1 - within / gsize;
+        it.bh = grp * p.group + within % gsize;
+        it.b = it.bh / p.H;
+        it.h = it.bh % p.H;
+        it.q0 = pr * 2 * kTileRows;
+    }
     int len = p.Lk;
     if (p.kv_lengths) len = max(0, min((int)p.kv_lengths[it.b], p.Lk));
     it.len = len;
@@ -186,52 +227,116 @@ __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w <<
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------------------
-// Pre-LN, step 1: per-row statistics of x [rows, N] (cms365.cn answer, step
-// two): mean and 1/sqrt(biased variance + eps), one warp per row, two passes
-// over the row (the second re-reads it from L1), fp32.
+// Pre-LN, step 1: per-row statistics of x [rows, N] ("How to fuse cross-
+// attention and layer-norm into a single CUDA kernel?" (cms365.cn), answer
+// step two): the mean and 1/sqrt(biased variance + eps), in fp32, two passes
+// over the row (the mean, then the sum of squared deviations), which avoids
+// the cancellation the page warns about.  One warp takes R rows at once (all
+// their loads in flight together).  Lane l handles the 16-byte chunks
+// c = l + 32 i in increasing i, in segments of 4 chunks per lane that stay in
+// registers between the passes when the row fits in one segment (N <= 1024);
+// the lane sums meet in an xor butterfly, after which every lane holds the
+// same bits.  Every user -- the attention kernel's statistics warps, its
+// softmax warps at D = 128, and the standalone pass of the no-allocation entry
+// point -- calls this routine, so all of them produce identical statistics.
+// A null row pointer gives unused values.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float chunk_sum8(const uint4 &u) {
+    return ((bf_lo(u.x) + bf_hi(u.x)) + (bf_lo(u.y) + bf_hi(u.y))) +
+           ((bf_lo(u.z) + bf_hi(u.z)) + (bf_lo(u.w) + bf_hi(u.w)));
+}
+
+__device__ __forceinline__ float chunk_sq8(const uint4 &u, float mean, float q) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float a = bf_lo(w[e]) - mean, b = bf_hi(w[e]) - mean;
+        q = fmaf(a, a, fmaf(b, b, q));
+    }
+    return q;
+}
+
+template <int R>
+__device__ __forceinline__ void ln_stats_warp(const __nv_bfloat16 *const (&xr)[R], int N, float eps,
+                                              int lane, float2 (&st)[R]) {
+    constexpr int kSeg = 4;                   // chunks per lane per segment
+    const int nchunk = N >> 3;                // N is a multiple of 64
+    const int nseg = (nchunk + 32 * kSeg - 1) / (32 * kSeg);
+    uint4 u[R][kSeg];
+    float s[R], q[R], mean[R];
+    auto load_seg = [&](int sg) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int i = 0; i < kSeg; ++i) {
+                const int c = lane + 32 * (sg * kSeg + i);
+                u[r][i] = (xr[r] != nullptr && c < nchunk)
+                              ? __ldg(reinterpret_cast<const uint4 *>(xr[r]) + c)
+                              : make_uint4(0u, 0u, 0u, 0u);
+            }
+    };
+#pragma unroll
+    for (int r = 0; r < R; ++r) s[r] = 0.f;
+    for (int sg = 0; sg < nseg; ++sg) {
+        load_seg(sg);
+#pragma unroll
+        for (int i = 0; i < kSeg; ++i)
+            if (lane + 32 * (sg * kSeg + i) < nchunk)
+#pragma unroll
+                for (int r = 0; r < R; ++r) s[r] += chunk_sum8(u[r][i]);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s[r] += __shfl_xor_sync(0xffffffffu, s[r], off);
+        mean[r] = s[r] / (float)N;
+        q[r] = 0.f;
+    }
+    for (int sg = 0; sg < nseg; ++sg) {
+        if (nseg > 1) load_seg(sg);
+#pragma unroll
+        for (int i = 0; i < kSeg; ++i)
+            if (lane + 32 * (sg * kSeg + i) < nchunk)
+#pragma unroll
+                for (int r = 0; r < R; ++r) q[r] = chunk_sq8(u[r][i], mean[r], q[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) q[r] += __shfl_xor_sync(0xffffffffu, q[r], off);
+        st[r] = make_float2(mean[r], rsqrtf(q[r] / (float)N + eps));
+    }
+}
+
+// The standalone statistics pass (used by the no-allocation entry point,
+// which keeps the statistics in a fixed device array): four rows per warp.
 __global__ void __launch_bounds__(256) ln_row_stats_kernel(const __nv_bfloat16 *__restrict__ x,
                                                            float2 *__restrict__ stats,
                                                            int64_t rows, int N, float eps) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int nchunk = N / 8;
-    for (int64_t r = warp; r < rows; r += nwarps) {
-        const uint4 *xr = reinterpret_cast<const uint4 *>(x + r * (int64_t)N);
-        float s = 0.f;
-        for (int c = lane; c < nchunk; c += 32) {
-            const uint4 u = __ldg(xr + c);
-            s += (bf_lo(u.x) + bf_hi(u.x)) + (bf_lo(u.y) + bf_hi(u.y)) +
-                 (bf_lo(u.z) + bf_hi(u.z)) + (bf_lo(u.w) + bf_hi(u.w));
-        }
+    for (int64_t r0 = 4 * warp; r0 < rows; r0 += 4 * nwarps) {
+        const __nv_bfloat16 *xr[4];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        const float mean = s / (float)N;
-        float q = 0.f;
-        for (int c = lane; c < nchunk; c += 32) {
-            const uint4 u = __ldg(xr + c);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        for (int r = 0; r < 4; ++r) xr[r] = r0 + r < rows ? x + (r0 + r) * (int64_t)N : nullptr;
+        float2 st[4];
+        ln_stats_warp<4>(xr, N, eps, lane, st);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float a = bf_lo(w[e]) - mean, b = bf_hi(w[e]) - mean;
-                q = fmaf(a, a, fmaf(b, b, q));
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
-        if (lane == 0) stats[r] = make_float2(mean, rsqrtf(q / (float)N + eps));
+        for (int r = 0; r < 4; ++r)
+            if (lane == r && r0 + r < rows) stats[r0 + r] = st[r];
     }
 }
 
 // Pre-LN, step 2: thread t normalises row t of a Q tile in place.  The tile
 // holds the head's D-column slice of x (loaded by TMA in the swizzled layout
-// the MMA reads); y = (x - mean) * rstd * gamma + beta, rounded to bf16.
+// the MMA reads); y = (x - mean) * rstd * gamma + beta, rounded to bf16, with
+// st = (mean, rstd) of the row.
 template <int D>
 __device__ __forceinline__ void prenorm_rows_in_place(const AttnParams &p, const Item &it,
-                                                      uint8_t *sQi, int row_in_tile, int row) {
+                                                      uint8_t *sQi, int row_in_tile, int row,
+                                                      float2 st) {
     if (row < p.Lq) {
-        const float2 st = p.ln_stats[(size_t)it.b * p.Lq + row];
         const float4 *g4 = reinterpret_cast<const float4 *>(p.gamma + it.h * D);
         const float4 *b4 = reinterpret_cast<const float4 *>(p.beta + it.h * D);
 #pragma unroll
@@ -255,6 +360,21 @@ __device__ __forceinline__ void prenorm_rows_in_place(const AttnParams &p, const
 #pragma unroll
         for (int c = 0; c < D / 8; ++c)
             *reinterpret_cast<uint4 *>(sQi + swz_off(row_in_tile, c)) = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// L2 prefetch of the rows [r0, r0 + n) of batch b of x (contiguous), in
+// pieces of at most 64 KB.
+__device__ __forceinline__ void prefetch_x_rows(const AttnParams &p, int b, int r0, int n) {
+    n = min(n, p.Lq - r0);
+    if (n <= 0) return;
+    const char *src = reinterpret_cast<const char *>(p.x + ((size_t)b * p.Lq + r0) * (size_t)p.N);
+    size_t bytes = (size_t)n * p.N * sizeof(__nv_bfloat16);
+    while (bytes > 0) {
+        const uint32_t piece = bytes > 65536 ? 65536u : (uint32_t)bytes;
+        prefetch_l2_bulk(src, piece);
+        src += piece;
+        bytes -= piece;
     }
 }
 
@@ -288,6 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NH = C::NH;
     constexpr uint32_t TILE = C::kTile;
     constexpr int S = C::kStages;
+    constexpr bool kStatsWarps = PRENORM && C::kStatsWarps;
+    const int G = PRENORM ? p.G : 1;   // items per chunk
 
     // A bounded wait that expired earlier leaves g_status set; later launches
     // then return at once instead of timing out again.
@@ -321,6 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->kv_empty[s], 1);
         }
+        mbar_init(&bars->stats_full, 64);                // every thread of warps 10-11
+        mbar_init(&bars->stats_free, 2 * kWgThreads);    // every softmax thread
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         mbar_fence_init();
@@ -367,8 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             ItemIter iter;
-            while (ok && iter.next(p.n_items)) {
-                const Item it = decode_item(p, iter.idx);
+            while (ok && iter.next(p.n_chunks))
+                for (int sub = 0; ok && sub < G; ++sub) {
+                const Item it = decode_item<PRENORM>(p, iter.idx * G + sub);
                 // The first key tiles go out before this item's Q tiles, whose
                 // buffers the previous item may still be reading.
                 const int pre = min(it.J, S);
@@ -437,8 +562,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // phase completes only at teardown).
         if (wait_limit_is_test()) ok = wwait(&bars->drain, 0, kSiteTest);
         ItemIter iter;
-        while (ok && iter.next(p.n_items)) {
-            const Item it = decode_item(p, iter.idx);
+        while (ok && iter.next(p.n_chunks))
+            for (int sub = 0; ok && sub < G; ++sub) {
+            const Item it = decode_item<PRENORM>(p, iter.idx * G + sub);
             // Every item passes through both Q barriers, with or without work
             // for the tile, so no role can run two phases ahead of another.
 #pragma unroll
@@ -535,6 +661,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++k;
         }
+    } else if (kStatsWarps) {
+        // --------------------- Pre-LN row statistics (warps 10-11) ---------------------
+        // Warp 10 + sw takes rows [128 sw, 128 sw + 128) of each chunk's 256-row
+        // block: their (mean, rstd), formed from the full rows of x, or copied
+        // from ln_stats, go to shared memory one chunk ahead of the softmax.
+        const int sw = warp - 10;
+        float2 *st_smem = reinterpret_cast<float2 *>(base + C::kStats);
+        uint32_t kc = 0;
+        bool ok = true;
+        ItemIter iter;
+        while (ok && iter.next(p.n_chunks)) {
+            const Item it = decode_item<PRENORM>(p, iter.idx * G);
+            if (kc > 0) {
+                const bool r = mbar_wait(&bars->stats_free, (kc - 1) & 1, kSiteStats, abort);
+                ok = __all_sync(0xffffffffu, r);
+                if (!ok) break;
+            }
+            const int r0 = it.q0 + 128 * sw;
+            if (p.stats_src == 0) {
+                if (lane == 0) prefetch_x_rows(p, it.b, r0, 128);
+                for (int rr = 0; rr < 128; rr += 2) {
+                    const __nv_bfloat16 *xr[2];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int row = r0 + rr + r;
+                        xr[r] = row < p.Lq ? p.x + ((size_t)it.b * p.Lq + row) * (size_t)p.N : nullptr;
+                    }
+                    float2 st[2];
+                    ln_stats_warp<2>(xr, p.N, p.eps, lane, st);
+                    if (lane < 2) st_smem[128 * sw + rr + lane] = lane == 0 ? st[0] : st[1];
+                }
+            } else {
+                for (int rr = lane; rr < 128; rr += 32) {
+                    const int row = r0 + rr;
+                    st_smem[128 * sw + rr] = row < p.Lq ? p.ln_stats[(size_t)it.b * p.Lq + row]
+                                                        : make_float2(0.f, 0.f);
+                }
+            }
+            mbar_arrive(&bars->stats_full);
+            ++kc;
+        }
     }
     // ------------------------------- teardown --------------------------------
     // Every softmax thread has arrived on barrier 1 once it is done with TMEM.
@@ -582,17 +749,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++wgp;
             return r;
         };
+        // Pre-LN: this thread's row statistics, taken when a chunk starts (the
+        // chunk's G items share the rows).
+        float2 st_row = make_float2(0.f, 0.f);
+        uint32_t kc = 0;
+        const float2 *st_smem = reinterpret_cast<const float2 *>(base + C::kStats);
         ItemIter iter;
-        while (ok && iter.next(p.n_items)) {
-            const Item it = decode_item(p, iter.idx);
+        while (ok && iter.next(p.n_chunks))
+            for (int sub = 0; ok && sub < G; ++sub) {
+            const Item it = decode_item<PRENORM>(p, iter.idx * G + sub);
             const int n = wg ? it.n[1] : it.n[0];
             const int q0i = it.q0 + wg * kTileRows;
             const int row = q0i + t;
+            if (PRENORM && sub == 0) {
+                if (kStatsWarps) {
+                    // Formed (or copied) by warps 10-11 one chunk ahead.
+                    ok = wwait(&bars->stats_full, kc & 1, kSiteStats);
+                    if (!ok) break;
+                    st_row = st_smem[wg * kTileRows + t];
+                    mbar_arrive(&bars->stats_free);
+                    ++kc;
+                } else if (p.stats_src == 1) {
+                    st_row = row < p.Lq ? p.ln_stats[(size_t)it.b * p.Lq + row]
+                                        : make_float2(0.f, 0.f);
+                } else {
+                    // No room for a shared buffer (D = 128): this warp forms its
+                    // own 32 rows' statistics, two rows at a time.
+                    const int rw = q0i + 32 * (warp & 3);
+                    if (lane == 0) prefetch_x_rows(p, it.b, rw, 32);
+#pragma unroll 1
+                    for (int rr = 0; rr < 32; rr += 2) {
+                        const __nv_bfloat16 *xr[2];
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const int rx = rw + rr + r;
+                            xr[r] = rx < p.Lq ? p.x + ((size_t)it.b * p.Lq + rx) * (size_t)p.N : nullptr;
+                        }
+                        float2 st[2];
+                        ln_stats_warp<2>(xr, p.N, p.eps, lane, st);
+                        if (lane == rr) st_row = st[0];
+                        if (lane == rr + 1) st_row = st[1];
+                    }
+                }
+            }
             ok = wwait(&bars->q_raw[wg], k & 1, kSiteQFull);
             if (!ok) break;
             if (PRENORM) {
                 if (n > 0) {
-                    prenorm_rows_in_place<D>(p, it, sQi, t, row);
+                    prenorm_rows_in_place<D>(p, it, sQi, t, row, st_row);
                     fence_proxy_async_smem();
                 }
                 if (!(ok = wg_sync())) break;
@@ -957,12 +1161,12 @@ thread_local int g_grid_override = 0;
 
 template <int D, bool PRENORM>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
-    constexpr size_t smem = Cfg<D>::kSmem;
+    constexpr size_t smem = PRENORM ? Cfg<D>::kSmemPrenorm : Cfg<D>::kSmemSelf;
     cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_fwd_bf16_kernel<D, PRENORM>), smem);
     if (e != cudaSuccess) return e;
     // Persistent grid: one CTA per SM (one fits per SM), unless overridden.
     int grid = g_grid_override > 0 ? g_grid_override : device_info().sms;
-    if (grid > p.n_items) grid = p.n_items;
+    if (grid > p.n_chunks) grid = p.n_chunks;
     attn_fwd_bf16_kernel<D, PRENORM><<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
@@ -1010,9 +1214,10 @@ cudaError_t noalloc_ln_stats(int64_t rows, float2 **ptr) {
 
 cudaError_t launch_ln_row_stats(const void *x, float2 *stats, int64_t rows, int N, float eps,
                                 cudaStream_t stream) {
-    const int64_t warps = (rows + 0) > 0 ? rows : 1;
+    const int64_t warps = rows > 0 ? (rows + 3) / 4 : 1;   // four rows per warp
     int64_t blocks = (warps + 7) / 8;
-    if (blocks > 152 * 32) blocks = 152 * 32;
+    const int64_t cap = 32ll * device_info().sms;
+    if (blocks > cap) blocks = cap;
     ln_row_stats_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16 *>(x), stats, rows, N, eps);
     return cudaGetLastError();
@@ -1064,6 +1269,25 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     p.scale_log2 = c.scale * 1.4426950408889634f;
     p.n_pairs = (c.Lq + 2 * kTileRows - 1) / (2 * kTileRows);
     p.n_items = (int)(BH * (uint64_t)p.n_pairs);
+    p.G = 1;
+    if (prenorm) {
+        // Heads per chunk: the largest divisor of H that still leaves at least
+        // six chunks per SM for the persistent schedule to balance; each chunk
+        // forms its rows' statistics once for its G heads.
+        const int64_t blocks = (int64_t)c.B * p.n_pairs;
+        const int64_t want = 6ll * (g_grid_override > 0 ? g_grid_override : device_info().sms);
+        for (int g = c.H; g >= 1; --g)
+            if (c.H % g == 0 && (blocks * (c.H / g) >= want || g == 1)) {
+                p.G = g;
+                break;
+            }
+        p.n_hg = c.H / p.G;
+        p.x = reinterpret_cast<const __nv_bfloat16 *>(c.x);
+        p.N = c.H * c.D;
+        p.eps = c.eps;
+        p.stats_src = ln_stats != nullptr ? 1 : 0;
+    }
+    p.n_chunks = p.n_items / p.G;
     {
         // (b, h) problems per scheduling group: their K and V together take
         // at most half of L2.
@@ -1074,9 +1298,14 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
         p.group = (int)grp;
     }
     if (prenorm) {
-        cudaError_t e = launch_ln_row_stats(c.x, ln_stats, (int64_t)c.B * c.Lq, c.H * c.D, c.eps,
-                                            stream);
-        if (e != cudaSuccess) return e;
+        // Statistics kept in caller-visible scratch (the no-allocation entry
+        // point's fixed array) come from the standalone pass; otherwise the
+        // attention kernel forms them itself.
+        if (ln_stats != nullptr) {
+            cudaError_t e = launch_ln_row_stats(c.x, ln_stats, (int64_t)c.B * c.Lq, c.H * c.D, c.eps,
+                                                stream);
+            if (e != cudaSuccess) return e;
+        }
         return c.D == 64 ? launch_attn<64, true>(p, stream) : launch_attn<128, true>(p, stream);
     }
     return c.D == 64 ? launch_attn<64, false>(p, stream) : launch_attn<128, false>(p, stream);

@@ -91,8 +91,10 @@ struct Bf16Call {
 };
 
 // Returns cudaSuccess or the first CUDA error; *driver_err receives a
-// nonzero CUresult when tensor-map encoding failed.  For the Pre-LN variant
-// `ln_stats` is device scratch of B*Lq float2 (row mean, 1/sqrt(var + eps)).
+// nonzero CUresult when tensor-map encoding failed.  Pre-LN variant: with
+// `ln_stats` null the attention kernel forms every row's (mean,
+// 1/sqrt(var + eps)) itself (one launch, no scratch); otherwise `ln_stats` is
+// device scratch of B*Lq float2 that a standalone pass fills first.
 cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_err,
                             float2 *ln_stats);
 

@@ -161,6 +161,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16, at a 16-byte aligned address)
+// of global memory into L2; nothing is written to shared memory.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *gptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gptr)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // 3-D tiled store of one box from shared memory (rows outside the tensor are
 // clipped by the unit).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int c0,

@@ -59,6 +59,51 @@ def test_prenorm_c4_sampled_rows():
     print(w.name, r)
 
 
+@pytest.mark.gpu
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_prenorm_chunks_of_heads_share_row_statistics(D, ctas):
+    """A capped grid makes the kernel group several heads of the same 256 rows
+    into one chunk (1 CTA: all 4 heads; 2 CTAs: pairs of heads), whose row
+    statistics are formed once -- by warps 10-11 into shared memory at D = 64,
+    by the softmax warps at D = 128 -- and walk many chunks per CTA, with
+    empty and ragged batches.  The result must not depend on the grouping."""
+    B, H, Lq, Lk = 3, 4, 300, 260
+    lens = [260, 0, 131]
+    x, g, b, k, v = _inputs(B, H, Lq, Lk, D, 31)
+    args = (dev(x), dev(g), dev(b), 1e-5, dev(k), dev(v), dev(lens_tensor(lens)))
+    ref = mha.prenorm_cross_attn_fwd(*args)
+    ref_r = mha.prenorm_cross_attn_residual_fwd(*args)
+    try:
+        mha.set_bf16_grid(ctas)
+        for _ in range(5):
+            out = mha.prenorm_cross_attn_fwd(*args)
+            out_r = mha.prenorm_cross_attn_residual_fwd(*args)
+            torch.cuda.synchronize()
+            assert mha.device_status() == 0
+            assert torch.equal(out, ref)
+            assert torch.equal(out_r, ref_r)
+    finally:
+        mha.set_bf16_grid(0)
+    want = oracle.prenorm_cross_attn(x.float().numpy(), g.numpy(), b.numpy(), 1e-5,
+                                     k.float().numpy(), v.float().numpy(), lens)
+    check_bf16(as_np(out), want, "chunks D=%d ctas=%d" % (D, ctas))
+
+
+@pytest.mark.gpu
+def test_prenorm_wide_rows_take_several_segments():
+    """Rows of 16 x 128 = 2048 features: the statistics routine runs two
+    segments per row and re-reads x for the second pass."""
+    B, H, Lq, Lk, D = 1, 16, 130, 70, 128
+    x, g, b, k, v = _inputs(B, H, Lq, Lk, D, 33)
+    out = mha.prenorm_cross_attn_fwd(dev(x), dev(g), dev(b), 1e-5, dev(k), dev(v), None)
+    torch.cuda.synchronize()
+    want = oracle.prenorm_cross_attn(x.float().numpy(), g.numpy(), b.numpy(), 1e-5,
+                                     k.float().numpy(), v.float().numpy(), None)
+    check_bf16(as_np(out), want, "wide rows")
+    assert mha.device_status() == 0
+
+
 def _c4():
     w = synthetic.WORKLOADS["c4_prenorm_bf16"]
     return w, synthetic.make(w, seed=0)

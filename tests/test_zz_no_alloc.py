@@ -71,6 +71,30 @@ def test_noalloc_matches_allocating_entry_point_on_two_calls():
 
 
 @pytest.mark.gpu
+def test_noalloc_matches_on_a_capped_grid():
+    """On one CTA the kernel groups all four heads of a row block into one
+    chunk; the no-allocation call (statistics copied from the fixed array)
+    still returns the same bits as prenorm_cross_attn_fwd (statistics formed
+    inside the attention kernel)."""
+    fn = _bind()
+    stream = torch.cuda.current_stream()
+    B, H, Lq, Lk, D = 3, 4, 300, 260, 64
+    x, g, b, k, v, lens = _inputs(B, H, Lq, Lk, D, 90)
+    try:
+        mha.set_bf16_grid(1)
+        ref = mha.prenorm_cross_attn_fwd(x, g, b, 1e-5, k, v, lens, scale=0.125)
+        out = torch.full_like(ref, float("nan"))
+        rc = fn(_p(x), _p(g), _p(b), 1e-5, _p(k), _p(v), _p(lens), _p(out), B, H, Lq, Lk, D,
+                0.125, 1, ctypes.c_void_p(stream.cuda_stream))
+        assert rc == 0, mha.mha_strerror(rc)
+        torch.cuda.synchronize()
+    finally:
+        mha.set_bf16_grid(0)
+    assert torch.equal(out, ref)
+    assert mha.device_status() == 0
+
+
+@pytest.mark.gpu
 def test_noalloc_refuses_problems_beyond_its_scratch():
     fn = _bind()
     fake = ctypes.c_void_p(0x10000)
