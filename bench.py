@@ -40,7 +40,7 @@ DEFAULT_L2 = 129 * 1024 * 1024
 KERNEL_OF = {  # dominant kernel of each workload
     "mha:f32": "mha_fwd_f32_kernel",      # D = 128; D = 64 runs attn_fwd_tf32x3_kernel
     "mha:bf16": "attn_fwd_bf16_kernel",
-    "prenorm:bf16": "attn_fwd_bf16_kernel<prenorm>",
+    "prenorm:bf16": "attn_fwd_bf16_kernel<prenorm>",   # one launch: statistics formed inside
     "prenorm_residual:bf16": "attn_fwd_bf16_kernel<prenorm>",
     "mha_bwd:f32": "mha_bwd_f32_kernel",
     "mha_bwd:bf16": "attn_bwd_bf16_kernel",   # tensor cores: key- and query-stationary kernels
@@ -127,9 +127,19 @@ def fp32_alu_peak_tflops(n_sm, mhz):
     return n_sm * 128 * 2 * mhz * 1e6 / 1e12
 
 
+def source_hash(paths):
+    """First 16 hex digits of the SHA-256 of the files' contents, in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel_key):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    on the current kernel source (the kernel's translation unit and the
+    device primitives it includes); else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -137,10 +147,8 @@ def traffic_record(kernel_key):
         rec = json.load(open(path)).get(kernel_key)
         if not rec:
             return None
-        src = os.path.join(ROOT, rec["source"])
-        import hashlib
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return rec if h == rec["source_sha256_16"] else None
+        srcs = rec.get("sources") or [rec["source"]]
+        return rec if source_hash(srcs) == rec["source_sha256_16"] else None
     except Exception:
         return None
 

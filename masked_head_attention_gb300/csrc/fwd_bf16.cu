@@ -25,19 +25,15 @@
 //                  PV0(j), S0(j+1), PV1(j), S1(j+1)
 //              so while one warpgroup runs its softmax the tensor cores work
 //              on the other query tile.
-//   warps 10-11 Pre-LN with D = 64: row-statistics warps.  A Pre-LN work
-//              chunk is G heads of the same 256 rows of x (consecutive items
-//              of one CTA); these warps compute the chunk's per-row mean and
-//              1/sqrt(var + eps) from the full rows of x into shared memory
-//              while the previous chunk runs, so every row's statistics are
-//              formed once per chunk, inside this kernel, with no scratch in
-//              global memory.  (At D = 128 shared memory has no room for the
-//              statistics buffer; there each softmax warp forms its own 32
-//              rows' statistics when a chunk starts.)  Otherwise idle.
-//              Warpgroup 2 (warps 8-11) hands registers to the two softmax
-//              warpgroups: 384 threads launch with 168 registers each
+//   warps 10-11 idle.  Warpgroup 2 (warps 8-11) hands registers to the two
+//              softmax warpgroups: 384 threads launch with 168 registers each
 //              (64512); after the split 2 x 128 x 200 + 128 x 104 = 64512,
 //              i.e. 504 per lane on each SM sub-partition (limit 512).
+// Pre-LN: a work chunk is G consecutive items of one CTA, the heads of one
+// 256-row block of x; when a chunk starts, each softmax warp forms its 32 rows'
+// mean and 1/sqrt(var + eps) from the full rows of x (in fp32, inside this
+// kernel: no scratch in global memory), keeps them in registers for the G
+// items and prefetches the next chunk's rows into L2.
 // All hand-offs are mbarriers (TMA transaction counts, tcgen05.commit, thread
 // arrivals); every wait is bounded.
 //
@@ -79,6 +75,14 @@ constexpr int kMaxStages = 3;
 // it by more than this many powers of two (P stays <= 256).  Exact after the
 // final O / l.
 constexpr float kRescaleThreshold = 8.0f;
+// Self-attention items are scheduled in groups of (b, h) problems whose K
+// and V together fill at most this fraction (1 / kL2GroupDenom) of L2.
+// (Quarter and eighth groups read less from DRAM on the long causal shape,
+// 820 and 678 MB against 840 MB, but ran 12% and 9% slower.)
+constexpr int kL2GroupDenom = 2;
+// Pre-LN row statistics: rows a softmax warp takes at once (all their loads
+// in flight together) at the chunk starts inside its item loop.
+constexpr int kStatsRows = 2;
 
 struct AttnParams {
     CUtensorMap tm_q;     // Q [B*H][Lq][D]; Pre-LN: x [B][Lq][H*D]; box {64, 128, 1}
@@ -114,8 +118,6 @@ struct __align__(8) Bars {
     uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];   // p_full, o_free: one arrival per warp
     uint64_t wg_bar[2];   // bounded barrier of each softmax warpgroup
-    uint64_t stats_full;  // Pre-LN (D = 64): a chunk's row statistics are in shared memory
-    uint64_t stats_free;  // ... and every softmax thread has taken its row's
     uint64_t drain;       // teardown after an abort
     uint32_t tmem_base;
     int abort;
@@ -134,13 +136,8 @@ struct Cfg {
     static constexpr uint32_t kStageWarp = 32 * 128;
     static constexpr uint32_t kO = kV + kStages * kTile;
     static constexpr uint32_t kBars = kO + 8 * kStageWarp;
-    // Pre-LN row statistics of one chunk (256 float2) after the barriers, when
-    // shared memory has room for them (D = 64; D = 128 leaves under 2 KB).
-    static constexpr bool kStatsWarps = D == 64;
-    static constexpr uint32_t kStats = kBars + ((sizeof(Bars) + 15u) & ~15u);
-    static constexpr size_t kSmemSelf = 1024 + kStats;
-    static constexpr size_t kSmemPrenorm = kSmemSelf + (kStatsWarps ? 256 * sizeof(float2) : 0);
-    static_assert(kSmemSelf <= 232448 && kSmemPrenorm <= 232448, "227 KB of shared memory per CTA");
+    static constexpr size_t kSmem = 1024 + kBars + sizeof(Bars);
+    static_assert(kSmem <= 232448, "227 KB of shared memory per CTA");
     static constexpr uint32_t kColO0 = 256;                // O_i at 256 + i * D; S_i at i * 128
     // P_i (bf16 pairs, 64 columns): in its own columns when D = 64 leaves
     // room (384 + 64 i); for D = 128 over the first half of S_i, where the
@@ -235,23 +232,30 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 // their loads in flight together).  Lane l handles the 16-byte chunks
 // c = l + 32 i in increasing i, in segments of 4 chunks per lane that stay in
 // registers between the passes when the row fits in one segment (N <= 1024);
-// the lane sums meet in an xor butterfly, after which every lane holds the
-// same bits.  Every user -- the attention kernel's statistics warps, its
-// softmax warps at D = 128, and the standalone pass of the no-allocation entry
-// point -- calls this routine, so all of them produce identical statistics.
-// A null row pointer gives unused values.
+// it keeps two partial sums (the even and the odd elements) on packed fp32x2
+// instructions, adds them, and the lane sums meet in an xor butterfly, after
+// which every lane holds the same bits.  Both users -- the attention kernel's
+// softmax warps and the standalone pass of the no-allocation entry point --
+// call this routine, so they produce identical statistics.  A null row
+// pointer gives unused values.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float chunk_sum8(const uint4 &u) {
-    return ((bf_lo(u.x) + bf_hi(u.x)) + (bf_lo(u.y) + bf_hi(u.y))) +
-           ((bf_lo(u.z) + bf_hi(u.z)) + (bf_lo(u.w) + bf_hi(u.w)));
+// Lane sums of one 16-byte chunk (eight bf16) on packed fp32x2 instructions:
+// the pair (element 2k, element 2k + 1) of word k goes into the two halves
+// of a running float2.
+__device__ __forceinline__ float2 chunk_sum8(const uint4 &u, float2 acc) {
+    acc = __fadd2_rn(acc, make_float2(bf_lo(u.x), bf_hi(u.x)));
+    acc = __fadd2_rn(acc, make_float2(bf_lo(u.y), bf_hi(u.y)));
+    acc = __fadd2_rn(acc, make_float2(bf_lo(u.z), bf_hi(u.z)));
+    acc = __fadd2_rn(acc, make_float2(bf_lo(u.w), bf_hi(u.w)));
+    return acc;
 }
 
-__device__ __forceinline__ float chunk_sq8(const uint4 &u, float mean, float q) {
+__device__ __forceinline__ float2 chunk_sq8(const uint4 &u, float2 nm, float2 q) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float a = bf_lo(w[e]) - mean, b = bf_hi(w[e]) - mean;
-        q = fmaf(a, a, fmaf(b, b, q));
+        const float2 d = __fadd2_rn(make_float2(bf_lo(w[e]), bf_hi(w[e])), nm);
+        q = __ffma2_rn(d, d, q);
     }
     return q;
 }
@@ -263,7 +267,8 @@ __device__ __forceinline__ void ln_stats_warp(const __nv_bfloat16 *const (&xr)[R
     const int nchunk = N >> 3;                // N is a multiple of 64
     const int nseg = (nchunk + 32 * kSeg - 1) / (32 * kSeg);
     uint4 u[R][kSeg];
-    float s[R], q[R], mean[R];
+    float2 acc[R];
+    float mean[R];
     auto load_seg = [&](int sg) {
 #pragma unroll
         for (int r = 0; r < R; ++r)
@@ -276,21 +281,22 @@ __device__ __forceinline__ void ln_stats_warp(const __nv_bfloat16 *const (&xr)[R
             }
     };
 #pragma unroll
-    for (int r = 0; r < R; ++r) s[r] = 0.f;
+    for (int r = 0; r < R; ++r) acc[r] = make_float2(0.f, 0.f);
     for (int sg = 0; sg < nseg; ++sg) {
         load_seg(sg);
 #pragma unroll
         for (int i = 0; i < kSeg; ++i)
             if (lane + 32 * (sg * kSeg + i) < nchunk)
 #pragma unroll
-                for (int r = 0; r < R; ++r) s[r] += chunk_sum8(u[r][i]);
+                for (int r = 0; r < R; ++r) acc[r] = chunk_sum8(u[r][i], acc[r]);
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
+        float s = acc[r].x + acc[r].y;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s[r] += __shfl_xor_sync(0xffffffffu, s[r], off);
-        mean[r] = s[r] / (float)N;
-        q[r] = 0.f;
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        mean[r] = s / (float)N;
+        acc[r] = make_float2(0.f, 0.f);
     }
     for (int sg = 0; sg < nseg; ++sg) {
         if (nseg > 1) load_seg(sg);
@@ -298,13 +304,15 @@ __device__ __forceinline__ void ln_stats_warp(const __nv_bfloat16 *const (&xr)[R
         for (int i = 0; i < kSeg; ++i)
             if (lane + 32 * (sg * kSeg + i) < nchunk)
 #pragma unroll
-                for (int r = 0; r < R; ++r) q[r] = chunk_sq8(u[r][i], mean[r], q[r]);
+                for (int r = 0; r < R; ++r)
+                    acc[r] = chunk_sq8(u[r][i], make_float2(-mean[r], -mean[r]), acc[r]);
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
+        float q = acc[r].x + acc[r].y;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) q[r] += __shfl_xor_sync(0xffffffffu, q[r], off);
-        st[r] = make_float2(mean[r], rsqrtf(q[r] / (float)N + eps));
+        for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
+        st[r] = make_float2(mean[r], rsqrtf(q / (float)N + eps));
     }
 }
 
@@ -378,6 +386,31 @@ __device__ __forceinline__ void prefetch_x_rows(const AttnParams &p, int b, int 
     }
 }
 
+// Statistics of the 32 rows [rw, rw + 32) of batch b, R rows at a time; lane
+// l returns row rw + l's.
+// (The kernel is compiled at its launch bound of 168 registers a thread for
+// every role, so inside the softmax warps' item loop only two rows at a time
+// fit without spilling; the first chunk, before that loop, takes eight.)
+template <int R>
+__device__ __forceinline__ float2 warp_rows_stats(const AttnParams &p, int b, int rw, int lane) {
+    float2 mine = make_float2(0.f, 0.f);
+#pragma unroll 1
+    for (int rr = 0; rr < 32; rr += R) {
+        const __nv_bfloat16 *xr[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int rx = rw + rr + r;
+            xr[r] = rx < p.Lq ? p.x + ((size_t)b * p.Lq + rx) * (size_t)p.N : nullptr;
+        }
+        float2 st[R];
+        ln_stats_warp<R>(xr, p.N, p.eps, lane, st);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (lane == rr + r) mine = st[r];
+    }
+    return mine;
+}
+
 // ---------------------------------------------------------------------------
 // The attention kernel.  CTA c takes items c, c + grid, c + 2*grid, ...; every
 // barrier phase runs on counters that continue across items:
@@ -408,7 +441,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NH = C::NH;
     constexpr uint32_t TILE = C::kTile;
     constexpr int S = C::kStages;
-    constexpr bool kStatsWarps = PRENORM && C::kStatsWarps;
     const int G = PRENORM ? p.G : 1;   // items per chunk
 
     // A bounded wait that expired earlier leaves g_status set; later launches
@@ -443,8 +475,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->kv_empty[s], 1);
         }
-        mbar_init(&bars->stats_full, 64);                // every thread of warps 10-11
-        mbar_init(&bars->stats_free, 2 * kWgThreads);    // every softmax thread
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         mbar_fence_init();
@@ -661,47 +691,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++k;
         }
-    } else if (kStatsWarps) {
-        // --------------------- Pre-LN row statistics (warps 10-11) ---------------------
-        // Warp 10 + sw takes rows [128 sw, 128 sw + 128) of each chunk's 256-row
-        // block: their (mean, rstd), formed from the full rows of x, or copied
-        // from ln_stats, go to shared memory one chunk ahead of the softmax.
-        const int sw = warp - 10;
-        float2 *st_smem = reinterpret_cast<float2 *>(base + C::kStats);
-        uint32_t kc = 0;
-        bool ok = true;
-        ItemIter iter;
-        while (ok && iter.next(p.n_chunks)) {
-            const Item it = decode_item<PRENORM>(p, iter.idx * G);
-            if (kc > 0) {
-                const bool r = mbar_wait(&bars->stats_free, (kc - 1) & 1, kSiteStats, abort);
-                ok = __all_sync(0xffffffffu, r);
-                if (!ok) break;
-            }
-            const int r0 = it.q0 + 128 * sw;
-            if (p.stats_src == 0) {
-                if (lane == 0) prefetch_x_rows(p, it.b, r0, 128);
-                for (int rr = 0; rr < 128; rr += 2) {
-                    const __nv_bfloat16 *xr[2];
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const int row = r0 + rr + r;
-                        xr[r] = row < p.Lq ? p.x + ((size_t)it.b * p.Lq + row) * (size_t)p.N : nullptr;
-                    }
-                    float2 st[2];
-                    ln_stats_warp<2>(xr, p.N, p.eps, lane, st);
-                    if (lane < 2) st_smem[128 * sw + rr + lane] = lane == 0 ? st[0] : st[1];
-                }
-            } else {
-                for (int rr = lane; rr < 128; rr += 32) {
-                    const int row = r0 + rr;
-                    st_smem[128 * sw + rr] = row < p.Lq ? p.ln_stats[(size_t)it.b * p.Lq + row]
-                                                        : make_float2(0.f, 0.f);
-                }
-            }
-            mbar_arrive(&bars->stats_full);
-            ++kc;
-        }
     }
     // ------------------------------- teardown --------------------------------
     // Every softmax thread has arrived on barrier 1 once it is done with TMEM.
@@ -749,11 +738,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++wgp;
             return r;
         };
-        // Pre-LN: this thread's row statistics, taken when a chunk starts (the
+        // Pre-LN: this thread's row statistics, formed when a chunk starts (the
         // chunk's G items share the rows).
         float2 st_row = make_float2(0.f, 0.f);
-        uint32_t kc = 0;
-        const float2 *st_smem = reinterpret_cast<const float2 *>(base + C::kStats);
         ItemIter iter;
         while (ok && iter.next(p.n_chunks))
             for (int sub = 0; ok && sub < G; ++sub) {
@@ -762,33 +749,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q0i = it.q0 + wg * kTileRows;
             const int row = q0i + t;
             if (PRENORM && sub == 0) {
-                if (kStatsWarps) {
-                    // Formed (or copied) by warps 10-11 one chunk ahead.
-                    ok = wwait(&bars->stats_full, kc & 1, kSiteStats);
-                    if (!ok) break;
-                    st_row = st_smem[wg * kTileRows + t];
-                    mbar_arrive(&bars->stats_free);
-                    ++kc;
-                } else if (p.stats_src == 1) {
+                if (p.stats_src == 1) {
                     st_row = row < p.Lq ? p.ln_stats[(size_t)it.b * p.Lq + row]
                                         : make_float2(0.f, 0.f);
                 } else {
-                    // No room for a shared buffer (D = 128): this warp forms its
-                    // own 32 rows' statistics, two rows at a time.
+                    // This warp's 32 rows, eight at a time; then the next
+                    // chunk's rows go to L2, ready when that chunk starts.
                     const int rw = q0i + 32 * (warp & 3);
-                    if (lane == 0) prefetch_x_rows(p, it.b, rw, 32);
-#pragma unroll 1
-                    for (int rr = 0; rr < 32; rr += 2) {
-                        const __nv_bfloat16 *xr[2];
-#pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            const int rx = rw + rr + r;
-                            xr[r] = rx < p.Lq ? p.x + ((size_t)it.b * p.Lq + rx) * (size_t)p.N : nullptr;
-                        }
-                        float2 st[2];
-                        ln_stats_warp<2>(xr, p.N, p.eps, lane, st);
-                        if (lane == rr) st_row = st[0];
-                        if (lane == rr + 1) st_row = st[1];
+                    st_row = warp_rows_stats<kStatsRows>(p, it.b, rw, lane);
+                    ItemIter peek = iter;
+                    if (lane == 0 && peek.next(p.n_chunks)) {
+                        const Item nx = decode_item<PRENORM>(p, peek.idx * G);
+                        prefetch_x_rows(p, nx.b, nx.q0 + wg * kTileRows + 32 * (warp & 3), 32);
                     }
                 }
             }
@@ -1161,7 +1133,7 @@ thread_local int g_grid_override = 0;
 
 template <int D, bool PRENORM>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
-    constexpr size_t smem = PRENORM ? Cfg<D>::kSmemPrenorm : Cfg<D>::kSmemSelf;
+    constexpr size_t smem = Cfg<D>::kSmem;
     cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_fwd_bf16_kernel<D, PRENORM>), smem);
     if (e != cudaSuccess) return e;
     // Persistent grid: one CTA per SM (one fits per SM), unless overridden.
@@ -1290,9 +1262,9 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     p.n_chunks = p.n_items / p.G;
     {
         // (b, h) problems per scheduling group: their K and V together take
-        // at most half of L2.
+        // at most 1/kL2GroupDenom of L2.
         const uint64_t kv_bytes = 4ull * (uint64_t)(c.Lk > 0 ? c.Lk : 1) * c.D;
-        uint64_t grp = (uint64_t)device_info().l2 / 2 / kv_bytes;
+        uint64_t grp = (uint64_t)device_info().l2 / kL2GroupDenom / kv_bytes;
         if (grp < 1) grp = 1;
         if (grp > BH) grp = BH;
         p.group = (int)grp;
