@@ -1243,16 +1243,24 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     p.n_items = (int)(BH * (uint64_t)p.n_pairs);
     p.G = 1;
     if (prenorm) {
-        // Heads per chunk: the largest divisor of H that still leaves at least
-        // six chunks per SM for the persistent schedule to balance; each chunk
-        // forms its rows' statistics once for its G heads.
-        const int64_t blocks = (int64_t)c.B * p.n_pairs;
-        const int64_t want = 6ll * (g_grid_override > 0 ? g_grid_override : device_info().sms);
-        for (int g = c.H; g >= 1; --g)
-            if (c.H % g == 0 && (blocks * (c.H / g) >= want || g == 1)) {
+        // Heads per chunk: a chunk forms its rows' statistics once for its G
+        // items, at a cost of about N/Lk items' worth of work (N features per
+        // row of x against Lk keys per row of attention), while larger chunks
+        // leave a longer tail (about G/2 items) when the persistent grid runs
+        // out of chunks.  Take the divisor of H that minimises
+        //     items per CTA * (1 + (N / Lk) / G) + G / 2.
+        const int grid = g_grid_override > 0 ? g_grid_override : device_info().sms;
+        const double per_cta = (double)p.n_items / (double)grid;
+        const double stats = (double)(c.H * c.D) / (double)(c.Lk > 0 ? c.Lk : 1);
+        double best = 0.0;
+        for (int g = 1; g <= c.H; ++g) {
+            if (c.H % g != 0) continue;
+            const double cost = per_cta * (1.0 + stats / g) + 0.5 * g;
+            if (g == 1 || cost < best) {
+                best = cost;
                 p.G = g;
-                break;
             }
+        }
         p.n_hg = c.H / p.G;
         p.x = reinterpret_cast<const __nv_bfloat16 *>(c.x);
         p.N = c.H * c.D;

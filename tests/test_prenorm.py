@@ -64,10 +64,10 @@ def test_prenorm_c4_sampled_rows():
 @pytest.mark.parametrize("ctas", [1, 2])
 def test_prenorm_chunks_of_heads_share_row_statistics(D, ctas):
     """A capped grid makes the kernel group several heads of the same 256 rows
-    into one chunk (1 CTA: all 4 heads; 2 CTAs: pairs of heads), whose row
-    statistics are formed once -- by warps 10-11 into shared memory at D = 64,
-    by the softmax warps at D = 128 -- and walk many chunks per CTA, with
-    empty and ragged batches.  The result must not depend on the grouping."""
+    into one chunk (the default grid runs one head per chunk at this size),
+    whose row statistics the softmax warps form once, and walk many chunks per
+    CTA, with empty and ragged batches.  The result must not depend on the
+    grouping."""
     B, H, Lq, Lk = 3, 4, 300, 260
     lens = [260, 0, 131]
     x, g, b, k, v = _inputs(B, H, Lq, Lk, D, 31)
