@@ -241,10 +241,18 @@ MHA_API int prenorm_cross_attn_fwd_noalloc(const void *x_q, const float *gamma,
 MHA_API const char *mha_strerror(int status);
 
 /*
- * mha_device_status -- read (and optionally clear) the device status word
- * that kernels set when a bounded wait expires.  Bit k set means wait site
- * k timed out (site numbers are listed in the kernel sources).  Synchronous:
- * copies from the current device.  Returns MHA_OK or MHA_ERR_CUDA.
+ * mha_device_status -- read (and optionally clear) the device status words
+ * the kernels set; *bits receives their union.
+ *   Bits 0-15: a bounded wait expired at wait site k (site numbers are
+ *   listed in the kernel sources).  The kernel returned without finishing,
+ *   and later launches of the same kernel family return at once, without
+ *   writing their outputs, until the bit is cleared.
+ *   Bit 16: a forward row with visible keys ended with a softmax sum that
+ *   is not positive and finite ("softmax sum != 1 is an error", cms365.cn
+ *   answer, closing notes); bit 17: a forward output element is not finite.
+ *   Both arise only from non-finite inputs; they do not stop later launches.
+ * Synchronous: copies from the current device.  Returns MHA_OK or
+ * MHA_ERR_CUDA.
  */
 MHA_API int mha_device_status(uint32_t *bits, int clear);
 

@@ -69,11 +69,12 @@ MHA_API void mha_set_bwd_kernel(int which);
 /*
  * mha_test_set_device_status -- OR `bits` into the device status word of
  * kernel unit `unit` on the current device (0 = bf16 forward, 1 = fp32
- * tensor-core forward, 2 = bf16 tensor-core backward), as an expired wait
- * would.  Lets a test check that mha_device_status reports and clears every
- * unit's word.  While a unit's word is non-zero its kernels return at once
- * without writing their outputs.  Returns MHA_OK, MHA_ERR_INVALID_ARG for an
- * unknown unit, or MHA_ERR_CUDA.
+ * tensor-core forward, 2 = bf16 tensor-core backward, 3 = bf16 decode), as
+ * an expired wait or a numeric flag would.  Lets a test check that
+ * mha_device_status reports and clears every unit's word.  While a unit's
+ * wait bits (0-15) are set its kernels return at once without writing their
+ * outputs.  Returns MHA_OK, MHA_ERR_INVALID_ARG for an unknown unit, or
+ * MHA_ERR_CUDA.
  */
 MHA_API int mha_test_set_device_status(int unit, uint32_t bits);
 

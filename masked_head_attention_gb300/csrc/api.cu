@@ -22,6 +22,7 @@ cudaError_t status_ctl(int unit, int op, uint64_t value, uint32_t *bits) {
         case 0: return mha::status_ctl_fwd_bf16(op, value, bits);
         case 1: return mha::status_ctl_fwd_tf32(op, value, bits);
         case 2: return mha::status_ctl_bwd_bf16(op, value, bits);
+        case 3: return mha::status_ctl_decode_bf16(op, value, bits);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -150,7 +150,7 @@ __device__ __forceinline__ void bwd_tile(const BwdBf16Params &p, int tr, int n_t
     constexpr int NS = kStagesB;
     constexpr int SW = bwd_soft_warps<D>();
     constexpr int kProdWarpB = SW, kMmaWarpB = SW + 1;
-    if (*reinterpret_cast<volatile unsigned int *>(&g_status) != 0u) return;
+    if (wait_expired_before()) return;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;

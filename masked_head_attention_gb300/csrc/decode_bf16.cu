@@ -253,6 +253,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         // A row that saw no visible key is written as zeros.
         const float inv = ll > 0.f ? 1.f / ll : 0.f;
+        // Its sum is 0 with no visible key and at least 1 otherwise, unless an
+        // input was not finite.
+        bool nonfinite = false;
+#pragma unroll
+        for (int c = 0; c < DC; ++c) nonfinite |= !finite_f(oc[c] * inv);
+        report_flag(!finite_f(ll), kFlagSum);
+        report_flag(nonfinite, kFlagNonFinite);
         if (lse != nullptr && lane == 0)
             lse[(size_t)bh * Lq + r] =
                 (ll > 0.f && mm != -INFINITY) ? 0.69314718055994531f * (mm + log2f(ll)) : -INFINITY;
@@ -299,6 +306,10 @@ cudaError_t launch_dec_rows(const Bf16Call &c, int splits, int chunk, cudaStream
 }
 
 }  // namespace
+
+cudaError_t status_ctl_decode_bf16(int op, uint64_t value, uint32_t *bits) {
+    return unit_status_ctl(op, value, bits);
+}
 
 void set_decode_override(int which) { g_decode_override = which; }
 void set_decode_splits(int splits) { g_decode_splits = splits; }

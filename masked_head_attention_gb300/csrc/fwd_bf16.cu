@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // A bounded wait that expired earlier leaves g_status set; later launches
     // then return at once instead of timing out again.
-    if (*reinterpret_cast<volatile unsigned int *>(&g_status) != 0u) return;
+    if (wait_expired_before()) return;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -863,6 +863,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
+                // A row with visible keys has l >= 1 (its largest weight is
+                // 2^(max - m_used) >= 1) unless an input was not finite.
+                report_flag(row < p.Lq && vis_end > 0 && !(l > 0.f && finite_f(l)), kFlagSum);
+                bool nonfinite = false;
                 const int row0 = q0i + 32 * (warp & 3);   // first row of this warp's slice
 #pragma unroll
                 for (int hh = 0; hh < NH; ++hh) {
@@ -900,6 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             f[6] += bf_lo(u.w);
                             f[7] += bf_hi(u.w);
                         }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) nonfinite |= !finite_f(f[q]);
                         uint4 w;
                         w.x = pack_bf16x2(f[0], f[1]);
                         w.y = pack_bf16x2(f[2], f[3]);
@@ -917,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_store_commit();
                     }
                 }
+                report_flag(row < p.Lq && nonfinite, kFlagNonFinite);
             } else if (row < p.Lq) {
                 // No visible key: the attention rows are zeros (the residual
                 // variant writes x's slice unchanged).

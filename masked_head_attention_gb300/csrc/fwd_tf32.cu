@@ -202,7 +202,7 @@ __device__ __forceinline__ float row_lse2(float m2, float l) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tf32x3_kernel(const __grid_constant__ Tf32Params p) {
-    if (*reinterpret_cast<volatile unsigned int *>(&g_status) != 0u) return;
+    if (wait_expired_before()) return;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -521,15 +521,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto store_rows = [&](const Item &it, const uint32_t (&o)[64], float inv) {
             if (lane == 0) tma_store_wait_read();   // the previous store has read the staging
             __syncwarp();
+            bool nonfinite = false;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     const int e = hh * 32 + ch * 4;
-                    *reinterpret_cast<float4 *>(stg + hh * kOBox + box_off(lane, ch * 4)) =
+                    const float4 v4 =
                         make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
                                     __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                    nonfinite |= !(finite_f(v4.x) && finite_f(v4.y) && finite_f(v4.z) && finite_f(v4.w));
+                    *reinterpret_cast<float4 *>(stg + hh * kOBox + box_off(lane, ch * 4)) = v4;
                 }
+            report_flag(nonfinite && it.q0 + warp * 32 + lane < p.Lq, kFlagNonFinite);
             fence_proxy_async_smem();
             __syncwarp();
             const int r0 = it.q0 + warp * 32;
@@ -637,6 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->o_free);
             const float inv = l > 0.f ? 1.f / l : 0.f;
+            // The sum is 0 for a row with no visible key and at least 1
+            // otherwise, unless an input was not finite.
+            report_flag(row < p.Lq && !finite_f(l), kFlagSum);
             store_rows(it, o, inv);
             if (p.lse && row < p.Lq) p.lse[(size_t)it.bh * p.Lq + row] = row_lse2(m, l);
             g += it.n;

@@ -116,15 +116,17 @@ cudaError_t launch_selftest_umma(int variant, int K_or_N, const void *a, const v
 constexpr int64_t kNoAllocMaxRows = 262144;
 cudaError_t noalloc_ln_stats(int64_t rows, float2 **ptr);
 
-// Device status word and wait limit of each unit with bounded waits
-// (fwd_bf16.cu, fwd_tf32.cu, bwd_bf16.cu; each keeps its own):
+// Device status word and wait limit of each unit with bounded waits or
+// numeric flags (fwd_bf16.cu, fwd_tf32.cu, bwd_bf16.cu, decode_bf16.cu; each
+// keeps its own):
 //   op 0: *bits = the word, cleared afterwards when value != 0;
 //   op 1: OR `value` into the word;
 //   op 2: wait limit = `value` ns (0 restores the default of 2 s).
 cudaError_t status_ctl_fwd_bf16(int op, uint64_t value, uint32_t *bits);
 cudaError_t status_ctl_fwd_tf32(int op, uint64_t value, uint32_t *bits);
 cudaError_t status_ctl_bwd_bf16(int op, uint64_t value, uint32_t *bits);
-constexpr int kStatusUnits = 3;
+cudaError_t status_ctl_decode_bf16(int op, uint64_t value, uint32_t *bits);
+constexpr int kStatusUnits = 4;
 
 // Launch-configuration overrides used by tests and benchmark sweeps (0 = default).
 void set_bf16_grid_override(int ctas);

@@ -29,6 +29,29 @@ enum WaitSite : uint32_t {
     kSiteStats = 12, kSiteTest = 13,
 };
 
+// Numeric flags, bits 16 and up of the same word ("softmax sum != 1 is an
+// error", in the cms365.cn answer's closing notes): a row with visible keys
+// whose softmax sum came out non-positive or non-finite, and an output
+// element that is not finite.  Both arise only from non-finite inputs.
+// Unlike the wait bits they do not make later launches return at once.
+enum NumericFlag : uint32_t { kFlagSum = 16, kFlagNonFinite = 17 };
+constexpr unsigned int kWaitBits = 0xFFFFu;
+
+__device__ __forceinline__ bool finite_f(float x) { return fabsf(x) <= 3.4028234663852886e38f; }
+
+// Whole warp (warp-uniform control flow): if any lane has `bad` set, one of
+// them ORs bit `flag` into the status word.
+__device__ __forceinline__ void report_flag(bool bad, uint32_t flag) {
+    const unsigned int m = __ballot_sync(0xffffffffu, bad);
+    if (m != 0u && (int)(threadIdx.x & 31) == __ffs(m) - 1) atomicOr(&g_status, 1u << flag);
+}
+
+// True when an earlier bounded wait of this unit expired (the kernels then
+// return at once).
+__device__ __forceinline__ bool wait_expired_before() {
+    return (*reinterpret_cast<volatile unsigned int *>(&g_status) & kWaitBits) != 0u;
+}
+
 // Wall-clock limit for one wait.  Healthy waits last microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

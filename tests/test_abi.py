@@ -182,7 +182,7 @@ def test_hooks_are_thread_local(L):
 
 
 def test_status_hook_rejects_unknown_unit(L):
-    assert L.mha_test_set_device_status(3, 1) == INVALID
+    assert L.mha_test_set_device_status(4, 1) == INVALID
     assert L.mha_test_set_device_status(-1, 1) == INVALID
 
 

@@ -16,7 +16,9 @@ import masked_head_attention_gb300 as mha
 import oracle
 from parity_util import as_np, check_bf16, check_f32, dev, randn
 
-UNITS = {0: "bf16 forward", 1: "fp32 tensor-core forward", 2: "bf16 tensor-core backward"}
+UNITS = {0: "bf16 forward", 1: "fp32 tensor-core forward", 2: "bf16 tensor-core backward",
+         3: "bf16 decode"}
+FLAG_SUM, FLAG_NONFINITE = 1 << 16, 1 << 17
 
 
 @pytest.mark.gpu
@@ -109,3 +111,39 @@ def test_expired_wait_sets_status_and_the_next_call_recovers(name):
     assert mha.device_status() == 0
     assert torch.equal(out, ref)    # these kernels are deterministic
     check(out)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", ["bf16", "tf32x3", "decode"])
+def test_non_finite_input_raises_numeric_flags_without_stopping_later_calls(kind):
+    """The pages call a softmax sum other than one an error: a NaN in one query
+    row makes that row's sum and output non-finite, which the kernels report
+    as status bits 16 and 17; those bits do not stop later launches, and the
+    other rows are unaffected."""
+    dtype = torch.float32 if kind == "tf32x3" else torch.bfloat16
+    Lq = 1 if kind == "decode" else 200
+    D = 64 if kind == "tf32x3" else 128
+    q = randn((2, 2, Lq, D), 91, 1.0, dtype)
+    k = randn((2, 2, 300, D), 92, 1.0, dtype)
+    v = randn((2, 2, 300, D), 93, 1.0, dtype)
+    assert mha.device_status(clear=True) == 0
+    clean = mha.mha_fwd(dev(q), dev(k), dev(v), 0)
+    torch.cuda.synchronize()
+    assert mha.device_status() == 0
+    bad = q.clone()
+    bad[1, 0, Lq - 1, 3] = float("nan")
+    out = mha.mha_fwd(dev(bad), dev(k), dev(v), 0)
+    torch.cuda.synchronize()
+    bits = mha.device_status(clear=True)
+    assert bits & FLAG_NONFINITE, hex(bits)
+    assert bits & FLAG_SUM, hex(bits)
+    assert bits & 0xFFFF == 0, hex(bits)          # no wait expired
+    o = out.cpu()
+    assert not torch.isfinite(o[1, 0, Lq - 1]).any()
+    keep = torch.ones(o.shape[:3], dtype=torch.bool)
+    keep[1, 0, Lq - 1] = False
+    assert torch.equal(o[keep], clean.cpu()[keep])   # every other row as before
+    again = mha.mha_fwd(dev(q), dev(k), dev(v), 0)
+    torch.cuda.synchronize()
+    assert torch.equal(again, clean)
+    assert mha.device_status() == 0
