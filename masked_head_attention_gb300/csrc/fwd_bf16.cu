@@ -866,7 +866,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // A row with visible keys has l >= 1 (its largest weight is
                 // 2^(max - m_used) >= 1) unless an input was not finite.
                 report_flag(row < p.Lq && vis_end > 0 && !(l > 0.f && finite_f(l)), kFlagSum);
-                bool nonfinite = false;
+                // The row's elements are summed on the side: a NaN or infinite
+                // element makes the sum non-finite (|O| <= max |V| + |x|).
+                float2 rsum = make_float2(0.f, 0.f);
                 const int row0 = q0i + 32 * (warp & 3);   // first row of this warp's slice
 #pragma unroll
                 for (int hh = 0; hh < NH; ++hh) {
@@ -905,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             f[7] += bf_hi(u.w);
                         }
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) nonfinite |= !finite_f(f[q]);
+                        for (int q = 0; q < 8; q += 2) rsum = __fadd2_rn(rsum, make_float2(f[q], f[q + 1]));
                         uint4 w;
                         w.x = pack_bf16x2(f[0], f[1]);
                         w.y = pack_bf16x2(f[2], f[3]);
@@ -923,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_store_commit();
                     }
                 }
-                report_flag(row < p.Lq && nonfinite, kFlagNonFinite);
+                report_flag(row < p.Lq && !finite_f(rsum.x + rsum.y), kFlagNonFinite);
             } else if (row < p.Lq) {
                 // No visible key: the attention rows are zeros (the residual
                 // variant writes x's slice unchanged).

@@ -521,7 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto store_rows = [&](const Item &it, const uint32_t (&o)[64], float inv) {
             if (lane == 0) tma_store_wait_read();   // the previous store has read the staging
             __syncwarp();
-            bool nonfinite = false;
+            // The row's elements are summed on the side: a NaN or infinite
+            // element makes the sum non-finite (|O| <= max |V|, so finite rows
+            // cannot overflow it).
+            float2 rsum = make_float2(0.f, 0.f);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
@@ -530,10 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float4 v4 =
                         make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
                                     __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                    nonfinite |= !(finite_f(v4.x) && finite_f(v4.y) && finite_f(v4.z) && finite_f(v4.w));
+                    rsum = __fadd2_rn(rsum, __fadd2_rn(make_float2(v4.x, v4.y), make_float2(v4.z, v4.w)));
                     *reinterpret_cast<float4 *>(stg + hh * kOBox + box_off(lane, ch * 4)) = v4;
                 }
-            report_flag(nonfinite && it.q0 + warp * 32 + lane < p.Lq, kFlagNonFinite);
+            report_flag(!finite_f(rsum.x + rsum.y) && it.q0 + warp * 32 + lane < p.Lq, kFlagNonFinite);
             fence_proxy_async_smem();
             __syncwarp();
             const int r0 = it.q0 + warp * 32;
