@@ -24,6 +24,10 @@ CASES = [
     (3, 1, 129, 129, 128, 2, [200, -5, 64]),
     (4, 2, 190, 190, 64, 3, [1, 63, 64, 190]),
     (2, 2, 256, 256, 128, 3, [129, 256]),
+    # the short-key kernel's chunk ring: 8 chunks of 32 keys, ragged rows
+    (2, 2, 300, 256, 64, 1, None),
+    (1, 3, 47, 250, 64, 2, [250, 33, 0]),
+    (3, 2, 128, 128, 128, 3, [128, 97, 5]),
 ]
 
 
