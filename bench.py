@@ -53,16 +53,8 @@ TF32X3_D = 64              # fp32 inputs with this head dimension run on the ten
 TF32_OVER_BF16 = 1.1 / 2.25
 
 
-SMALL_F32_AUTO_WORK = 1 << 22   # D = 64: B*H*Lq*Lk at most this (and short keys) -> CUDA cores
-
-
-def small_f32_problem(w):
-    return w.Lk * w.D <= SMALL_F32_MAX_KD and w.B * w.H * w.Lq * w.Lk <= SMALL_F32_AUTO_WORK
-
-
 def uses_tf32x3(w):
-    return (w.kind == "mha" and w.dtype == "f32" and w.D == TF32X3_D
-            and not small_f32_problem(w))
+    return w.kind == "mha" and w.dtype == "f32" and w.D == TF32X3_D
 
 
 def kernel_of(w):

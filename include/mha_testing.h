@@ -33,14 +33,12 @@ MHA_API void mha_set_bf16_grid(int ctas);
 /*
  * mha_set_f32_kernel -- fp32 kernel choice.  0 = automatic: for D = 64 the
  * tensor-core kernel (three TF32 MMAs per product: hi*hi + lo*hi + hi*lo of
- * the operands split as x = hi + lo, fp32 accumulation in TMEM), except for
- * small problems (Lk*D <= 16384 and B*H*Lq*Lk <= 2^22), which run the
- * CUDA-core short-key-range kernel (16-row query blocks, K/V streamed in
- * 32-key chunks); for D = 128 the CUDA-core kernels: the short-key-range
- * kernel when Lk*D <= 16384, else the tiled kernel (64-row query tiles,
- * 64-key K/V tiles).  1 = always the tiled CUDA-core kernel; 2 = the
- * short-key-range kernel whenever Lk*D <= 16384, else the tiled one; 3 = the
- * tensor-core kernel whenever D = 64.  Other values act as 0.
+ * the operands split as x = hi + lo, fp32 accumulation in TMEM); for D = 128
+ * the CUDA-core kernels: the short-key-range kernel (every visible K/V row of
+ * a 16-row query block staged in shared memory at once) when Lk*D <= 16384,
+ * else the tiled kernel (64-row query tiles, 64-key K/V tiles).  1 = always
+ * the tiled CUDA-core kernel; 2 = the short-key-range kernel whenever
+ * Lk*D <= 16384, else the tiled one; 3 = as 0.  Other values act as 0.
  */
 MHA_API void mha_set_f32_kernel(int which);
 

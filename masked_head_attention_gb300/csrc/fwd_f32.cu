@@ -246,36 +246,21 @@ __global__ void __launch_bounds__(kThreads)
 // Many small CTAs, latest (heaviest under a causal mask) query blocks first,
 // replace a few long serial ones when B * H * Lq is small.
 // ---------------------------------------------------------------------------
-// Short key ranges (Lk * D <= 16384, e.g. L = 128 at D = 64): a launch of
-// many small CTAs with the shortest critical path.  CTA = 16 query rows of
-// one (b, h): eight warps of two rows.  K and V stream through shared memory
-// in chunks of 32 keys on a two-stage cp.async ring, so the first chunk's
-// work starts after one load latency and later chunks land while earlier
-// ones are used; chunks past the keys any of the CTA's rows can see are never
-// loaded.  Per chunk a lane takes one key for S (the query rows broadcast from
-// shared memory, its K row read with 16-byte loads from rows padded to D + 4
-// floats: conflict-free), the warp runs the online softmax of each row by
-// shuffles (running max, rescaled running sum, base-2 exponent), and for P.V
-// the lane takes D/32 output columns with each key's weight broadcast by a
-// shuffle.  The latest (for a causal mask the heaviest) query blocks launch
-// first.
-// ---------------------------------------------------------------------------
-constexpr int kSmallRows = 16;                        // query rows per CTA
-constexpr int kSmallWarps = 8;
-constexpr int kSmallR = kSmallRows / kSmallWarps;     // query rows per warp
+constexpr int kSmallRows = 16;
+constexpr int kSmallR = 4;                               // query rows per warp (2 or 4)
+constexpr int kSmallWarps = kSmallRows / kSmallR;
 constexpr int kSmallThreads = 32 * kSmallWarps;
-constexpr int kSmallChunk = 32;                       // keys per chunk (one per lane)
-constexpr int kSmallMaxKD = 16384;                    // Lk * D limit of this kernel
-// Automatic choice for D = 64: this kernel below this many (row, key) pairs
-// (B * H * Lq * Lk), the tensor-core kernel above.
-constexpr int64_t kSmallAutoWork = 1ll << 22;
+constexpr int kSmallMaxKD = 16384;   // Lk * D limit (K and V: 2 x 64 KB + padding)
 
 template <int D>
 struct SmallCfg {
-    static constexpr int LDK = D + 4;                        // padded K row (floats)
-    static constexpr int kKChunk = kSmallChunk * LDK;        // floats per K stage
-    static constexpr int kVChunk = kSmallChunk * D;          // floats per V stage
-    static constexpr size_t kSmem = sizeof(float) * ((size_t)kSmallRows * D + 2 * (kKChunk + kVChunk));
+    static constexpr int LDK = D + 4;                 // padded K row (conflict-free 16-byte loads)
+    static constexpr int kMaxKeys = kSmallMaxKD / D;  // 256 (D = 64) or 128 (D = 128)
+    static constexpr int KB = kMaxKeys / 32;          // key blocks of 32 per lane
+    static size_t smem(int keys) {
+        return sizeof(float) * ((size_t)keys * LDK + (size_t)keys * D + kSmallRows * D +
+                                (size_t)kSmallWarps * keys * kSmallR);
+    }
 };
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
@@ -290,21 +275,82 @@ __device__ __forceinline__ void cp_async_wait_group() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Q.K for the warp's R query rows against keys kb*32 + lane, kb < NKB.
+template <int D, int NKB, int KB>
+__device__ __forceinline__ void small_scores(const float *sK, const float *Qw, int lane,
+                                             float (&s)[kSmallR][KB]) {
+    constexpr int LDK = SmallCfg<D>::LDK;
+#pragma unroll 2
+    for (int d = 0; d < D; d += 4) {
+        float4 qq[kSmallR];
+#pragma unroll
+        for (int r = 0; r < kSmallR; ++r) qq[r] = *reinterpret_cast<const float4 *>(Qw + r * D + d);
+#pragma unroll
+        for (int kb = 0; kb < NKB; ++kb) {
+            const float4 kk = *reinterpret_cast<const float4 *>(sK + (kb * 32 + lane) * LDK + d);
+#pragma unroll
+            for (int r = 0; r < kSmallR; ++r) {
+                s[r][kb] = fmaf(qq[r].x, kk.x, s[r][kb]);
+                s[r][kb] = fmaf(qq[r].y, kk.y, s[r][kb]);
+                s[r][kb] = fmaf(qq[r].z, kk.z, s[r][kb]);
+                s[r][kb] = fmaf(qq[r].w, kk.w, s[r][kb]);
+            }
+        }
+    }
+}
+
+// acc[r][c] += P[key][r] * V[key][lane*DC + c] for the warp's rows.
 template <int D>
-__global__ void __launch_bounds__(kSmallThreads)
+__device__ __forceinline__ void small_pv_key(const float *Pw, const float *Vl, int key,
+                                             float (&acc)[kSmallR][D / 32]) {
+    constexpr int DC = D / 32;
+    static_assert(kSmallR == 2 || kSmallR == 4, "P is read as one float2 / float4 per key");
+    float pp[kSmallR];
+    if (kSmallR == 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(Pw + key * kSmallR);
+        pp[0] = t.x;
+        pp[1] = t.y;
+        pp[kSmallR - 2] = t.z;
+        pp[kSmallR - 1] = t.w;
+    } else {
+        const float2 t = *reinterpret_cast<const float2 *>(Pw + key * kSmallR);
+        pp[0] = t.x;
+        pp[1] = t.y;
+    }
+    float vv[DC];
+    if (DC == 2) {
+        const float2 t = *reinterpret_cast<const float2 *>(Vl + (size_t)key * D);
+        vv[0] = t.x;
+        vv[1] = t.y;
+    } else {
+        const float4 t = *reinterpret_cast<const float4 *>(Vl + (size_t)key * D);
+        vv[0] = t.x;
+        vv[1] = t.y;
+        vv[DC - 2] = t.z;
+        vv[DC - 1] = t.w;
+    }
+#pragma unroll
+    for (int c = 0; c < DC; ++c)
+#pragma unroll
+        for (int r = 0; r < kSmallR; ++r) acc[r][c] = fmaf(pp[r], vv[c], acc[r][c]);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kSmallThreads, 2)
     mha_fwd_f32_small_kernel(const float *__restrict__ q, const float *__restrict__ k,
                              const float *__restrict__ v, const int32_t *__restrict__ kv_lengths,
                              float *__restrict__ out, float *__restrict__ lse, int H, int Lq,
-                             int Lk, int mask_kind, float scale_log2) {
+                             int Lk, int mask_kind, float scale_log2, int keys_cap) {
     using C = SmallCfg<D>;
     constexpr int DC = D / 32;   // output columns per lane
     constexpr int R = kSmallR;
-    constexpr int V4 = D / 4;
     extern __shared__ float4 small_smem[];
-    float *sQ = reinterpret_cast<float *>(small_smem);   // [16][D]
-    float *sK = sQ + kSmallRows * D;                      // [2][32][LDK]
-    float *sV = sK + 2 * C::kKChunk;                      // [2][32][D]
+    float *sK = reinterpret_cast<float *>(small_smem);   // [keys_cap][LDK]
+    float *sV = sK + (size_t)keys_cap * C::LDK;          // [keys_cap][D]
+    float *sQ = sV + (size_t)keys_cap * D;               // [16][D]
+    float *sP = sQ + kSmallRows * D;                     // [warps][keys_cap][R]
 
+    // Latest (for causal masks the heaviest) query blocks are launched first.
     const int h = blockIdx.y, b = blockIdx.z;
     const int q0 = ((int)gridDim.x - 1 - (int)blockIdx.x) * kSmallRows;
     const size_t bh = (size_t)b * H + h;
@@ -319,143 +365,142 @@ __global__ void __launch_bounds__(kSmallThreads)
     if (mask_kind & 2) len = max(0, min((int)kv_lengths[b], Lk));
     int kend = len;                                   // keys any row of the CTA can see
     if (causal) kend = min(kend, q0 + kSmallRows);
-    kend = max(kend, 0);
-    const int nch = (kend + kSmallChunk - 1) / kSmallChunk;
 
-    // Chunk c into stage c & 1; keys at or past kend are zero (finite, and
-    // their weights are exactly 0).
-    auto load_chunk = [&](int c) {
-        float *dK = sK + (c & 1) * C::kKChunk;
-        float *dV = sV + (c & 1) * C::kVChunk;
-        for (int idx = tid; idx < kSmallChunk * V4; idx += kSmallThreads) {
-            const int r = idx / V4, cc = idx % V4;
-            const int key = c * kSmallChunk + r;
-            if (key < kend) {
-                cp_async16(dK + r * C::LDK + 4 * cc, Kg + (size_t)key * D + 4 * cc);
-                cp_async16(dV + r * D + 4 * cc, Vg + (size_t)key * D + 4 * cc);
-            } else {
-                *reinterpret_cast<float4 *>(dK + r * C::LDK + 4 * cc) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4 *>(dV + r * D + 4 * cc) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        cp_async_commit();
-    };
-    for (int idx = tid; idx < kSmallRows * V4; idx += kSmallThreads) {
-        const int r = idx / V4, cc = idx % V4;
-        if (q0 + r < Lq)
-            cp_async16(sQ + r * D + 4 * cc, Qg + (size_t)(q0 + r) * D + 4 * cc);
-        else
-            *reinterpret_cast<float4 *>(sQ + r * D + 4 * cc) = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int V4 = D / 4;
+    for (int idx = tid; idx < kend * V4; idx += kSmallThreads) {
+        const int r = idx / V4, c = idx % V4;
+        cp_async16(sK + r * C::LDK + 4 * c, Kg + (size_t)r * D + 4 * c);
     }
-    if (nch > 0) load_chunk(0);   // the Q copies join the first group
-    else cp_async_commit();
-    if (nch > 1) load_chunk(1);
+    cp_async_commit();
+    for (int idx = tid; idx < kend * V4; idx += kSmallThreads) {
+        const int r = idx / V4, c = idx % V4;
+        cp_async16(sV + r * D + 4 * c, Vg + (size_t)r * D + 4 * c);
+    }
+    cp_async_commit();
+    for (int idx = tid; idx < kSmallRows * V4; idx += kSmallThreads) {
+        const int r = idx / V4, c = idx % V4;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (q0 + r < Lq) val = __ldg(reinterpret_cast<const float4 *>(Qg + (size_t)(q0 + r) * D) + c);
+        *reinterpret_cast<float4 *>(sQ + r * D + 4 * c) = val;
+    }
+    cp_async_wait_group<1>();   // K has landed (V may still be in flight)
+    __syncthreads();
 
+    const int r0 = q0 + R * warp;                    // first row of this warp
+    int kw = len;                                    // keys any of the warp's rows can see
+    if (causal) kw = min(kw, r0 + R);
+    kw = max(kw, 0);
+    const int nkb = (kw + 31) / 32;
     const float *Qw = sQ + R * warp * D;
-    int vis_end[R];
-    float m[R], l[R], o[R][DC];
+
+    // S for the warp's rows and keys kb*32 + lane.
+    float s[R][C::KB];
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+        for (int r = 0; r < R; ++r) s[r][kb] = 0.f;
+    switch (nkb) {
+#define MHA_SMALL_S_CASE(N)                                                              \
+    case N:                                                                              \
+        if (N <= C::KB) small_scores<D, (N <= C::KB ? N : 1), C::KB>(sK, Qw, lane, s);   \
+        break;
+        MHA_SMALL_S_CASE(1)
+        MHA_SMALL_S_CASE(2)
+        MHA_SMALL_S_CASE(3)
+        MHA_SMALL_S_CASE(4)
+        MHA_SMALL_S_CASE(5)
+        MHA_SMALL_S_CASE(6)
+        MHA_SMALL_S_CASE(7)
+        MHA_SMALL_S_CASE(8)
+#undef MHA_SMALL_S_CASE
+        default:
+            break;
+    }
+    // Mask, scale into base 2, row max / exp / row sum (warp shuffles).
+    float l[R], mrow[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        const int row = q0 + R * warp + r;
-        vis_end[r] = causal ? min(len, row + 1) : len;
-        m[r] = -INFINITY;
-        l[r] = 0.f;
+        const int row = r0 + r;
+        const int vis_end = causal ? min(len, row + 1) : len;
+        float mx = -INFINITY;
 #pragma unroll
-        for (int cc = 0; cc < DC; ++cc) o[r][cc] = 0.f;
+        for (int kb = 0; kb < C::KB; ++kb) {
+            const int key = kb * 32 + lane;
+            const float x = (kb < nkb && key < vis_end) ? s[r][kb] * scale_log2 : -INFINITY;
+            s[r][kb] = x;
+            mx = fmaxf(mx, x);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m = (mx == -INFINITY) ? 0.f : mx;
+        float sum = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb) {
+            const float pj = ex2_approx(s[r][kb] - m);
+            s[r][kb] = pj;
+            sum += pj;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        l[r] = sum;
+        mrow[r] = mx;
     }
-    for (int c = 0; c < nch; ++c) {
-        if (c + 1 < nch)
-            cp_async_wait_group<1>();
-        else
-            cp_async_wait_group<0>();
-        __syncthreads();
-        // S for the warp's rows and key c * 32 + lane.
-        const float *Kl = sK + (c & 1) * C::kKChunk + lane * C::LDK;
-        float sc[R];
+    if (lse != nullptr && lane < R && r0 + lane < Lq) {
+        float mm = mrow[0], ll = l[0];
 #pragma unroll
-        for (int r = 0; r < R; ++r) sc[r] = 0.f;
-#pragma unroll 8
-        for (int d = 0; d < D; d += 4) {
-            const float4 kk = *reinterpret_cast<const float4 *>(Kl + d);
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float4 qq = *reinterpret_cast<const float4 *>(Qw + r * D + d);
-                sc[r] = fmaf(qq.x, kk.x, sc[r]);
-                sc[r] = fmaf(qq.y, kk.y, sc[r]);
-                sc[r] = fmaf(qq.z, kk.z, sc[r]);
-                sc[r] = fmaf(qq.w, kk.w, sc[r]);
+        for (int r = 1; r < R; ++r)
+            if (lane == r) {
+                mm = mrow[r];
+                ll = l[r];
             }
-        }
-        // Mask, base-2 logits, online softmax per row (warp shuffles).
-        const int key = c * kSmallChunk + lane;
-        float p[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float x = key < vis_end[r] ? sc[r] * scale_log2 : -INFINITY;
-            float cm = x;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-            const float m_new = fmaxf(m[r], cm);
-            const float msub = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2_approx(m[r] - msub);
-            p[r] = ex2_approx(x - msub);
-            float ps = p[r];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-            l[r] = fmaf(l[r], alpha, ps);
-            m[r] = m_new;
-#pragma unroll
-            for (int cc = 0; cc < DC; ++cc) o[r][cc] *= alpha;
-        }
-        // O += P V: the lane's D/32 columns, each key's weight by shuffle.
-        const float *Vl = sV + (c & 1) * C::kVChunk + lane * DC;
-#pragma unroll 8
-        for (int j = 0; j < kSmallChunk; ++j) {
-            float vv[DC];
-            if (DC == 2) {
-                const float2 t = *reinterpret_cast<const float2 *>(Vl + j * D);
-                vv[0] = t.x;
-                vv[DC - 1] = t.y;
-            } else {
-                const float4 t = *reinterpret_cast<const float4 *>(Vl + j * D);
-                vv[0] = t.x;
-                vv[1] = t.y;
-                vv[DC - 2] = t.z;
-                vv[DC - 1] = t.w;
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float pj = __shfl_sync(0xffffffffu, p[r], j);
-#pragma unroll
-                for (int cc = 0; cc < DC; ++cc) o[r][cc] = fmaf(pj, vv[cc], o[r][cc]);
-            }
-        }
-        __syncthreads();   // every warp is done with stage c & 1
-        if (c + 2 < nch) load_chunk(c + 2);
+        lse[bh * (size_t)Lq + r0 + lane] = row_lse(mm, ll);
     }
-    if (nch == 0) cp_async_wait_group<0>();
+    float *Pw = sP + (size_t)warp * keys_cap * R;
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb)
+        if (kb < nkb)
+        {
+            float *dst = Pw + (kb * 32 + lane) * R;
+            if (R == 4)
+                *reinterpret_cast<float4 *>(dst) =
+                    make_float4(s[0][kb], s[1][kb], s[R - 2][kb], s[R - 1][kb]);
+            else
+                *reinterpret_cast<float2 *>(dst) = make_float2(s[0][kb], s[1][kb]);
+        }
+    cp_async_wait_group<0>();   // V has landed
+    __syncthreads();
+
+    // O = P V for the warp's rows, lane's columns lane*DC .. lane*DC + DC - 1;
+    // even and odd keys go to separate accumulators (two chains per output).
+    float o[2][R][DC];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < DC; ++c) o[h2][r][c] = 0.f;
+    const float *Vl = sV + lane * DC;
+    int key = 0;
+#pragma unroll 4
+    for (; key + 1 < kw; key += 2) {
+        small_pv_key<D>(Pw, Vl, key, o[0]);
+        small_pv_key<D>(Pw, Vl, key + 1, o[1]);
+    }
+    if (key < kw) small_pv_key<D>(Pw, Vl, key, o[0]);
     // O / l; a row that saw no visible key (l == 0) is written as zeros.
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        const int row = q0 + R * warp + r;
-        const bool live = row < Lq;
+        const int row = r0 + r;
+        if (row >= Lq) continue;
         const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
-        report_flag(live && !finite_f(l[r]), kFlagSum);
-        float res[DC];
-        float rsum = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < DC; ++cc) {
-            res[cc] = o[r][cc] * inv;
-            rsum += res[cc];
-        }
-        report_flag(live && !finite_f(rsum), kFlagNonFinite);
-        if (!live) continue;
         float *dst = Og + (size_t)row * D + lane * DC;
+        float res[DC];
+#pragma unroll
+        for (int c = 0; c < DC; ++c) res[c] = (o[0][r][c] + o[1][r][c]) * inv;
         if (DC == 2)
-            *reinterpret_cast<float2 *>(dst) = make_float2(res[0], res[DC - 1]);
+            *reinterpret_cast<float2 *>(dst) = make_float2(res[0], res[1]);
         else
             *reinterpret_cast<float4 *>(dst) = make_float4(res[0], res[1], res[DC - 2], res[DC - 1]);
-        if (lse != nullptr && lane == 0) lse[bh * (size_t)Lq + row] = row_lse(m[r], l[r]);
     }
 }
 
@@ -463,12 +508,14 @@ template <int D>
 cudaError_t launch_small(const float *q, const float *k, const float *v, const int32_t *kv,
                          float *out, float *lse, int B, int H, int Lq, int Lk, int mask_kind, float scale,
                          cudaStream_t stream) {
-    constexpr size_t smem = SmallCfg<D>::kSmem;
-    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(mha_fwd_f32_small_kernel<D>), smem);
+    using C = SmallCfg<D>;
+    const int keys_cap = ((Lk + 31) / 32) * 32;
+    const size_t smem = C::smem(keys_cap);
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(mha_fwd_f32_small_kernel<D>), C::smem(C::kMaxKeys));
     if (e != cudaSuccess) return e;
     const dim3 grid((Lq + kSmallRows - 1) / kSmallRows, H, B);
     mha_fwd_f32_small_kernel<D><<<grid, kSmallThreads, smem, stream>>>(
-        q, k, v, kv, out, lse, H, Lq, Lk, mask_kind, scale * 1.4426950408889634f);
+        q, k, v, kv, out, lse, H, Lq, Lk, mask_kind, scale * 1.4426950408889634f, keys_cap);
     return cudaGetLastError();
 }
 
@@ -500,15 +547,10 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v,
                            cudaStream_t stream, int *driver_err) {
     *driver_err = 0;
     const int which = (g_f32_kernel >= 1 && g_f32_kernel <= 3) ? g_f32_kernel : 0;
-    // Small problems with short key ranges are latency-bound: the CUDA-core
-    // short-key kernel's many small CTAs finish sooner than the tensor-core
-    // kernel's 128-row items.
-    const bool short_keys = (int64_t)Lk * D <= kSmallMaxKD;
-    const bool small_problem = short_keys && (int64_t)B * H * Lq * Lk <= kSmallAutoWork;
-    if ((which == 3 || (which == 0 && !small_problem)) && tf32x3_applies(D))
+    if ((which == 0 || which == 3) && tf32x3_applies(D))
         return launch_fwd_tf32x3(q, k, v, kv_lengths, out, lse, B, H, Lq, Lk, D, mask_kind, scale,
                                  stream, driver_err);
-    if (short_keys && which != 1) {
+    if ((int64_t)Lk * D <= kSmallMaxKD && which != 1) {
         if (D == 64)
             return launch_small<64>(q, k, v, kv_lengths, out, lse, B, H, Lq, Lk, mask_kind, scale,
                                     stream);

@@ -49,8 +49,6 @@ def test_backward_accounting():
 def test_kernel_choice_and_tf32_roofline():
     c2 = synthetic.WORKLOADS["c2_padding_f32"]
     assert bench.kernel_of(c2) == "attn_fwd_tf32x3_kernel"
-    # The small causal fp32 problem is latency-bound: the CUDA-core short-key kernel.
-    assert bench.kernel_of(synthetic.WORKLOADS["c1_causal_f32"]) == "mha_fwd_f32_small_kernel"
     d128 = synthetic.small(dtype="f32", D=128, Lq=512, Lk=512)
     assert bench.kernel_of(d128) == "mha_fwd_f32_kernel"
     peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 7000.0, "_source": "test"}
