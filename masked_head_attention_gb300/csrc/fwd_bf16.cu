@@ -1253,14 +1253,15 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     p.G = 1;
     if (prenorm) {
         // Heads per chunk: a chunk forms its rows' statistics once for its G
-        // items, at a cost of about N/Lk items' worth of work (N features per
-        // row of x against Lk keys per row of attention), while larger chunks
-        // leave a longer tail (about G/2 items) when the persistent grid runs
-        // out of chunks.  Take the divisor of H that minimises
-        //     items per CTA * (1 + (N / Lk) / G) + G / 2.
+        // items, at a cost of about 2.2 N/Lk items' worth of work (N features
+        // per row of x against Lk keys per row of attention; the factor is
+        // measured on the Pre-LN workload), while larger chunks leave a longer
+        // tail (about G/2 items) when the persistent grid runs out of chunks.
+        // Take the divisor of H that minimises
+        //     items per CTA * (1 + 2.2 (N / Lk) / G) + G / 2.
         const int grid = g_grid_override > 0 ? g_grid_override : device_info().sms;
         const double per_cta = (double)p.n_items / (double)grid;
-        const double stats = (double)(c.H * c.D) / (double)(c.Lk > 0 ? c.Lk : 1);
+        const double stats = 2.2 * (double)(c.H * c.D) / (double)(c.Lk > 0 ? c.Lk : 1);
         double best = 0.0;
         for (int g = 1; g <= c.H; ++g) {
             if (c.H % g != 0) continue;
