@@ -79,8 +79,30 @@ struct DecPartial {
     float o[R][D];
 };
 
+// 16-byte asynchronous copy global -> shared memory (completion per thread:
+// cp.async.wait_group).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Per-warp V staging: one 32-key block of V rows (32 x D bf16), filled by
+// asynchronous copies issued together with the block's K loads.
+template <int D>
+constexpr size_t dec_smem_bytes() {
+    return (size_t)kDecWarps * 32 * D * sizeof(__nv_bfloat16);
+}
+
+// Few query rows: two CTAs per SM (a (b, h) problem per CTA, 256 of them
+// resident at once on 152 SMs).
 template <int D, int R>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(kDecThreads, R <= 2 ? 2 : 1)
     attn_decode_bf16_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                             const __nv_bfloat16 *__restrict__ v, const int32_t *__restrict__ kv_lengths,
                             __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, int H,
@@ -89,6 +111,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __shared__ float sQ[R][D];
     __shared__ DecPartial<D, R> sW[kDecWarps];   // per-warp partials
     __shared__ DecPartial<D, R> sC;              // this CTA's partial (read by cluster rank 0)
+    extern __shared__ uint4 dec_smem[];          // [warp][32 keys][D] bf16 V staging
 
     const int split = blockIdx.x, nsplit = gridDim.x;
     const int bh = blockIdx.y;
@@ -118,12 +141,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
         for (int c = 0; c < DC; ++c) o[r][c] = 0.f;
     }
-    // V rows in flight per batch: the whole 32-key block when the registers
-    // allow (few query rows), else 8.
-    constexpr int VB = R <= 2 ? 32 : 8;
+    __nv_bfloat16 *sVw = reinterpret_cast<__nv_bfloat16 *>(dec_smem) + (size_t)warp * 32 * D;
     for (int base = k0 + 32 * warp; base < k1; base += 32 * kDecWarps) {
         const int key = base + lane;
         const bool live = key < k1;
+        // The block's V rows go to this warp's staging slot by asynchronous
+        // copies (rows past the range copy the last valid row; their weight is
+        // 0), so they are in flight together with the K loads below.  The
+        // previous block's reads of the slot finished before this point
+        // (__syncwarp at the end of the loop body).
+        {
+            constexpr int kChunks = D / 8;   // 16-byte chunks per row
+#pragma unroll
+            for (int t = lane; t < 32 * kChunks; t += 32) {
+                const int jr = t / kChunks, c8 = t % kChunks;
+                const int vrow = min(base + jr, k1 - 1);
+                cp_async16(sVw + jr * D + c8 * 8, Vg + (size_t)vrow * D + c8 * 8);
+            }
+            cp_async_commit();
+        }
         // Every load of the block's K rows is issued before any use (keys past
         // the range read the last valid row and are masked below).
         const uint4 *kr = reinterpret_cast<const uint4 *>(Kg + (size_t)min(key, k1 - 1) * D);
@@ -165,39 +201,36 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
             for (int c = 0; c < DC; ++c) o[r][c] *= alpha;
         }
-        // O += P V over the block's keys; lane holds output columns lane*DC...
-        // VB V rows are in flight at a time; rows past the range are read
-        // from the last valid row and carry weight 0 (their p is 2^-inf).
+        // O += P V over the block's keys from the staged V rows; lane holds
+        // output columns lane*DC ...; rows past the range carry weight 0 (their
+        // p is 2^-inf).
+        cp_async_wait_all();
+        __syncwarp();
         const int nk = min(32, k1 - base);
-#pragma unroll
-        for (int j0 = 0; j0 < 32; j0 += VB) {
-            if (j0 >= nk) break;
-            float vv[VB][DC];
-#pragma unroll
-            for (int jj = 0; jj < VB; ++jj) {
-                const int vrow = min(base + j0 + jj, k1 - 1);
-                const __nv_bfloat16 *vr = Vg + (size_t)vrow * D + lane * DC;
-                if (DC == 4) {
-                    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(vr));
-                    vv[jj][0] = bf_lo(u.x);
-                    vv[jj][1] = bf_hi(u.x);
-                    vv[jj][DC - 2] = bf_lo(u.y);
-                    vv[jj][DC - 1] = bf_hi(u.y);
-                } else {
-                    const uint32_t u = __ldg(reinterpret_cast<const uint32_t *>(vr));
-                    vv[jj][0] = bf_lo(u);
-                    vv[jj][DC - 1] = bf_hi(u);
-                }
+#pragma unroll 8
+        for (int jj = 0; jj < 32; ++jj) {
+            if (jj >= nk) break;
+            const __nv_bfloat16 *vr = sVw + jj * D + lane * DC;
+            float vv[DC];
+            if (DC == 4) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(vr);
+                vv[0] = bf_lo(u.x);
+                vv[1] = bf_hi(u.x);
+                vv[DC - 2] = bf_lo(u.y);
+                vv[DC - 1] = bf_hi(u.y);
+            } else {
+                const uint32_t u = *reinterpret_cast<const uint32_t *>(vr);
+                vv[0] = bf_lo(u);
+                vv[DC - 1] = bf_hi(u);
             }
 #pragma unroll
-            for (int jj = 0; jj < VB; ++jj)
+            for (int r = 0; r < R; ++r) {
+                const float pj = __shfl_sync(0xffffffffu, p[r], jj);
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const float pj = __shfl_sync(0xffffffffu, p[r], j0 + jj);
-#pragma unroll
-                    for (int c = 0; c < DC; ++c) o[r][c] = fmaf(pj, vv[jj][c], o[r][c]);
-                }
+                for (int c = 0; c < DC; ++c) o[r][c] = fmaf(pj, vv[c], o[r][c]);
+            }
         }
+        __syncwarp();   // the slot is free for the next block's copies
     }
     // Warp partials -> shared memory.
 #pragma unroll
@@ -276,10 +309,14 @@ thread_local int g_decode_splits = 0;   // 0 automatic, else CTAs per (b, h) (at
 
 template <int D, int R>
 cudaError_t launch_dec(const Bf16Call &c, int splits, int chunk, cudaStream_t stream) {
+    constexpr size_t smem = dec_smem_bytes<D>();
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_decode_bf16_kernel<D, R>),
+                                   smem + sizeof(float) * R * D + sizeof(DecPartial<D, R>) * (kDecWarps + 1));
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)splits, (unsigned)(c.B * c.H), 1);
     cfg.blockDim = dim3(kDecThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
