@@ -310,8 +310,9 @@ thread_local int g_decode_splits = 0;   // 0 automatic, else CTAs per (b, h) (at
 template <int D, int R>
 cudaError_t launch_dec(const Bf16Call &c, int splits, int chunk, cudaStream_t stream) {
     constexpr size_t smem = dec_smem_bytes<D>();
-    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_decode_bf16_kernel<D, R>),
-                                   smem + sizeof(float) * R * D + sizeof(DecPartial<D, R>) * (kDecWarps + 1));
+    // The limit covers the dynamic part (the V staging slots) only; the
+    // static arrays come on top of it.
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_decode_bf16_kernel<D, R>), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)splits, (unsigned)(c.B * c.H), 1);

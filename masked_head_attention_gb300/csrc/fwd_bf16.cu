@@ -390,7 +390,7 @@ __device__ __forceinline__ void prefetch_x_rows(const AttnParams &p, int b, int 
 // l returns row rw + l's.
 // (The kernel is compiled at its launch bound of 168 registers a thread for
 // every role, so inside the softmax warps' item loop only two rows at a time
-// fit without spilling; the first chunk, before that loop, takes eight.)
+// fit without spilling.)
 template <int R>
 __device__ __forceinline__ float2 warp_rows_stats(const AttnParams &p, int b, int rw, int lane) {
     float2 mine = make_float2(0.f, 0.f);
@@ -753,8 +753,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st_row = row < p.Lq ? p.ln_stats[(size_t)it.b * p.Lq + row]
                                         : make_float2(0.f, 0.f);
                 } else {
-                    // This warp's 32 rows, eight at a time; then the next
-                    // chunk's rows go to L2, ready when that chunk starts.
+                    // This warp's 32 rows, kStatsRows at a time; then the
+                    // next chunk's rows go to L2, ready when that chunk starts.
                     const int rw = q0i + 32 * (warp & 3);
                     st_row = warp_rows_stats<kStatsRows>(p, it.b, rw, lane);
                     ItemIter peek = iter;
