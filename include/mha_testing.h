@@ -52,10 +52,11 @@ MHA_API void mha_set_f32_kernel(int which);
 MHA_API void mha_set_bf16_decode(int mode);
 
 /*
- * mha_set_bf16_decode_splits -- split the keys of every (b, h) over `splits`
- * CTAs of the decode kernel (one cluster; values above 8 act as 8); 0
- * restores the automatic choice (about one CTA per SM in total, at least 256
- * keys per CTA).
+ * mha_set_bf16_decode_splits -- split the visible keys of every (b, h) over
+ * `splits` CTAs of the decode kernel (one cluster; values above 8 act as 8);
+ * 0 restores the automatic choice (about one CTA per SM in total, at least
+ * 256 keys per CTA; two per (b, h) when the problems number at least one per
+ * SM and at most the CTAs resident at once).
  */
 MHA_API void mha_set_bf16_decode_splits(int splits);
 

@@ -305,7 +305,10 @@ def mha_strerror(status):
 
 
 def device_status(clear=False):
-    """Bits of the device status word (nonzero: a bounded wait expired)."""
+    """Union of the kernels' device status words: bits 0-15 name bounded
+    waits that expired, bit 16 a softmax row sum that was not positive and
+    finite, bit 17 a non-finite output.  `clear` resets the words after
+    reading them."""
     bits = ctypes.c_uint32(0)
     _check(lib().mha_device_status(ctypes.byref(bits), 1 if clear else 0), "mha_device_status")
     return bits.value
@@ -313,7 +316,8 @@ def device_status(clear=False):
 
 def test_set_device_status(unit, bits):
     """Test hook: OR `bits` into kernel unit `unit`'s device status word
-    (0 bf16 forward, 1 fp32 tensor-core forward, 2 bf16 backward)."""
+    (0 bf16 forward, 1 fp32 tensor-core forward, 2 bf16 backward, 3 bf16
+    decode)."""
     _check(lib().mha_test_set_device_status(int(unit), int(bits)), "mha_test_set_device_status")
 
 

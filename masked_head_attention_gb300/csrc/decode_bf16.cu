@@ -38,6 +38,8 @@ namespace {
 constexpr int kDecWarps = 8;
 constexpr int kDecThreads = 32 * kDecWarps;
 constexpr int kDecMaxCluster = 8;
+// Batches up to this count are ordered by visible length (below).
+constexpr int kDecRankMaxB = 256;
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -105,8 +107,8 @@ template <int D, int R>
 __global__ void __launch_bounds__(kDecThreads, R <= 2 ? 2 : 1)
     attn_decode_bf16_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                             const __nv_bfloat16 *__restrict__ v, const int32_t *__restrict__ kv_lengths,
-                            __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, int H,
-                            int Lq, int Lk, int mask_kind, float scale_log2, int chunk) {
+                            __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, int B, int H,
+                            int Lq, int Lk, int mask_kind, float scale_log2) {
     constexpr int DC = D / 32;   // output columns per lane
     __shared__ float sQ[R][D];
     __shared__ DecPartial<D, R> sW[kDecWarps];   // per-warp partials
@@ -114,14 +116,37 @@ __global__ void __launch_bounds__(kDecThreads, R <= 2 ? 2 : 1)
     extern __shared__ uint4 dec_smem[];          // [warp][32 keys][D] bf16 V staging
 
     const int split = blockIdx.x, nsplit = gridDim.x;
-    const int bh = blockIdx.y;
-    const int b = bh / H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool causal = (mask_kind & 1) != 0;
-    int len = Lk;
-    if (mask_kind & 2) len = max(0, min((int)kv_lengths[b], Lk));
-    int kend = len;                                     // keys any row can see
-    if (causal) kend = min(kend, Lq);
+    // Keys any query row of batch bb can see.
+    auto visible = [&](int bb) {
+        int len = Lk;
+        if (kv_lengths != nullptr) len = max(0, min((int)kv_lengths[bb], Lk));
+        return causal ? min(len, Lq) : len;
+    };
+    // Problem order: with per-batch lengths (and at most kDecRankMaxB
+    // batches) grid row y takes the batch of rank y / H by decreasing visible
+    // length (ties by index), so the longest problems start first and the
+    // shortest fill the end of the launch; else y = b * H + h.
+    int bh = blockIdx.y;
+    if (kv_lengths != nullptr && B <= kDecRankMaxB) {
+        __shared__ int s_batch;
+        const int want = (int)blockIdx.y / H;
+        for (int cand = tid; cand < B; cand += kDecThreads) {
+            const int lc = visible(cand);
+            int rank = 0;
+            for (int o = 0; o < B; ++o) {
+                const int lo = visible(o);
+                rank += (lo > lc || (lo == lc && o < cand)) ? 1 : 0;
+            }
+            if (rank == want) s_batch = cand;   // ranks are a permutation: one writer
+        }
+        __syncthreads();
+        bh = s_batch * H + (int)blockIdx.y % H;
+    }
+    const int kend = visible(bh / H);
+    // This problem's keys in nsplit contiguous chunks of a multiple of 32.
+    const int chunk = max(32, (((kend + nsplit - 1) / nsplit + 31) / 32) * 32);
     const int k0 = split * chunk, k1 = min(kend, k0 + chunk);
 
     const __nv_bfloat16 *Qg = q + (size_t)bh * Lq * D;
@@ -308,7 +333,7 @@ thread_local int g_decode_override = 0;  // 0 automatic, 1 never
 thread_local int g_decode_splits = 0;   // 0 automatic, else CTAs per (b, h) (at most 8)
 
 template <int D, int R>
-cudaError_t launch_dec(const Bf16Call &c, int splits, int chunk, cudaStream_t stream) {
+cudaError_t launch_dec(const Bf16Call &c, int splits, cudaStream_t stream) {
     constexpr size_t smem = dec_smem_bytes<D>();
     // The limit covers the dynamic part (the V staging slots) only; the
     // static arrays come on top of it.
@@ -331,16 +356,16 @@ cudaError_t launch_dec(const Bf16Call &c, int splits, int chunk, cudaStream_t st
                               reinterpret_cast<const __nv_bfloat16 *>(c.k),
                               reinterpret_cast<const __nv_bfloat16 *>(c.v),
                               (c.mask_kind & 2) ? c.kv_lengths : nullptr,
-                              reinterpret_cast<__nv_bfloat16 *>(c.out), c.lse, c.H, c.Lq, c.Lk,
-                              c.mask_kind, c.scale * 1.4426950408889634f, chunk);
+                              reinterpret_cast<__nv_bfloat16 *>(c.out), c.lse, c.B, c.H, c.Lq, c.Lk,
+                              c.mask_kind, c.scale * 1.4426950408889634f);
 }
 
 template <int D>
-cudaError_t launch_dec_rows(const Bf16Call &c, int splits, int chunk, cudaStream_t stream) {
-    if (c.Lq <= 1) return launch_dec<D, 1>(c, splits, chunk, stream);
-    if (c.Lq <= 2) return launch_dec<D, 2>(c, splits, chunk, stream);
-    if (c.Lq <= 4) return launch_dec<D, 4>(c, splits, chunk, stream);
-    return launch_dec<D, 8>(c, splits, chunk, stream);
+cudaError_t launch_dec_rows(const Bf16Call &c, int splits, cudaStream_t stream) {
+    if (c.Lq <= 1) return launch_dec<D, 1>(c, splits, stream);
+    if (c.Lq <= 2) return launch_dec<D, 2>(c, splits, stream);
+    if (c.Lq <= 4) return launch_dec<D, 4>(c, splits, stream);
+    return launch_dec<D, 8>(c, splits, stream);
 }
 
 }  // namespace
@@ -359,27 +384,28 @@ bool decode_applies(const Bf16Call &c) {
 }
 
 cudaError_t launch_decode_bf16(const Bf16Call &c, int num_sms, cudaStream_t stream) {
-    // Keys any row can see at most; the split covers them in contiguous
-    // chunks of a multiple of 32 keys.
+    // Keys any row can see at most (each CTA splits its own problem's
+    // visible keys into chunks of a multiple of 32).
     const int kend = (c.mask_kind & 1) ? (c.Lq < c.Lk ? c.Lq : c.Lk) : c.Lk;
     const int64_t BH = (int64_t)c.B * c.H;
     // About one CTA per SM in total, at least 256 keys per CTA, at most a
-    // portable cluster of 8.  Splitting costs more than the wave it fills
-    // (measured on the 8 x 32-head, 8192-key decode step: one CTA per (b, h)
-    // 171 us, two 195 us, eight 211 us), so problems with at least one
-    // (b, h) per SM are not split at all.
+    // portable cluster of 8.  With at least one (b, h) per SM: two CTAs per
+    // problem while one CTA per problem would fit in a single wave (few-row
+    // launches hold two CTAs per SM), which evens out the end of the launch;
+    // else one.  Measured on the 8 x 32-head decode step with cache lengths
+    // 4096..8192 (longest problems first): one CTA per (b, h) 163 us, two
+    // 161, three 164, four 168, eight 189.
+    const int64_t slots = (int64_t)num_sms * (c.Lq <= 2 ? 2 : 1);
     int64_t want = ((int64_t)num_sms + BH - 1) / BH;
+    if (BH >= num_sms && BH <= slots) want = 2;
     const int64_t by_keys = (kend + 255) / 256;
     if (want > by_keys) want = by_keys;
     if (want > kDecMaxCluster) want = kDecMaxCluster;
     if (want < 1) want = 1;
     if (g_decode_splits > 0) want = g_decode_splits < kDecMaxCluster ? g_decode_splits : kDecMaxCluster;
     const int splits = (int)want;
-    int chunk = (kend + splits - 1) / splits;
-    chunk = ((chunk + 31) / 32) * 32;
-    if (chunk < 32) chunk = 32;
-    return c.D == 64 ? launch_dec_rows<64>(c, splits, chunk, stream)
-                     : launch_dec_rows<128>(c, splits, chunk, stream);
+    return c.D == 64 ? launch_dec_rows<64>(c, splits, stream)
+                     : launch_dec_rows<128>(c, splits, stream);
 }
 
 }  // namespace mha
