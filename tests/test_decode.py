@@ -98,3 +98,43 @@ def test_decode_forced_splits(splits):
     want = oracle.mha_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), mask, lens)
     check_bf16(as_np(out), want, "splits=%d" % splits)
     assert mha.device_status() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,H,Lq,Lk,D", [(40, 3, 2, 300, 128), (300, 1, 1, 64, 64)],
+                         ids=["ranked-40-batches", "natural-order-300-batches"])
+def test_decode_problem_order(B, H, Lq, Lk, D):
+    """With per-batch lengths the problems run longest first (the kernel ranks
+    up to 256 batches itself, ties by index); every (b, h) output still lands
+    in its own place.  Lengths with many ties, zeros and values past Lk; 300
+    batches take the unranked order."""
+    rng = np.random.default_rng(91)
+    lens = [int(x) for x in rng.choice([0, 1, 17, Lk // 2, Lk, Lk + 5], size=B)]
+    q = randn((B, H, Lq, D), 92, 1.0, torch.bfloat16)
+    k = randn((B, H, Lk, D), 93, 1.0, torch.bfloat16)
+    v = randn((B, H, Lk, D), 94, 1.0, torch.bfloat16)
+    out = mha.mha_fwd(dev(q), dev(k), dev(v), 2, dev(lens_tensor(lens)))
+    torch.cuda.synchronize()
+    want = oracle.mha_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), 2, lens)
+    check_bf16(as_np(out), want, "B=%d" % B)
+    assert mha.device_status() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("splits", [2, 8])
+def test_decode_short_problems_forced_splits(splits):
+    """Each problem's visible keys are split on their own; with short lengths
+    the later CTAs of a cluster get no key at all and contribute nothing."""
+    B, H, Lq, Lk, D, mask, lens = 3, 2, 2, 500, 64, 2, [5, 0, 33]
+    q = randn((B, H, Lq, D), 95, 1.0, torch.bfloat16)
+    k = randn((B, H, Lk, D), 96, 1.0, torch.bfloat16)
+    v = randn((B, H, Lk, D), 97, 1.0, torch.bfloat16)
+    mha.set_bf16_decode_splits(splits)
+    try:
+        out = mha.mha_fwd(dev(q), dev(k), dev(v), mask, dev(lens_tensor(lens)))
+        torch.cuda.synchronize()
+    finally:
+        mha.set_bf16_decode_splits(0)
+    want = oracle.mha_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), mask, lens)
+    check_bf16(as_np(out), want, "splits=%d" % splits)
+    assert mha.device_status() == 0
