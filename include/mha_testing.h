@@ -68,6 +68,15 @@ MHA_API void mha_set_bf16_decode_splits(int splits);
 MHA_API void mha_set_bwd_kernel(int which);
 
 /*
+ * mha_set_pdl -- 1 (the default): every kernel is launched with programmatic
+ * dependent launch allowed, so its grid can be scheduled while the previous
+ * kernel of the stream finishes (each kernel still waits, on the device, for
+ * that kernel's completion and writes before it touches global memory);
+ * 0: ordinary launches.  Lets a test compare the two.
+ */
+MHA_API void mha_set_pdl(int on);
+
+/*
  * mha_test_set_device_status -- OR `bits` into the device status word of
  * kernel unit `unit` on the current device (0 = bf16 forward, 1 = fp32
  * tensor-core forward, 2 = bf16 tensor-core backward, 3 = bf16 decode), as

@@ -77,6 +77,8 @@ def lib():
         L.mha_set_bf16_decode_splits.restype = None
         L.mha_set_bwd_kernel.argtypes = [i]
         L.mha_set_bwd_kernel.restype = None
+        L.mha_set_pdl.argtypes = [i]
+        L.mha_set_pdl.restype = None
         _lib = L
     return _lib
 
@@ -350,6 +352,12 @@ def set_bf16_decode_splits(splits):
 def set_bwd_kernel(which):
     """Backward kernels: 0 automatic (bf16 on the tensor cores), 1 CUDA cores."""
     lib().mha_set_bwd_kernel(int(which))
+
+
+def set_pdl(on):
+    """Test hook: programmatic dependent launch on (1, default) or off (0) for
+    calls made from this thread."""
+    lib().mha_set_pdl(1 if on else 0)
 
 
 def set_f32_kernel(which):

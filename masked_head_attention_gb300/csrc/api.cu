@@ -31,6 +31,9 @@ cudaError_t status_ctl(int unit, int op, uint64_t value, uint32_t *bits) {
 // cores), 1 CUDA cores for both.
 thread_local int g_bwd_kernel = 0;
 
+// Programmatic dependent launch on (1, the default) or off (0); test hook.
+thread_local int g_pdl = 1;
+
 // Shared checks of the shape arguments; 1 means "nothing to do".
 int check_shape(int B, int H, int Lq, int Lk, int D, float scale, int *empty) {
     *empty = 0;
@@ -45,6 +48,11 @@ int check_shape(int B, int H, int Lq, int Lk, int D, float scale, int *empty) {
 }
 
 }  // namespace
+
+namespace mha {
+bool pdl_enabled() { return g_pdl != 0; }
+void set_pdl(int on) { g_pdl = on != 0 ? 1 : 0; }
+}  // namespace mha
 
 extern "C" {
 
@@ -352,5 +360,6 @@ void mha_set_bf16_decode(int mode) { mha::set_decode_override(mode); }
 void mha_set_bf16_decode_splits(int splits) { mha::set_decode_splits(splits); }
 
 void mha_set_bwd_kernel(int which) { g_bwd_kernel = (which == 1) ? 1 : 0; }
+void mha_set_pdl(int on) { mha::set_pdl(on); }
 
 }  // extern "C"

@@ -90,6 +90,8 @@ template <int D, typename T>
 __global__ void __launch_bounds__(256)
     bwd_row_delta_kernel(const T *__restrict__ o, const T *__restrict__ dout,
                          float *__restrict__ delta, float *__restrict__ dq, int64_t rows) {
+    pdl_wait();      // the stream's previous kernel has completed; its writes are visible
+    pdl_trigger();   // the next kernel may be scheduled
     constexpr int PER = D / 64;   // groups of 4 elements per lane
     const int64_t row = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4);
     const int lane = threadIdx.x & 15;
@@ -120,6 +122,8 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
                        const float *__restrict__ delta, const int32_t *__restrict__ kv_lengths,
                        float *__restrict__ dq, T *__restrict__ dk, T *__restrict__ dv, int H,
                        int Lq, int Lk, int mask_kind, float scale, float scale_log2) {
+    pdl_wait();      // the stream's previous kernel has completed; its writes are visible
+    pdl_trigger();   // the next kernel may be scheduled
     using C = BwdCfg<D>;
     constexpr int OC = C::OC;
     extern __shared__ float4 bwd_smem[];
@@ -329,6 +333,8 @@ __global__ void __launch_bounds__(kBwdThreads, D == 64 ? 2 : 1)
 // dq (bf16) from the fp32 accumulator, 8 elements per thread.
 __global__ void __launch_bounds__(256)
     bwd_dq_convert_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, int64_t n8) {
+    pdl_wait();      // the stream's previous kernel has completed; its writes are visible
+    pdl_trigger();   // the next kernel may be scheduled
     const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
     if (i >= n8) return;
     const float4 a = __ldg(reinterpret_cast<const float4 *>(acc) + 2 * i);
@@ -349,19 +355,17 @@ cudaError_t launch_bwd(const T *q, const T *k, const T *v, const T *o, const T *
     const int64_t rows = (int64_t)B * H * Lq;
     cudaError_t e = cudaSuccess;
     if (rows > 0) {
-        bwd_row_delta_kernel<D, T><<<(unsigned)((rows + 15) / 16), 256, 0, stream>>>(
-            o, dout, delta, dq_acc, rows);
-        e = cudaGetLastError();
+        e = launch_kernel(bwd_row_delta_kernel<D, T>, dim3((unsigned)((rows + 15) / 16)), dim3(256),
+                          0, stream, nullptr, o, dout, delta, dq_acc, rows);
     }
     if (e != cudaSuccess || Lk == 0) return e;
     constexpr size_t smem = BwdCfg<D>::kSmem;
     e = set_smem_limit(reinterpret_cast<const void *>(mha_bwd_f32_kernel<D, T>), smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((Lk + kBwdBN - 1) / kBwdBN, H, B);
-    mha_bwd_f32_kernel<D, T><<<grid, kBwdThreads, smem, stream>>>(
-        q, k, v, dout, lse, delta, kv, dq_acc, dk, dv, H, Lq, Lk, mask_kind, scale,
-        scale * 1.4426950408889634f);
-    return cudaGetLastError();
+    return launch_kernel(mha_bwd_f32_kernel<D, T>, grid, dim3(kBwdThreads), smem, stream, nullptr,
+                         q, k, v, dout, lse, delta, kv, dq_acc, dk, dv, H, Lq, Lk, mask_kind, scale,
+                         scale * 1.4426950408889634f);
 }
 
 }  // namespace
@@ -382,13 +386,14 @@ cudaError_t launch_bwd_row_delta_bf16(const void *o, const void *dout, float *de
     if (rows <= 0) return cudaSuccess;
     using bf = __nv_bfloat16;
     const unsigned grid = (unsigned)((rows + 15) / 16);
+    float *no_dq = nullptr;
     if (D == 64)
-        bwd_row_delta_kernel<64, bf><<<grid, 256, 0, stream>>>(
-            static_cast<const bf *>(o), static_cast<const bf *>(dout), delta, nullptr, rows);
-    else
-        bwd_row_delta_kernel<128, bf><<<grid, 256, 0, stream>>>(
-            static_cast<const bf *>(o), static_cast<const bf *>(dout), delta, nullptr, rows);
-    return cudaGetLastError();
+        return launch_kernel(bwd_row_delta_kernel<64, bf>, dim3(grid), dim3(256), 0, stream, nullptr,
+                             static_cast<const bf *>(o), static_cast<const bf *>(dout), delta, no_dq,
+                             rows);
+    return launch_kernel(bwd_row_delta_kernel<128, bf>, dim3(grid), dim3(256), 0, stream, nullptr,
+                         static_cast<const bf *>(o), static_cast<const bf *>(dout), delta, no_dq,
+                         rows);
 }
 
 cudaError_t launch_bwd_bf16(const void *q, const void *k, const void *v, const void *o,
@@ -409,9 +414,9 @@ cudaError_t launch_bwd_bf16(const void *q, const void *k, const void *v, const v
     if (e != cudaSuccess) return e;
     const int64_t n8 = (int64_t)B * H * Lq * D / 8;
     if (n8 == 0) return cudaSuccess;
-    bwd_dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(
-        dq_acc, static_cast<bf *>(dq), n8);
-    return cudaGetLastError();
+    return launch_kernel(bwd_dq_convert_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0,
+                         stream, nullptr, static_cast<const float *>(dq_acc), static_cast<bf *>(dq),
+                         n8);
 }
 
 }  // namespace mha

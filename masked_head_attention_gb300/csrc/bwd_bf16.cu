@@ -624,6 +624,8 @@ struct BwdBf16Launch {
 template <int D>
 __global__ void __launch_bounds__(bwd_threads<D>(), 1)
     attn_bwd_bf16_kernel(const __grid_constant__ BwdBf16Launch L) {
+    pdl_wait();      // the stream's previous kernel has completed; its writes are visible
+    pdl_trigger();   // the next kernel may be scheduled
     const int idx = (int)blockIdx.x, BH = L.BH;
     const int m = min(L.n_kv, L.n_q);
     int r, bh;
@@ -662,8 +664,8 @@ cudaError_t launch_bwd_bf16_tc(const BwdBf16Launch &L, cudaStream_t stream) {
     const uint64_t blocks = ((uint64_t)L.n_kv + (uint64_t)L.n_q) * (uint64_t)L.BH;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-    attn_bwd_bf16_kernel<D><<<(unsigned)blocks, bwd_threads<D>(), smem, stream>>>(L);
-    return cudaGetLastError();
+    return launch_kernel(attn_bwd_bf16_kernel<D>, dim3((unsigned)blocks), dim3(bwd_threads<D>()), smem,
+                         stream, nullptr, L);
 }
 
 }  // namespace

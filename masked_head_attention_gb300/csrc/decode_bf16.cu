@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(kDecThreads, R <= 2 ? 2 : 1)
                             const __nv_bfloat16 *__restrict__ v, const int32_t *__restrict__ kv_lengths,
                             __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, int B, int H,
                             int Lq, int Lk, int mask_kind, float scale_log2) {
+    pdl_wait();      // the stream's previous kernel has completed; its writes are visible
+    pdl_trigger();   // the next kernel may be scheduled
     constexpr int DC = D / 32;   // output columns per lane
     __shared__ float sQ[R][D];
     __shared__ DecPartial<D, R> sW[kDecWarps];   // per-warp partials
@@ -339,25 +341,19 @@ cudaError_t launch_dec(const Bf16Call &c, int splits, cudaStream_t stream) {
     // static arrays come on top of it.
     cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_decode_bf16_kernel<D, R>), smem);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)splits, (unsigned)(c.B * c.H), 1);
-    cfg.blockDim = dim3(kDecThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_decode_bf16_kernel<D, R>,
-                              reinterpret_cast<const __nv_bfloat16 *>(c.q),
-                              reinterpret_cast<const __nv_bfloat16 *>(c.k),
-                              reinterpret_cast<const __nv_bfloat16 *>(c.v),
-                              (c.mask_kind & 2) ? c.kv_lengths : nullptr,
-                              reinterpret_cast<__nv_bfloat16 *>(c.out), c.lse, c.B, c.H, c.Lq, c.Lk,
-                              c.mask_kind, c.scale * 1.4426950408889634f);
+    cudaLaunchAttribute cluster;
+    cluster.id = cudaLaunchAttributeClusterDimension;
+    cluster.val.clusterDim.x = (unsigned)splits;
+    cluster.val.clusterDim.y = 1;
+    cluster.val.clusterDim.z = 1;
+    return launch_kernel(attn_decode_bf16_kernel<D, R>, dim3((unsigned)splits, (unsigned)(c.B * c.H), 1),
+                         dim3(kDecThreads), smem, stream, &cluster,
+                         reinterpret_cast<const __nv_bfloat16 *>(c.q),
+                         reinterpret_cast<const __nv_bfloat16 *>(c.k),
+                         reinterpret_cast<const __nv_bfloat16 *>(c.v),
+                         (c.mask_kind & 2) ? c.kv_lengths : nullptr,
+                         reinterpret_cast<__nv_bfloat16 *>(c.out), c.lse, c.B, c.H, c.Lq, c.Lk,
+                         c.mask_kind, c.scale * 1.4426950408889634f);
 }
 
 template <int D>

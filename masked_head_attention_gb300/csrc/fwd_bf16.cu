@@ -321,6 +321,8 @@ __device__ __forceinline__ void ln_stats_warp(const __nv_bfloat16 *const (&xr)[R
 __global__ void __launch_bounds__(256) ln_row_stats_kernel(const __nv_bfloat16 *__restrict__ x,
                                                            float2 *__restrict__ stats,
                                                            int64_t rows, int N, float eps) {
+    pdl_wait();      // the stream's previous kernel has completed; its writes are visible
+    pdl_trigger();   // the next kernel may be scheduled
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -437,6 +439,8 @@ struct ItemIter {
 template <int D, bool PRENORM>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ AttnParams p) {
+    pdl_wait();      // the stream's previous kernel has completed; its writes are visible
+    pdl_trigger();   // the next kernel may be scheduled
     using C = Cfg<D>;
     constexpr int NH = C::NH;
     constexpr uint32_t TILE = C::kTile;
@@ -1148,8 +1152,8 @@ cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
     // Persistent grid: one CTA per SM (one fits per SM), unless overridden.
     int grid = g_grid_override > 0 ? g_grid_override : device_info().sms;
     if (grid > p.n_chunks) grid = p.n_chunks;
-    attn_fwd_bf16_kernel<D, PRENORM><<<grid, kThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(attn_fwd_bf16_kernel<D, PRENORM>, dim3(grid), dim3(kThreads), smem, stream,
+                         nullptr, p);
 }
 
 }  // namespace
@@ -1199,9 +1203,8 @@ cudaError_t launch_ln_row_stats(const void *x, float2 *stats, int64_t rows, int 
     int64_t blocks = (warps + 7) / 8;
     const int64_t cap = 32ll * device_info().sms;
     if (blocks > cap) blocks = cap;
-    ln_row_stats_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16 *>(x), stats, rows, N, eps);
-    return cudaGetLastError();
+    return launch_kernel(ln_row_stats_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, nullptr,
+                         reinterpret_cast<const __nv_bfloat16 *>(x), stats, rows, N, eps);
 }
 
 cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_err,

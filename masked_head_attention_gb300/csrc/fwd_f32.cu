@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(kThreads)
                        const float *__restrict__ v, const int32_t *__restrict__ kv_lengths,
                        float *__restrict__ out, float *__restrict__ lse, int H, int Lq, int Lk,
                        int mask_kind, float scale_log2) {
+    pdl_wait();      // the stream's previous kernel has completed; its writes are visible
+    pdl_trigger();   // the next kernel may be scheduled
     using C = F32Cfg<D>;
     extern __shared__ float4 f32_smem[];
     float *sQ = reinterpret_cast<float *>(f32_smem);
@@ -341,6 +343,8 @@ __global__ void __launch_bounds__(kSmallThreads, 2)
                              const float *__restrict__ v, const int32_t *__restrict__ kv_lengths,
                              float *__restrict__ out, float *__restrict__ lse, int H, int Lq,
                              int Lk, int mask_kind, float scale_log2, int keys_cap) {
+    pdl_wait();      // the stream's previous kernel has completed; its writes are visible
+    pdl_trigger();   // the next kernel may be scheduled
     using C = SmallCfg<D>;
     constexpr int DC = D / 32;   // output columns per lane
     constexpr int R = kSmallR;
@@ -514,9 +518,9 @@ cudaError_t launch_small(const float *q, const float *k, const float *v, const i
     cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(mha_fwd_f32_small_kernel<D>), C::smem(C::kMaxKeys));
     if (e != cudaSuccess) return e;
     const dim3 grid((Lq + kSmallRows - 1) / kSmallRows, H, B);
-    mha_fwd_f32_small_kernel<D><<<grid, kSmallThreads, smem, stream>>>(
-        q, k, v, kv, out, lse, H, Lq, Lk, mask_kind, scale * 1.4426950408889634f, keys_cap);
-    return cudaGetLastError();
+    return launch_kernel(mha_fwd_f32_small_kernel<D>, grid, dim3(kSmallThreads), smem, stream, nullptr,
+                         q, k, v, kv, out, lse, H, Lq, Lk, mask_kind, scale * 1.4426950408889634f,
+                         keys_cap);
 }
 
 template <int D>
@@ -528,9 +532,8 @@ cudaError_t launch(const float *q, const float *k, const float *v, const int32_t
     if (e != cudaSuccess) return e;
     const dim3 grid((Lq + kBM - 1) / kBM, H, B);
     const float scale_log2 = scale * 1.4426950408889634f;
-    mha_fwd_f32_kernel<D><<<grid, kThreads, smem, stream>>>(q, k, v, kv, out, lse, H, Lq, Lk,
-                                                            mask_kind, scale_log2);
-    return cudaGetLastError();
+    return launch_kernel(mha_fwd_f32_kernel<D>, grid, dim3(kThreads), smem, stream, nullptr, q, k, v,
+                         kv, out, lse, H, Lq, Lk, mask_kind, scale_log2);
 }
 
 // 0 automatic, 1 tiled only, 2 short-key kernel where it applies, 3 the

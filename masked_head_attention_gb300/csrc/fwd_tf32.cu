@@ -202,6 +202,8 @@ __device__ __forceinline__ float row_lse2(float m2, float l) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tf32x3_kernel(const __grid_constant__ Tf32Params p) {
+    pdl_wait();      // the stream's previous kernel has completed; its writes are visible
+    pdl_trigger();   // the next kernel may be scheduled
     if (wait_expired_before()) return;
 
     extern __shared__ uint8_t smem_raw[];
@@ -720,8 +722,8 @@ cudaError_t launch_fwd_tf32x3(const float *q, const float *k, const float *v,
     int grid = device_info().sms;
     if (grid > p.n_items) grid = p.n_items;
     if (grid < 1) return cudaSuccess;
-    attn_fwd_tf32x3_kernel<<<grid, kThreads, kSmem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(attn_fwd_tf32x3_kernel, dim3(grid), dim3(kThreads), kSmem, stream, nullptr,
+                         p);
 }
 
 cudaError_t status_ctl_fwd_tf32(int op, uint64_t value, uint32_t *bits) {

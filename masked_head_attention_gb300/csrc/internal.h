@@ -9,6 +9,48 @@
 
 namespace mha {
 
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with it allowed, so its grid may be scheduled while the previous kernel of
+// the stream is still finishing; each kernel starts with pdl_wait(), which
+// returns once the previous grid has completed and its memory writes are
+// visible, before it reads or writes global memory, and calls pdl_trigger()
+// to let the next grid be scheduled in turn.  Without the attribute (or with
+// a previous kernel that never triggers) both are no-ops and ordinary stream
+// order applies.  The thread-local switch is a test hook (mha_set_pdl).
+bool pdl_enabled();
+void set_pdl(int on);
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
+// cudaLaunchKernelEx with programmatic dependent launch allowed (when
+// pdl_enabled()) and up to one more launch attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, const cudaLaunchAttribute *extra,
+                          Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (extra != nullptr) attr[n++] = *extra;
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // SM count and L2 size of the current device (cached per device).
 struct DeviceInfo {
     int sms = 0;
@@ -50,9 +92,9 @@ cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const
                            const float *dout, const float *lse, const int32_t *kv_lengths,
                            float *dq, float *dk, float *dv, float *delta, int B, int H, int Lq,
                            int Lk, int D, int mask_kind, float scale, cudaStream_t stream);
-// bf16 backward on the tensor cores (bwd_bf16.cu): dK, dV by a key-stationary
-// kernel and dQ by a query-stationary one, from the forward's log-sum-exp and
-// Delta (B*H*Lq floats each).  Every gradient element written once.
+// bf16 backward on the tensor cores (bwd_bf16.cu): key-stationary dK/dV tiles
+// and query-stationary dQ tiles in one launch, from the forward's log-sum-exp
+// and Delta (B*H*Lq floats each).  Every gradient element written once.
 cudaError_t launch_bwd_bf16_tensor(const void *q, const void *k, const void *v, const void *dout,
                                    const float *lse, const float *delta, const int32_t *kv_lengths,
                                    void *dq, void *dk, void *dv, int B, int H, int Lq, int Lk, int D,
