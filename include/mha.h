@@ -22,9 +22,11 @@
  *    shift) and 5.2 (divide the logits by sqrt(d_k)).
  *
  * Conventions for every entry point.
- *  - Pointers are DEVICE pointers owned by the caller; the library keeps no
- *    per-call state and allocates no device memory.  (mha_bwd uses a
- *    workspace the caller passes in, see mha_bwd_workspace_size.)
+ *  - Pointers are DEVICE pointers owned by the caller (mha_fwd_host: host
+ *    tensors, device workspace); the library keeps no per-call state and
+ *    allocates no device memory.  (mha_bwd and mha_fwd_host use a workspace
+ *    the caller passes in, see mha_bwd_workspace_size and
+ *    mha_fwd_host_workspace_size.)
  *  - Layouts are dense and row-major: q, out [B,H,Lq,D]; k, v [B,H,Lk,D];
  *    kv_lengths int32 [B].  Every tensor pointer must be 16-byte aligned.
  *  - Work is enqueued on `stream` (0 = legacy default stream); no entry
@@ -109,6 +111,47 @@ MHA_API int mha_fwd(const void *q, const void *k, const void *v, int mask_kind,
 MHA_API int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_kind,
                         const int32_t *kv_lengths, void *out, float *lse, int B, int H,
                         int Lq, int Lk, int D, float scale, int dtype, cudaStream_t stream);
+
+/*
+ * mha_fwd_host -- mha_fwd on tensors in HOST memory: the call copies q, k, v
+ * (and kv_lengths) to the device, runs the forward and copies out back, with
+ * the copies and the kernels of successive pieces overlapped.  The problems
+ * are taken in pieces of consecutive heads of one batch (contiguous in every
+ * tensor); each piece goes through one of two device slots in `workspace`:
+ * its inputs are copied in on one internal stream while the previous piece
+ * is computed on `stream` and the one before is copied out on another, so
+ * the link carries inputs and outputs at the same time and the kernels run
+ * behind the copies.  Results are identical to mha_fwd's on the same data.
+ *   q, k, v, out, kv_lengths   HOST pointers, layouts as for mha_fwd
+ *               (kv_lengths host int32 [B]).  Page-locked memory
+ *               (cudaHostAlloc / cudaHostRegister) gives asynchronous,
+ *               overlapped copies; pageable memory works but its copies are
+ *               staged by the driver.  out must not overlap the inputs.
+ *               The inputs are read, and out written, asynchronously: they
+ *               must stay valid and untouched until `stream` reaches the end
+ *               of the call.
+ *   workspace   device scratch of at least mha_fwd_host_workspace_size(...)
+ *               bytes, 16-byte aligned, owned by the caller, not used by
+ *               anything else until `stream` reaches the end of the call.
+ *   workspace_bytes  its size; too small returns MHA_ERR_INVALID_ARG.
+ *   stream      every copy and kernel of the call is ordered after the work
+ *               already enqueued on it, and the work enqueued on it later is
+ *               ordered after them (two internal streams, created and
+ *               released by the call, carry the copies).
+ * Other arguments and errors as for mha_fwd.  Returns MHA_OK or a negative
+ * mha_status.
+ */
+MHA_API int mha_fwd_host(const void *q, const void *k, const void *v, int mask_kind,
+                         const int32_t *kv_lengths, void *out, int B, int H, int Lq, int Lk,
+                         int D, float scale, int dtype, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
+ * mha_fwd_host_workspace_size -- bytes of device workspace mha_fwd_host
+ * needs for these sizes (two slots of one piece's q, k, v and out, plus the
+ * lengths); 0 for an empty problem or an unsupported argument.
+ */
+MHA_API size_t mha_fwd_host_workspace_size(int B, int H, int Lq, int Lk, int D, int dtype);
 
 /*
  * mha_bwd -- backward pass of mha_fwd: the gradients of the loss

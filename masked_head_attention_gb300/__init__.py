@@ -57,6 +57,10 @@ def lib():
         L.mha_bwd.restype = i
         L.mha_bwd_workspace_size.argtypes = [i, i, i, i, i]
         L.mha_bwd_workspace_size.restype = ctypes.c_size_t
+        L.mha_fwd_host.argtypes = [P, P, P, i, P, P, i, i, i, i, i, f, i, P, ctypes.c_size_t, P]
+        L.mha_fwd_host.restype = i
+        L.mha_fwd_host_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.mha_fwd_host_workspace_size.restype = ctypes.c_size_t
         L.mha_test_set_device_status.argtypes = [i, ctypes.c_uint32]
         L.mha_test_set_device_status.restype = i
         L.mha_test_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
@@ -190,6 +194,65 @@ def mha_fwd_lse(q, k, v, mask_kind=MASK_NONE, kv_lengths=None, out=None, lse=Non
                              _ptr(out), _ptr(lse), B, H, Lq, Lk, D, scale, _dtype_code(q),
                              _stream(stream, q.get_device())), "mha_fwd_lse")
     return out, lse
+
+
+def _host(t, name, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError("%s must be a host (CPU) tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+def mha_fwd_host_workspace_size(B, H, Lq, Lk, D, dtype):
+    """Bytes of device workspace mha_fwd_host needs (dtype: F32 or BF16 code)."""
+    return int(lib().mha_fwd_host_workspace_size(int(B), int(H), int(Lq), int(Lk), int(D),
+                                                 int(dtype)))
+
+
+def mha_fwd_host(q, k, v, mask_kind=MASK_NONE, kv_lengths=None, out=None, scale=None,
+                 workspace=None, device=None, stream=None):
+    """mha_fwd on HOST tensors (pinned memory for overlapped copies): copies in,
+    computes and copies out in pieces, the copies overlapping the kernels.
+
+    q [B,H,Lq,D], k/v [B,H,Lk,D] (fp32 or bf16), kv_lengths host int32 [B].
+    `out` (host, pinned when omitted) receives the result once the stream
+    reaches the end of the call (synchronise before reading it).
+    `workspace` is a device uint8 tensor of at least
+    mha_fwd_host_workspace_size(...) bytes; when omitted, one is taken from
+    torch's allocator for this call (the library itself never allocates)."""
+    torch = _torch()
+    _host(q, "q")
+    _host(k, "k", q.dtype)
+    _host(v, "v", q.dtype)
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    if tuple(k.shape) != (B, H, Lk, D) or tuple(v.shape) != (B, H, Lk, D):
+        raise ValueError("k and v must be [B,H,Lk,D] matching q")
+    if kv_lengths is not None:
+        _host(kv_lengths, "kv_lengths", torch.int32)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    else:
+        _host(out, "out", q.dtype)
+    dt = _dtype_code(q)
+    dev_index = torch.cuda.current_device() if device is None else int(device)
+    need = mha_fwd_host_workspace_size(B, H, Lq, Lk, D, dt)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8,
+                                device=torch.device("cuda", dev_index))
+    else:
+        _dev(workspace, "workspace")
+        dev_index = workspace.get_device()
+    wbytes = workspace.numel() * workspace.element_size()
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(lib().mha_fwd_host(_ptr(q), _ptr(k), _ptr(v), int(mask_kind), _ptr(kv_lengths),
+                              _ptr(out), B, H, Lq, Lk, D, scale, dt, _ptr(workspace), wbytes,
+                              _stream(stream, dev_index)), "mha_fwd_host")
+    return out
 
 
 def mha_bwd_workspace_size(B, H, Lq, D, dtype):

@@ -47,6 +47,44 @@ int check_shape(int B, int H, int Lq, int Lk, int D, float scale, int *empty) {
     return MHA_OK;
 }
 
+// mha_fwd_host: the problems go through the device in pieces of `heads`
+// consecutive heads of one batch (contiguous in q, k, v and out), each held in
+// one of two workspace slots.  A piece carries at most kHostPieceBytes of q,
+// k, v and out unless one head alone is larger.
+constexpr int64_t kHostPieceBytes = 64ll << 20;
+
+struct HostPlan {
+    int heads = 1;              // heads per piece
+    size_t q_bytes = 0;         // one piece of q (and of out)
+    size_t k_bytes = 0;         // one piece of k (and of v)
+    size_t off_k = 0, off_v = 0, off_out = 0, slot = 0;   // offsets inside a slot
+    size_t off_lens = 0;        // after the two slots
+    size_t total = 0;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Returns false for an empty problem or unsupported arguments.
+bool host_plan(int B, int H, int Lq, int Lk, int D, int dtype, HostPlan *pl) {
+    if (B <= 0 || H <= 0 || Lq <= 0 || Lk < 0 || (D != 64 && D != 128)) return false;
+    if (dtype != MHA_F32 && dtype != MHA_BF16) return false;
+    const int64_t esz = dtype == MHA_F32 ? 4 : 2;
+    const int64_t per_head = (2 * (int64_t)Lq + 2 * (int64_t)Lk) * D * esz;
+    int heads = 1;
+    for (int g = 1; g <= H; ++g)
+        if (H % g == 0 && g * per_head <= kHostPieceBytes) heads = g;
+    pl->heads = heads;
+    pl->q_bytes = (size_t)heads * Lq * D * esz;
+    pl->k_bytes = (size_t)heads * Lk * D * esz;
+    pl->off_k = round256(pl->q_bytes);
+    pl->off_v = pl->off_k + round256(pl->k_bytes);
+    pl->off_out = pl->off_v + round256(pl->k_bytes);
+    pl->slot = pl->off_out + round256(pl->q_bytes);
+    pl->off_lens = 2 * pl->slot;
+    pl->total = pl->off_lens + round256(sizeof(int32_t) * (size_t)B);
+    return true;
+}
+
 }  // namespace
 
 namespace mha {
@@ -135,6 +173,115 @@ int mha_fwd_lse(const void *q, const void *k, const void *v, int mask_kind,
         e = mha::launch_fwd_bf16(c, stream, &drv, nullptr);
     }
     return drv != 0 ? MHA_ERR_CUDA : from_cuda(e);
+}
+
+size_t mha_fwd_host_workspace_size(int B, int H, int Lq, int Lk, int D, int dtype) {
+    HostPlan pl;
+    return host_plan(B, H, Lq, Lk, D, dtype, &pl) ? pl.total : 0;
+}
+
+int mha_fwd_host(const void *q, const void *k, const void *v, int mask_kind,
+                 const int32_t *kv_lengths, void *out, int B, int H, int Lq, int Lk, int D,
+                 float scale, int dtype, void *workspace, size_t workspace_bytes,
+                 cudaStream_t stream) {
+    int empty = 0;
+    int st = check_shape(B, H, Lq, Lk, D, scale, &empty);
+    if (st != MHA_OK) return st;
+    if (mask_kind < 0 || mask_kind > (MHA_MASK_CAUSAL | MHA_MASK_KV_LEN)) return MHA_ERR_INVALID_ARG;
+    if (dtype != MHA_F32 && dtype != MHA_BF16) return MHA_ERR_UNSUPPORTED;
+    if (empty) return MHA_OK;
+    if (!q || !out || (Lk > 0 && (!k || !v))) return MHA_ERR_INVALID_ARG;
+    const bool use_lens = (mask_kind & MHA_MASK_KV_LEN) != 0;
+    if (use_lens && !kv_lengths) return MHA_ERR_INVALID_ARG;
+    HostPlan pl;
+    if (!host_plan(B, H, Lq, Lk, D, dtype, &pl)) return MHA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < pl.total) return MHA_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return MHA_ERR_MISALIGNED;
+
+    // Two copy streams (in, out) and the events that order them with the
+    // kernels on `stream`; slot s's in-copy waits for the out-copy of the
+    // piece that used the slot before (which itself followed that piece's
+    // kernel).
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t start = nullptr, done_in[2] = {}, done_kernel[2] = {}, done_out[2] = {};
+    bool ok = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < 2; ++i)
+        ok = cudaEventCreateWithFlags(&done_in[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&done_kernel[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&done_out[i], cudaEventDisableTiming) == cudaSuccess;
+    // Everything already on `stream` (e.g. an earlier call using the same
+    // workspace) comes first.
+    ok = ok && cudaEventRecord(start, stream) == cudaSuccess &&
+         cudaStreamWaitEvent(s_in, start, 0) == cudaSuccess &&
+         cudaStreamWaitEvent(s_out, start, 0) == cudaSuccess;
+    char *ws = static_cast<char *>(workspace);
+    const int32_t *dlens = nullptr;
+    if (ok && use_lens) {
+        ok = cudaMemcpyAsync(ws + pl.off_lens, kv_lengths, sizeof(int32_t) * (size_t)B,
+                             cudaMemcpyHostToDevice, s_in) == cudaSuccess;
+        dlens = reinterpret_cast<const int32_t *>(ws + pl.off_lens);
+    }
+    st = ok ? MHA_OK : MHA_ERR_CUDA;
+    const int per_batch = H / pl.heads;
+    const int64_t pieces = (int64_t)B * per_batch;
+    for (int64_t c = 0; st == MHA_OK && c < pieces; ++c) {
+        const int b = (int)(c / per_batch), h0 = (int)(c % per_batch) * pl.heads, sl = (int)(c & 1);
+        char *slot = ws + sl * pl.slot;
+        const size_t first = (size_t)b * H + h0;   // first (b, h) problem of the piece
+        const char *qh = static_cast<const char *>(q) + first * pl.q_bytes / pl.heads;
+        char *oh = static_cast<char *>(out) + first * pl.q_bytes / pl.heads;
+        ok = cudaStreamWaitEvent(s_in, done_out[sl], 0) == cudaSuccess &&
+             cudaMemcpyAsync(slot, qh, pl.q_bytes, cudaMemcpyHostToDevice, s_in) == cudaSuccess;
+        if (ok && Lk > 0) {
+            const size_t koff = first * pl.k_bytes / pl.heads;
+            ok = cudaMemcpyAsync(slot + pl.off_k, static_cast<const char *>(k) + koff, pl.k_bytes,
+                                 cudaMemcpyHostToDevice, s_in) == cudaSuccess &&
+                 cudaMemcpyAsync(slot + pl.off_v, static_cast<const char *>(v) + koff, pl.k_bytes,
+                                 cudaMemcpyHostToDevice, s_in) == cudaSuccess;
+        }
+        ok = ok && cudaEventRecord(done_in[sl], s_in) == cudaSuccess &&
+             cudaStreamWaitEvent(stream, done_in[sl], 0) == cudaSuccess;
+        if (!ok) {
+            st = MHA_ERR_CUDA;
+            break;
+        }
+        st = mha_fwd(slot, Lk > 0 ? slot + pl.off_k : nullptr, Lk > 0 ? slot + pl.off_v : nullptr,
+                     mask_kind, dlens ? dlens + b : nullptr, slot + pl.off_out, 1, pl.heads, Lq, Lk,
+                     D, scale, dtype, stream);
+        if (st != MHA_OK) break;
+        ok = cudaEventRecord(done_kernel[sl], stream) == cudaSuccess &&
+             cudaStreamWaitEvent(s_out, done_kernel[sl], 0) == cudaSuccess &&
+             cudaMemcpyAsync(oh, slot + pl.off_out, pl.q_bytes, cudaMemcpyDeviceToHost, s_out) ==
+                 cudaSuccess &&
+             cudaEventRecord(done_out[sl], s_out) == cudaSuccess;
+        if (!ok) st = MHA_ERR_CUDA;
+    }
+    // Later work on `stream` follows every copy of the call (both copy
+    // streams end before their last event: the out-stream's last copy
+    // follows the last kernel, which followed the last in-copy).
+    cudaEvent_t end = nullptr;
+    if (s_in && s_out && cudaEventCreateWithFlags(&end, cudaEventDisableTiming) == cudaSuccess) {
+        bool j = cudaEventRecord(end, s_out) == cudaSuccess &&
+                 cudaStreamWaitEvent(stream, end, 0) == cudaSuccess &&
+                 cudaEventRecord(end, s_in) == cudaSuccess &&
+                 cudaStreamWaitEvent(stream, end, 0) == cudaSuccess;
+        if (!j && st == MHA_OK) st = MHA_ERR_CUDA;
+        cudaEventDestroy(end);
+    } else if (st == MHA_OK) {
+        st = MHA_ERR_CUDA;
+    }
+    // Released once the device has finished with them.
+    for (int i = 0; i < 2; ++i) {
+        if (done_in[i]) cudaEventDestroy(done_in[i]);
+        if (done_kernel[i]) cudaEventDestroy(done_kernel[i]);
+        if (done_out[i]) cudaEventDestroy(done_out[i]);
+    }
+    if (start) cudaEventDestroy(start);
+    if (s_in) cudaStreamDestroy(s_in);
+    if (s_out) cudaStreamDestroy(s_out);
+    return st;
 }
 
 size_t mha_bwd_workspace_size(int B, int H, int Lq, int D, int dtype) {

@@ -30,6 +30,9 @@ def L():
     lib.mha_bwd_workspace_size.argtypes = [i, i, i, i, i]
     lib.mha_bwd_workspace_size.restype = ctypes.c_size_t
     lib.mha_test_set_device_status.argtypes = [i, ctypes.c_uint32]
+    lib.mha_fwd_host.argtypes = [P, P, P, i, P, P, i, i, i, i, i, f, i, P, ctypes.c_size_t, P]
+    lib.mha_fwd_host_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.mha_fwd_host_workspace_size.restype = ctypes.c_size_t
     return lib
 
 
@@ -148,6 +151,45 @@ def bwd(L, q=A, k=A2, v=A3, o=OUT, g=G, lse=LSE, mask=0, lens=None, dq=DQ, dk=DK
 ])
 def test_bwd_host_validation(L, kw, want):
     assert bwd(L, **kw) == want
+
+
+def fwd_host(L, q=A, k=A2, v=A3, mask=0, lens=None, out=OUT, B=2, H=2, Lq=8, Lk=8, D=64,
+             scale=0.125, dtype=1, ws=WS, ws_bytes=1 << 30):
+    return L.mha_fwd_host(q, k, v, mask, lens, out, B, H, Lq, Lk, D, scale, dtype, ws, ws_bytes,
+                          None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), INVALID), (dict(out=None), INVALID), (dict(v=None), INVALID),
+    (dict(mask=2, lens=None), INVALID), (dict(mask=4), INVALID), (dict(scale=0.0), INVALID),
+    (dict(D=96), UNSUPPORTED), (dict(dtype=3), UNSUPPORTED),
+    (dict(ws=None), INVALID), (dict(ws_bytes=1024), INVALID),
+    (dict(ws=ctypes.c_void_p(0xA0008)), MISALIGNED),
+    (dict(B=0), OK), (dict(Lq=0), OK),
+])
+def test_fwd_host_copies_validation(L, kw, want):
+    """mha_fwd_host (host tensors, pipelined copies) rejects bad arguments
+    before it creates a stream or copies anything."""
+    assert fwd_host(L, **kw) == want
+
+
+def test_fwd_host_workspace_size(L):
+    """Two slots of one piece (q, k, v, out of the largest divisor of H whose
+    piece holds at most 64 MB), each part rounded up to 256 bytes, plus the
+    lengths."""
+    r = lambda x: (x + 255) // 256 * 256
+    # long causal workload shape: 8 MB per head, pieces of 8 heads
+    q = 8 * 8192 * 128 * 2
+    assert L.mha_fwd_host_workspace_size(2, 32, 8192, 8192, 128, 1) == 2 * 4 * q + r(8)
+    # H = 5 (prime), small heads: one piece per batch
+    q, k = 5 * 100 * 64 * 4, 5 * 300 * 64 * 4
+    assert L.mha_fwd_host_workspace_size(3, 5, 100, 300, 64, 0) == 2 * (2 * r(q) + 2 * r(k)) + r(12)
+    # one head larger than a piece: pieces of one head
+    q = 65536 * 128 * 4
+    assert L.mha_fwd_host_workspace_size(1, 3, 65536, 65536, 128, 0) == 2 * 4 * q + r(4)
+    assert L.mha_fwd_host_workspace_size(0, 5, 70, 70, 64, 0) == 0
+    assert L.mha_fwd_host_workspace_size(3, 5, 70, 70, 96, 0) == 0
+    assert L.mha_fwd_host_workspace_size(3, 5, 70, 70, 64, 4) == 0
 
 
 def test_bwd_workspace_size(L):
