@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kDecThreads, R <= 2 ? 2 : 1)
     __shared__ float sQ[R][D];
     __shared__ DecPartial<D, R> sW[kDecWarps];   // per-warp partials
     __shared__ DecPartial<D, R> sC;              // this CTA's partial (read by cluster rank 0)
+    __shared__ __align__(16) float sP[kDecWarps][R][32];   // each warp's block weights
     extern __shared__ uint4 dec_smem[];          // [warp][32 keys][D] bf16 V staging
 
     const int split = blockIdx.x, nsplit = gridDim.x;
@@ -227,34 +228,43 @@ __global__ void __launch_bounds__(kDecThreads, R <= 2 ? 2 : 1)
             l[r] = fmaf(l[r], alpha, ps);
 #pragma unroll
             for (int c = 0; c < DC; ++c) o[r][c] *= alpha;
+            sP[warp][r][lane] = p[r];
         }
         // O += P V over the block's keys from the staged V rows; lane holds
-        // output columns lane*DC ...; rows past the range carry weight 0 (their
-        // p is 2^-inf).
+        // output columns lane*DC ...; the weights come four keys at a time
+        // from shared memory (one broadcast read).  Rows past the range carry
+        // weight 0 (their p is 2^-inf) and their staged V rows are finite
+        // copies, so a group of four is taken whole.
         cp_async_wait_all();
         __syncwarp();
         const int nk = min(32, k1 - base);
-#pragma unroll 8
-        for (int jj = 0; jj < 32; ++jj) {
-            if (jj >= nk) break;
-            const __nv_bfloat16 *vr = sVw + jj * D + lane * DC;
-            float vv[DC];
-            if (DC == 4) {
-                const uint2 u = *reinterpret_cast<const uint2 *>(vr);
-                vv[0] = bf_lo(u.x);
-                vv[1] = bf_hi(u.x);
-                vv[DC - 2] = bf_lo(u.y);
-                vv[DC - 1] = bf_hi(u.y);
-            } else {
-                const uint32_t u = *reinterpret_cast<const uint32_t *>(vr);
-                vv[0] = bf_lo(u);
-                vv[DC - 1] = bf_hi(u);
-            }
+#pragma unroll 2
+        for (int j0 = 0; j0 < 32; j0 += 4) {
+            if (j0 >= nk) break;
+            float4 p4[R];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float pj = __shfl_sync(0xffffffffu, p[r], jj);
+            for (int r = 0; r < R; ++r) p4[r] = *reinterpret_cast<const float4 *>(&sP[warp][r][j0]);
 #pragma unroll
-                for (int c = 0; c < DC; ++c) o[r][c] = fmaf(pj, vv[c], o[r][c]);
+            for (int jj = 0; jj < 4; ++jj) {
+                const __nv_bfloat16 *vr = sVw + (j0 + jj) * D + lane * DC;
+                float vv[DC];
+                if (DC == 4) {
+                    const uint2 u = *reinterpret_cast<const uint2 *>(vr);
+                    vv[0] = bf_lo(u.x);
+                    vv[1] = bf_hi(u.x);
+                    vv[DC - 2] = bf_lo(u.y);
+                    vv[DC - 1] = bf_hi(u.y);
+                } else {
+                    const uint32_t u = *reinterpret_cast<const uint32_t *>(vr);
+                    vv[0] = bf_lo(u);
+                    vv[DC - 1] = bf_hi(u);
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float pj = jj == 0 ? p4[r].x : jj == 1 ? p4[r].y : jj == 2 ? p4[r].z : p4[r].w;
+#pragma unroll
+                    for (int c = 0; c < DC; ++c) o[r][c] = fmaf(pj, vv[c], o[r][c]);
+                }
             }
         }
         __syncwarp();   // the slot is free for the next block's copies
