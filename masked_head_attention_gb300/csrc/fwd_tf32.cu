@@ -1,11 +1,12 @@
 // fwd_tf32.cu -- fused masked multi-head attention forward for fp32 inputs on
 // the sm_103a tensor cores, at fp32-level accuracy through a three-term TF32
 // split: every fp32 operand x is written as
-//     x = hi + lo,   hi = tf32(x),   lo = tf32(x - hi)
-// (tf32 keeps 10 explicit mantissa bits; x - hi is exact in fp32), and each
-// product as
+//     x = hi + lo,   hi = x truncated to tf32,   lo = x - hi
+// (tf32 keeps 10 explicit mantissa bits; x - hi is exact in fp32; the tensor
+// core itself truncates an fp32 word to tf32, so x is passed as hi and lo's
+// low bits are dropped below 2^-20 |x|), and each product as
 //     a b ~= a_hi b_hi + a_lo b_hi + a_hi b_lo
-// where the dropped a_lo b_lo is below 2^-22 |a b|.  S = Q K^T and O += P V
+// where the dropped a_lo b_lo is below 2^-20 |a b|.  S = Q K^T and O += P V
 // are each three tcgen05 kind::tf32 MMAs per K-step, accumulating in fp32 in
 // TMEM.  The softmax is the same online form as the other kernels.
 //
@@ -20,10 +21,11 @@
 //              asked).
 //   warps 4-7  converters: the Q tile's rows, times scale * log2(e), into
 //              hi / lo TMEM columns (the A operand of S, read from TMEM, so S
-//              arrives in the base-2 domain); each K tile into hi (in place)
-//              and lo in shared memory; each V tile into transposed hi / lo
-//              tiles (the B operand of P V, K-major: row = feature, 64 keys
-//              along the row), so every MMA operand is K-major.
+//              arrives in the base-2 domain); each K tile's lo beside it in
+//              shared memory (the raw tile is its hi); each V tile into
+//              transposed hi / lo tiles (the B operand of P V, K-major: row =
+//              feature, 64 keys along the row), so every MMA operand is
+//              K-major.
 //   warp 8     TMA producer: the Q tile per item, K and V tiles of 64 keys
 //              through two stages; key tiles past the causal limit or the
 //              valid length are never loaded.
@@ -172,27 +174,24 @@ __device__ __forceinline__ uint32_t box_off(int row, int col) {
     return (uint32_t)(row * 128 + ((((col >> 2) ^ (row & 7)) & 7) << 4) + (col & 3) * 4);
 }
 
-// x = hi + lo with hi holding 11 significant bits (a tf32 value) and lo the
-// rest, by Veltkamp's splitting (T. J. Dekker, "A floating-point technique
-// for extending the available precision", 1971): with sigma = 2^13 + 1,
-//     t = fl(sigma x),  hi = fl(t - fl(t - x)),  lo = fl(x - hi)  (exact),
-// so hi is x rounded to 11 bits and |lo| <= 2^-11 |x|.  lo (up to 13 bits)
-// is made a tf32 value by clearing its low 13 mantissa bits, an error below
-// 2^-21 |x|.  Done on pairs with the packed fp32x2 instructions (half the
-// issue slots of scalar ones); a - b is formed as fma(b, -1, a), which
-// rounds once exactly like the subtraction.  The _rn intrinsics are never
-// contracted into other FMAs, which would break the splitting.
+// x = hi + lo with hi = x's top 11 significant bits (its low 13 mantissa
+// bits cleared: a tf32 value) and lo = x - hi, exact in fp32 (x and hi share
+// their exponent and top bits).  The tensor core reads a tf32 operand from an
+// fp32 word by ignoring its low 13 mantissa bits -- measured on GB300 for
+// operands in shared memory and in TMEM: 8192 of 8192 products of random fp32
+// values equal the products of their truncations -- so x itself is passed as
+// hi, and lo's own bits beyond 11 are dropped by the same rule: |lo| < 2^-10
+// |x|, so that costs below 2^-20 |x|.  Done on pairs: two bit masks and one
+// packed fp32x2 FMA (x - hi formed as fma(hi, -1, x), one exact rounding).
+// The _rn intrinsic is never contracted into other FMAs.
 __device__ __forceinline__ void split_tf32x2(float2 v, uint32_t &hi0, uint32_t &hi1, uint32_t &lo0,
                                              uint32_t &lo1) {
-    const float2 m1 = make_float2(-1.f, -1.f);
-    const float2 t = __fmul2_rn(v, make_float2(8193.0f, 8193.0f));
-    const float2 d = __ffma2_rn(v, m1, t);   // t - v
-    const float2 h = __ffma2_rn(d, m1, t);   // t - (t - v)
-    const float2 l = __ffma2_rn(h, m1, v);   // v - hi, exact
-    hi0 = __float_as_uint(h.x);
-    hi1 = __float_as_uint(h.y);
-    lo0 = __float_as_uint(l.x) & 0xFFFFE000u;
-    lo1 = __float_as_uint(l.y) & 0xFFFFE000u;
+    hi0 = __float_as_uint(v.x);
+    hi1 = __float_as_uint(v.y);
+    const float2 h = make_float2(__uint_as_float(hi0 & 0xFFFFE000u), __uint_as_float(hi1 & 0xFFFFE000u));
+    const float2 l = __ffma2_rn(h, make_float2(-1.f, -1.f), v);   // v - hi, exact
+    lo0 = __float_as_uint(l.x);
+    lo1 = __float_as_uint(l.y);
 }
 
 __device__ __forceinline__ float row_lse2(float m2, float l) {
@@ -460,18 +459,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; ok && j < it.n; ++j) {
                 const uint32_t st = g & 1;
                 uint8_t *stage = base + kStage0 + st * kStageBytes;
-                // K: hi in place, lo beside it (same swizzled positions).
+                // K: the raw tile serves as hi in place; lo beside it (same
+                // swizzled positions).
                 ok = wwait(&bars->k_raw[st], (g >> 1) & 1, kSiteKFull);
                 if (!ok) break;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    float4 *ph = reinterpret_cast<float4 *>(stage + kKh) + c + 128 * i;
+                    const float4 *ph = reinterpret_cast<const float4 *>(stage + kKh) + c + 128 * i;
                     float4 *pl = reinterpret_cast<float4 *>(stage + kKl) + c + 128 * i;
                     const float4 x = *ph;
                     uint4 h, l;
                     split_tf32x2(make_float2(x.x, x.y), h.x, h.y, l.x, l.y);
                     split_tf32x2(make_float2(x.z, x.w), h.z, h.w, l.z, l.w);
-                    *reinterpret_cast<uint4 *>(ph) = h;
                     *reinterpret_cast<uint4 *>(pl) = l;
                 }
                 fence_proxy_async_smem();
