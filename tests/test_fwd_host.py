@@ -80,3 +80,19 @@ def test_fwd_host_workspace_reused_by_consecutive_calls():
     assert torch.equal(out_a, mha.mha_fwd(dev(a[0]), dev(a[1]), dev(a[2]), 1).cpu())
     assert torch.equal(out_b, mha.mha_fwd(dev(b[0]), dev(b[1]), dev(b[2]), 1).cpu())
     assert mha.device_status() == 0
+
+
+@pytest.mark.gpu
+def test_fwd_host_no_keys_and_single_head():
+    """Lk = 0 gives zeros (k and v may be empty); one batch of one head is a
+    single piece."""
+    q = randn((2, 3, 50, 64), 451, 1.0, torch.bfloat16).pin_memory()
+    e = torch.empty((2, 3, 0, 64), dtype=torch.bfloat16)
+    out = mha.mha_fwd_host(q, e, e, 0, None)
+    torch.cuda.synchronize()
+    assert torch.equal(out, torch.zeros_like(q))
+    q, k, v = _inputs(1, 1, 130, 257, 128, torch.float32, 461)
+    got = mha.mha_fwd_host(q, k, v, 1, None)
+    torch.cuda.synchronize()
+    assert torch.equal(got, mha.mha_fwd(dev(q), dev(k), dev(v), 1).cpu())
+    assert mha.device_status() == 0
