@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kDecThreads, R <= 2 ? 2 : 1)
     pdl_wait();      // the stream's previous kernel has completed; its writes are visible
     pdl_trigger();   // the next kernel may be scheduled
     constexpr int DC = D / 32;   // output columns per lane
-    __shared__ float sQ[R][D];
+    __shared__ __align__(16) uint32_t sQ2[R][D / 2];   // Q rows as bf16 pairs (as given)
     __shared__ DecPartial<D, R> sW[kDecWarps];   // per-warp partials
     __shared__ DecPartial<D, R> sC;              // this CTA's partial (read by cluster rank 0)
     __shared__ __align__(16) float sP[kDecWarps][R][32];   // each warp's block weights
@@ -155,9 +155,9 @@ __global__ void __launch_bounds__(kDecThreads, R <= 2 ? 2 : 1)
     const __nv_bfloat16 *Qg = q + (size_t)bh * Lq * D;
     const __nv_bfloat16 *Kg = k + (size_t)bh * Lk * D;
     const __nv_bfloat16 *Vg = v + (size_t)bh * Lk * D;
-    for (int e = tid; e < R * D; e += kDecThreads) {
-        const int r = e / D, d = e % D;
-        sQ[r][d] = r < Lq ? __bfloat162float(Qg[(size_t)r * D + d]) : 0.f;
+    for (int e = tid; e < R * D / 2; e += kDecThreads) {
+        const int r = e / (D / 2), d2 = e % (D / 2);
+        sQ2[r][d2] = r < Lq ? reinterpret_cast<const uint32_t *>(Qg + (size_t)r * D)[d2] : 0u;
     }
     __syncthreads();
 
@@ -204,9 +204,14 @@ __global__ void __launch_bounds__(kDecThreads, R <= 2 ? 2 : 1)
             const float kf[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
                                  bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+            for (int r = 0; r < R; ++r) {
+                // Eight Q elements in one broadcast read.
+                const uint4 qv = *reinterpret_cast<const uint4 *>(&sQ2[r][c8 * 4]);
+                const float qf[8] = {bf_lo(qv.x), bf_hi(qv.x), bf_lo(qv.y), bf_hi(qv.y),
+                                     bf_lo(qv.z), bf_hi(qv.z), bf_lo(qv.w), bf_hi(qv.w)};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) s[r] = fmaf(sQ[r][c8 * 8 + e], kf[e], s[r]);
+                for (int e = 0; e < 8; ++e) s[r] = fmaf(qf[e], kf[e], s[r]);
+            }
         }
         // Mask, block max, rescale, exponentials, row sums (base 2).
         float p[R];
