@@ -284,6 +284,30 @@ class GpuWorkload:
         return n
 
 
+class nvtx_range:
+    """An NVTX range around a phase of the run (visible to a profiler's
+    timeline); a no-op where NVTX is unavailable."""
+
+    def __init__(self, name):
+        self.name = name
+        self.pushed = False
+
+    def __enter__(self):
+        try:
+            torch.cuda.nvtx.range_push(self.name)
+            self.pushed = True
+        except Exception:
+            pass
+        return self
+
+    def __exit__(self, *a):
+        if self.pushed:
+            try:
+                torch.cuda.nvtx.range_pop()
+            except Exception:
+                pass
+
+
 def time_steps(wl, steps, warmup, sync_ranks=None):
     """Warm up, then time exactly `steps` back-to-back steps between two CUDA
     events on the launching stream; returns the total in ms.
@@ -301,11 +325,12 @@ def time_steps(wl, steps, warmup, sync_ranks=None):
         sync_ranks()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    t0.record(stream)
-    for _ in range(steps):
-        wl.step()
-    t1.record(stream)
-    torch.cuda.synchronize()
+    with nvtx_range("timed %d steps: %s" % (steps, wl.w.name)):
+        t0.record(stream)
+        for _ in range(steps):
+            wl.step()
+        t1.record(stream)
+        torch.cuda.synchronize()
     if sync_ranks:
         sync_ranks()
     return t0.elapsed_time(t1)
@@ -350,11 +375,12 @@ def time_e2e(wl, steps, warmup):
         one()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        one()
-    b.record()
-    torch.cuda.synchronize()
+    with nvtx_range("e2e %d steps: %s" % (steps, w.name)):
+        a.record()
+        for _ in range(steps):
+            one()
+        b.record()
+        torch.cuda.synchronize()
     return a.elapsed_time(b) / steps, path
 
 
