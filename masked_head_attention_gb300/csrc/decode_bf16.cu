@@ -44,34 +44,6 @@ constexpr int kDecRankMaxB = 256;
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Whole-cluster barrier (every thread of every CTA of the cluster arrives;
-// release / acquire order the shared-memory writes before it with the reads
-// after it).
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address of `p` (this CTA's shared memory) in the shared memory of cluster
-// CTA `rank`, for ld.shared::cluster.
-__device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 // Partial result of a set of keys for R query rows: running max (base-2
 // logits), sum of 2^(s - max), and O = sum of 2^(s - max) V.
 template <int D, int R>

@@ -29,11 +29,15 @@
 //              softmax warpgroups: 384 threads launch with 168 registers each
 //              (64512); after the split 2 x 128 x 200 + 128 x 104 = 64512,
 //              i.e. 504 per lane on each SM sub-partition (limit 512).
-// Pre-LN: a work chunk is G consecutive items of one CTA, the heads of one
-// 256-row block of x; when a chunk starts, each softmax warp forms its 32 rows'
-// mean and 1/sqrt(var + eps) from the full rows of x (in fp32, inside this
-// kernel: no scratch in global memory), keeps them in registers for the G
-// items and prefetches the next chunk's rows into L2.
+// Pre-LN: a work chunk is G consecutive items of one CTA, G heads of one
+// 256-row block of x.  Before the roles start, the CTA's warps form the mean
+// and 1/sqrt(var + eps) of every row of its chunks from the full rows of x (in
+// fp32, inside this kernel: no scratch in global memory) into shared memory;
+// with clusters of two CTAs, which take two head groups of the same blocks,
+// each forms half of the rows and stores them in both.  Where shared memory
+// cannot hold them all (D = 128), each softmax warp forms its 32 rows' when a
+// chunk starts and prefetches the next chunk's rows into L2.  Chunks are
+// ordered by decreasing visible length of their batch.
 // All hand-offs are mbarriers (TMA transaction counts, tcgen05.commit, thread
 // arrivals); every wait is bounded.
 //
@@ -83,6 +87,12 @@ constexpr int kL2GroupDenom = 2;
 // Pre-LN row statistics: rows a softmax warp takes at once (all their loads
 // in flight together) at the chunk starts inside its item loop.
 constexpr int kStatsRows = 2;
+// Pre-LN: chunks are ordered by decreasing visible length of their batch
+// (each CTA ranks the batch lengths itself) when there are at most this many
+// batches.
+constexpr int kMaxSortB = 128;
+// Pre-LN statistics prologue: at most this many chunks per CTA.
+constexpr int kProMaxChunks = 32;
 
 struct AttnParams {
     CUtensorMap tm_q;     // Q [B*H][Lq][D]; Pre-LN: x [B][Lq][H*D]; box {64, 128, 1}
@@ -109,6 +119,9 @@ struct AttnParams {
     int N;                // Pre-LN: features per row of x (H * D)
     float eps;
     int stats_src;        // Pre-LN: 0 = statistics formed in this kernel, 1 = read from ln_stats
+    int pre_chunks;       // Pre-LN: chunks per CTA whose statistics the prologue forms (0: none)
+    int cs;               // CTAs per cluster; > 1 only for the Pre-LN prologue, whose cluster
+                          // CTAs take cs head groups of the same blocks and share the statistics
 };
 
 struct __align__(8) Bars {
@@ -121,6 +134,9 @@ struct __align__(8) Bars {
     uint64_t drain;       // teardown after an abort
     uint32_t tmem_base;
     int abort;
+    int sorted;           // Pre-LN: batches taken in the order ord[]
+    int ord[kMaxSortB];   // Pre-LN: batch at length rank r
+    int len[kMaxSortB];   // Pre-LN: clamped visible length of batch b
 };
 
 template <int D>
@@ -138,6 +154,15 @@ struct Cfg {
     static constexpr uint32_t kBars = kO + 8 * kStageWarp;
     static constexpr size_t kSmem = 1024 + kBars + sizeof(Bars);
     static_assert(kSmem <= 232448, "227 KB of shared memory per CTA");
+    // Pre-LN: the row statistics of the CTA's first chunks (256 float2 per
+    // chunk), formed before the roles start, in what shared memory is left.
+    static constexpr uint32_t kStats = (kBars + (uint32_t)sizeof(Bars) + 15u) & ~15u;
+    static constexpr uint32_t kChunkStatsBytes = 2 * kTileRows * sizeof(float2);
+    static constexpr int kPreChunksFit = (int)((232448u - 1024u - kStats) / kChunkStatsBytes);
+    static constexpr int kPreChunksMax = kPreChunksFit < kProMaxChunks ? kPreChunksFit : kProMaxChunks;
+    static size_t smem_prenorm(int pre_chunks) {
+        return pre_chunks > 0 ? 1024 + kStats + (size_t)pre_chunks * kChunkStatsBytes : kSmem;
+    }
     static constexpr uint32_t kColO0 = 256;                // O_i at 256 + i * D; S_i at i * 128
     // P_i (bf16 pairs, 64 columns): in its own columns when D = 64 leaves
     // room (384 + 64 i); for D = 128 over the first half of S_i, where the
@@ -158,18 +183,21 @@ struct Item {
 // heaviest) 256-row query blocks come first and the (b, h) index varies
 // fastest, so CTAs running at the same time share K/V tiles through L2.
 // Pre-LN: chunk c (items c*G .. c*G + G - 1) is the head group c % n_hg of
-// 256-row block (c / n_hg) % n_pairs of batch c / (n_pairs * n_hg); its G
+// 256-row block (c / n_hg) % n_pairs of the batch of length rank
+// c / (n_pairs * n_hg) (ord[]: longest visible length first, so the
+// persistent walk hands out the heavy chunks first; or batch order); its G
 // items are that block's heads in order, so one set of row statistics serves
 // the whole chunk, and the n_hg chunks of one block (which read the same rows
 // of x) run side by side on different SMs.
 template <bool PRENORM>
-__device__ __forceinline__ Item decode_item(const AttnParams &p, int item) {
+__device__ __forceinline__ Item decode_item(const AttnParams &p, int item, const int *ord) {
     Item it;
     if (PRENORM) {
         const int c = item / p.G, sub = item - c * p.G;
         const int per_b = p.n_pairs * p.n_hg;
-        it.b = c / per_b;
-        const int rem = c - it.b * per_b;
+        const int rb = c / per_b;
+        it.b = ord != nullptr ? ord[rb] : rb;
+        const int rem = c - rb * per_b;
         const int pr = p.n_pairs - 1 - rem / p.n_hg;
         it.h = (rem % p.n_hg) * p.G + sub;
         it.bh = it.b * p.H + it.h;
@@ -269,6 +297,7 @@ __device__ __forceinline__ void ln_stats_warp(const __nv_bfloat16 *const (&xr)[R
     uint4 u[R][kSeg];
     float2 acc[R];
     float mean[R];
+    const float inv_n = 1.0f / (float)N;
     auto load_seg = [&](int sg) {
 #pragma unroll
         for (int r = 0; r < R; ++r)
@@ -295,7 +324,7 @@ __device__ __forceinline__ void ln_stats_warp(const __nv_bfloat16 *const (&xr)[R
         float s = acc[r].x + acc[r].y;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        mean[r] = s / (float)N;
+        mean[r] = s * inv_n;
         acc[r] = make_float2(0.f, 0.f);
     }
     for (int sg = 0; sg < nseg; ++sg) {
@@ -312,7 +341,7 @@ __device__ __forceinline__ void ln_stats_warp(const __nv_bfloat16 *const (&xr)[R
         float q = acc[r].x + acc[r].y;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
-        st[r] = make_float2(mean[r], rsqrtf(q / (float)N + eps));
+        st[r] = make_float2(mean[r], rsqrtf(q * inv_n + eps));
     }
 }
 
@@ -422,16 +451,24 @@ __device__ __forceinline__ float2 warp_rows_stats(const AttnParams &p, int b, in
 // Item sequence of a CTA: a persistent grid walks the ordered item list in
 // rounds of gridDim.x, forward in even rounds and backward in odd ones, so a
 // CTA that drew a heavy item early draws a light one next (a static
-// approximation of longest-processing-time-first).
+// approximation of longest-processing-time-first).  With clusters of cs CTAs
+// the clusters walk units of cs consecutive chunks the same way, and cluster
+// CTA k takes chunk k of each unit.
 struct ItemIter {
     int r = 0, idx = -1;
+    int cs;   // CTAs per cluster: a cluster walks units of cs consecutive chunks
+    __device__ explicit ItemIter(int cs_) : cs(cs_) {}
     __device__ __forceinline__ bool next(int n_items) {
-        const int G = gridDim.x, c = blockIdx.x;
+        const int W = gridDim.x / cs, w = blockIdx.x / cs, rank = blockIdx.x - w * cs;
+        const int n_units = n_items / cs;
         for (;;) {
-            if ((long long)r * G >= n_items) return false;
-            idx = (r & 1) ? (r + 1) * G - 1 - c : r * G + c;
+            if ((long long)r * W >= n_units) return false;
+            const int u = (r & 1) ? (r + 1) * W - 1 - w : r * W + w;
             ++r;
-            if (idx < n_items) return true;
+            if (u < n_units) {
+                idx = u * cs + rank;
+                return true;
+            }
         }
     }
 };
@@ -449,7 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // A bounded wait that expired earlier leaves g_status set; later launches
     // then return at once instead of timing out again.
-    if (wait_expired_before()) return;
+    if (wait_expired_before()) {
+        // A cluster peer that read the word a moment earlier may still write
+        // statistics into this CTA's shared memory: meet it first.
+        if (PRENORM && p.cs > 1) cluster_sync_all();
+        return;
+    }
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -483,6 +525,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         bars->abort = 0;
         mbar_fence_init();
     }
+    // Pre-LN: batch order by visible length (rank = number of batches before it).
+    const bool sorted = PRENORM && p.kv_lengths != nullptr && p.B > 1 && p.B <= kMaxSortB;
+    if (sorted) {
+        for (int b = threadIdx.x; b < p.B; b += kThreads)
+            bars->len[b] = max(0, min((int)p.kv_lengths[b], p.Lk));
+        __syncthreads();
+        for (int b = threadIdx.x; b < p.B; b += kThreads) {
+            const int lb = bars->len[b];
+            int rank = 0;
+            for (int u = 0; u < p.B; ++u) {
+                const int lu = bars->len[u];
+                rank += (lu > lb || (lu == lb && u < b)) ? 1 : 0;
+            }
+            bars->ord[rank] = b;
+        }
+    }
+    const int *ord = sorted ? bars->ord : nullptr;
     if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
@@ -497,6 +556,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+
+    // Pre-LN with the statistics formed here: before the roles start, all 12
+    // warps form the row statistics of the CTA's first pre_chunks chunks into
+    // shared memory, four rows per warp at a time (nothing else runs yet, so
+    // the loads of 48 rows are in flight at once and no role waits on them).
+    // In a cluster of cs CTAs (which run chunks of the same blocks) CTA k
+    // forms rows [k 256/cs, (k + 1) 256/cs) of each block and stores them in
+    // every CTA of the cluster.  Chunks past those form theirs when they
+    // start (softmax warps).
+    float2 *s_stats = reinterpret_cast<float2 *>(base + C::kStats);
+    const int pre_chunks = PRENORM && p.stats_src == 0 ? p.pre_chunks : 0;
+    if (PRENORM && pre_chunks > 0) {
+        const int cs = p.cs;
+        const int rank = (int)(blockIdx.x % (unsigned)cs);
+        const int part = 2 * kTileRows / cs;   // rows of a block this CTA forms
+        const int groups_per_chunk = part / 4;
+        ItemIter iter(p.cs);
+        int ci = -1;
+        Item it{};
+        for (int grp = warp;; grp += kThreads / 32) {
+            const int want = grp / groups_per_chunk;
+            if (want >= pre_chunks) break;
+            bool more = true;
+            while (ci < want && (more = iter.next(p.n_chunks))) {
+                it = decode_item<PRENORM>(p, iter.idx * G, ord);
+                ++ci;
+            }
+            if (!more) break;
+            const int rr = rank * part + (grp - want * groups_per_chunk) * 4;
+            const __nv_bfloat16 *xr[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int row = it.q0 + rr + r;
+                xr[r] = row < p.Lq ? p.x + ((size_t)it.b * p.Lq + row) * (size_t)p.N : nullptr;
+            }
+            float2 st[4];
+            ln_stats_warp<4>(xr, p.N, p.eps, lane, st);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (lane == r) {
+                    float2 *dst = &s_stats[want * 2 * kTileRows + rr + r];
+                    *dst = st[r];
+                    for (int k = 1; k < cs; ++k)
+                        st_cluster_f32x2(map_to_rank(dst, (uint32_t)((rank + k) % cs)), st[r]);
+                }
+        }
+        // The cluster barrier also orders the peers' stores before the reads.
+        if (cs > 1)
+            cluster_sync_all();
+        else
+            __syncthreads();
+    }
 
     if (warp >= 8) {
     setmaxnreg_dec<kControlRegs>();
@@ -524,10 +635,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++g;
                 return true;
             };
-            ItemIter iter;
+            ItemIter iter(p.cs);
             while (ok && iter.next(p.n_chunks))
                 for (int sub = 0; ok && sub < G; ++sub) {
-                const Item it = decode_item<PRENORM>(p, iter.idx * G + sub);
+                const Item it = decode_item<PRENORM>(p, iter.idx * G + sub, ord);
                 // The first key tiles go out before this item's Q tiles, whose
                 // buffers the previous item may still be reading.
                 const int pre = min(it.J, S);
@@ -595,10 +706,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Under a test's short wait limit: a wait that must expire (the drain
         // phase completes only at teardown).
         if (wait_limit_is_test()) ok = wwait(&bars->drain, 0, kSiteTest);
-        ItemIter iter;
+        ItemIter iter(p.cs);
         while (ok && iter.next(p.n_chunks))
             for (int sub = 0; ok && sub < G; ++sub) {
-            const Item it = decode_item<PRENORM>(p, iter.idx * G + sub);
+            const Item it = decode_item<PRENORM>(p, iter.idx * G + sub, ord);
             // Every item passes through both Q barriers, with or without work
             // for the tile, so no role can run two phases ahead of another.
 #pragma unroll
@@ -742,20 +853,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++wgp;
             return r;
         };
-        // Pre-LN: this thread's row statistics, formed when a chunk starts (the
-        // chunk's G items share the rows).
+        // Pre-LN: this thread's row statistics, taken when a chunk starts (the
+        // chunk's G items share the rows): from the prologue's shared-memory
+        // table for the CTA's first pre_chunks chunks, else formed here.
         float2 st_row = make_float2(0.f, 0.f);
-        ItemIter iter;
+        int kc = -1;   // chunks started so far - 1
+        ItemIter iter(p.cs);
         while (ok && iter.next(p.n_chunks))
             for (int sub = 0; ok && sub < G; ++sub) {
-            const Item it = decode_item<PRENORM>(p, iter.idx * G + sub);
+            const Item it = decode_item<PRENORM>(p, iter.idx * G + sub, ord);
             const int n = wg ? it.n[1] : it.n[0];
             const int q0i = it.q0 + wg * kTileRows;
             const int row = q0i + t;
             if (PRENORM && sub == 0) {
+                ++kc;
                 if (p.stats_src == 1) {
                     st_row = row < p.Lq ? p.ln_stats[(size_t)it.b * p.Lq + row]
                                         : make_float2(0.f, 0.f);
+                } else if (kc < pre_chunks) {
+                    st_row = s_stats[kc * 2 * kTileRows + wg * kTileRows + t];
                 } else {
                     // This warp's 32 rows, kStatsRows at a time; then the
                     // next chunk's rows go to L2, ready when that chunk starts.
@@ -763,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st_row = warp_rows_stats<kStatsRows>(p, it.b, rw, lane);
                     ItemIter peek = iter;
                     if (lane == 0 && peek.next(p.n_chunks)) {
-                        const Item nx = decode_item<PRENORM>(p, peek.idx * G);
+                        const Item nx = decode_item<PRENORM>(p, peek.idx * G, ord);
                         prefetch_x_rows(p, nx.b, nx.q0 + wg * kTileRows + 32 * (warp & 3), 32);
                     }
                 }
@@ -1145,20 +1261,33 @@ namespace {
 thread_local int g_grid_override = 0;
 
 template <int D, bool PRENORM>
-cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
-    constexpr size_t smem = Cfg<D>::kSmem;
-    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_fwd_bf16_kernel<D, PRENORM>), smem);
+cudaError_t launch_attn(const AttnParams &p, int grid, cudaStream_t stream) {
+    using C = Cfg<D>;
+    // The attribute is set once per kernel and device, to the largest size
+    // any launch of the kernel asks for.
+    const size_t smem_max = PRENORM ? C::smem_prenorm(C::kPreChunksMax) : C::kSmem;
+    const size_t smem = PRENORM ? C::smem_prenorm(p.pre_chunks) : C::kSmem;
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(attn_fwd_bf16_kernel<D, PRENORM>),
+                                   smem_max);
     if (e != cudaSuccess) return e;
-    // Persistent grid: one CTA per SM (one fits per SM), unless overridden.
-    int grid = g_grid_override > 0 ? g_grid_override : device_info().sms;
-    if (grid > p.n_chunks) grid = p.n_chunks;
+    cudaLaunchAttribute cluster;
+    cluster.id = cudaLaunchAttributeClusterDimension;
+    cluster.val.clusterDim.x = (unsigned)p.cs;
+    cluster.val.clusterDim.y = 1;
+    cluster.val.clusterDim.z = 1;
     return launch_kernel(attn_fwd_bf16_kernel<D, PRENORM>, dim3(grid), dim3(kThreads), smem, stream,
-                         nullptr, p);
+                         p.cs > 1 ? &cluster : nullptr, p);
 }
 
 }  // namespace
 
 void set_bf16_grid_override(int ctas) { g_grid_override = ctas; }
+
+// Pre-LN: most chunks per CTA whose statistics the prologue can hold in
+// shared memory (0 at D = 128, whose tiles leave no room).
+static int prologue_chunks_max(int D) {
+    return D == 64 ? Cfg<64>::kPreChunksMax : Cfg<128>::kPreChunksMax;
+}
 
 cudaError_t status_ctl_fwd_bf16(int op, uint64_t value, uint32_t *bits) {
     return unit_status_ctl(op, value, bits);
@@ -1254,21 +1383,34 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     p.n_pairs = (c.Lq + 2 * kTileRows - 1) / (2 * kTileRows);
     p.n_items = (int)(BH * (uint64_t)p.n_pairs);
     p.G = 1;
+    // Persistent grid: one CTA per SM (one fits per SM), unless overridden.
+    int grid = g_grid_override > 0 ? g_grid_override : device_info().sms;
     if (prenorm) {
-        // Heads per chunk: a chunk forms its rows' statistics once for its G
-        // items, at a cost of about 2.2 N/Lk items' worth of work (N features
-        // per row of x against Lk keys per row of attention; the factor is
-        // measured on the Pre-LN workload), while larger chunks leave a longer
-        // tail (about G/2 items) when the persistent grid runs out of chunks.
-        // Take the divisor of H that minimises
-        //     items per CTA * (1 + 2.2 (N / Lk) / G) + G / 2.
-        const int grid = g_grid_override > 0 ? g_grid_override : device_info().sms;
-        const double per_cta = (double)p.n_items / (double)grid;
-        const double stats = 2.2 * (double)(c.H * c.D) / (double)(c.Lk > 0 ? c.Lk : 1);
+        // Heads per chunk.  A chunk forms its rows' statistics once for its G
+        // items, and a CTA runs at most ceil(chunks / grid) chunks.  Where the
+        // prologue can hold the statistics of all of a CTA's chunks (D = 64),
+        // forming them costs about kPre N/Lk items' worth of work per chunk,
+        // shared by the kPair CTAs of a cluster when the head groups pair up;
+        // at the chunk starts inside the item loop about kLoop N/Lk (N
+        // features per row of x against Lk keys per row of attention; both
+        // factors measured on the Pre-LN workload); statistics read from the
+        // caller's array cost nothing.  Take the divisor of H that minimises
+        //     ceil(chunks / grid) * (G + factor * N / Lk).
+        // (Clusters of two CTAs all fit at once, one per SM; clusters of four
+        // left 8 of 152 SMs idle.)
+        constexpr double kPre = 1.0, kLoop = 2.2;
+        constexpr int kPair = 2;
+        const int pre_max = prologue_chunks_max(c.D);
+        const double ratio = (double)(c.H * c.D) / (double)(c.Lk > 0 ? c.Lk : 1);
         double best = 0.0;
         for (int g = 1; g <= c.H; ++g) {
             if (c.H % g != 0) continue;
-            const double cost = per_cta * (1.0 + stats / g) + 0.5 * g;
+            const long long chunks = (long long)p.n_items / g;
+            const long long per_cta = (chunks + grid - 1) / grid;
+            const bool pre = ln_stats == nullptr && per_cta <= pre_max;
+            const bool pair = pre && (c.H / g) % kPair == 0 && grid % kPair == 0;
+            const double factor = ln_stats != nullptr ? 0.0 : pre ? kPre / (pair ? kPair : 1) : kLoop;
+            const double cost = (double)per_cta * (g + factor * ratio);
             if (g == 1 || cost < best) {
                 best = cost;
                 p.G = g;
@@ -1281,6 +1423,19 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
         p.stats_src = ln_stats != nullptr ? 1 : 0;
     }
     p.n_chunks = p.n_items / p.G;
+    if (grid > p.n_chunks) grid = p.n_chunks;
+    p.cs = 1;
+    if (prenorm && ln_stats == nullptr) {
+        const int pre_max = prologue_chunks_max(c.D);
+        const int per_cta = (p.n_chunks + grid - 1) / grid;
+        p.pre_chunks = per_cta < pre_max ? per_cta : pre_max;
+        // Two CTAs of a cluster take two head groups of the same blocks and
+        // form half of each block's row statistics each.
+        if (p.pre_chunks == per_cta && p.n_hg % 2 == 0 && grid % 2 == 0) {
+            p.cs = 2;
+            p.pre_chunks = (p.n_chunks / 2 + grid / 2 - 1) / (grid / 2);
+        }
+    }
     {
         // (b, h) problems per scheduling group: their K and V together take
         // at most 1/kL2GroupDenom of L2.
@@ -1299,9 +1454,11 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
                                                 stream);
             if (e != cudaSuccess) return e;
         }
-        return c.D == 64 ? launch_attn<64, true>(p, stream) : launch_attn<128, true>(p, stream);
+        return c.D == 64 ? launch_attn<64, true>(p, grid, stream)
+                         : launch_attn<128, true>(p, grid, stream);
     }
-    return c.D == 64 ? launch_attn<64, false>(p, stream) : launch_attn<128, false>(p, stream);
+    return c.D == 64 ? launch_attn<64, false>(p, grid, stream)
+                     : launch_attn<128, false>(p, grid, stream);
 }
 
 cudaError_t launch_selftest_umma(int variant, int kn, const void *a, const void *b, float *c,

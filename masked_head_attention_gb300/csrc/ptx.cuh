@@ -26,7 +26,7 @@ enum WaitSite : uint32_t {
     kSiteQFull = 0, kSiteKFull = 1, kSiteVFull = 2, kSiteKvEmpty = 3,
     kSiteSFull = 4, kSitePFull = 5, kSitePvDone = 6, kSiteQEmpty = 7,
     kSiteOFree = 8, kSiteDrain = 9, kSiteSelftest = 10, kSiteWg = 11,
-    kSiteStats = 12, kSiteTest = 13,
+    kSiteStats = 12, kSiteTest = 13,   // kSiteStats: Pre-LN statistics prologue
 };
 
 // Numeric flags, bits 16 and up of the same word ("softmax sum != 1 is an
@@ -189,6 +189,40 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
 __device__ __forceinline__ void prefetch_l2_bulk(const void *gptr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gptr)),
                  "r"(bytes)
+                 : "memory");
+}
+
+// ---------------------------- thread-block clusters -------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Whole-cluster barrier (every thread of every CTA of the cluster arrives;
+// release / acquire order the shared-memory writes before it with the reads
+// after it).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of `p` (this CTA's shared memory) in the shared memory of cluster
+// CTA `rank`, for ld/st.shared::cluster.
+__device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
                  : "memory");
 }
 

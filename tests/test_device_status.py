@@ -1,5 +1,6 @@
 """Failure detection without a GPU fault: every bounded device-side wait of
-the tensor-core kernels (bf16 forward, fp32 3xTF32 forward, bf16 backward)
+the tensor-core kernels (bf16 forward and its Pre-LN variant, fp32 3xTF32
+forward, bf16 backward)
 reports its expiry through mha_device_status, the word is cleared on
 request, and the next call with the normal limit is correct again.
 
@@ -46,6 +47,25 @@ def _bf16_fwd():
     return run, check
 
 
+def _prenorm_fwd():
+    """Pre-LN forward (row statistics formed inside the kernel first)."""
+    B, H, Lq, Lk, D = 2, 4, 300, 200, 64
+    x = randn((B, Lq, H * D), 71, 1.0, torch.bfloat16)
+    k, v = (randn((B, H, Lk, D), s, 1.0, torch.bfloat16) for s in (72, 73))
+    g = torch.linspace(0.5, 1.5, H * D, dtype=torch.float32)
+    b = torch.linspace(-0.2, 0.2, H * D, dtype=torch.float32)
+    lens = torch.tensor([200, 77], dtype=torch.int32)
+
+    def run():
+        return mha.prenorm_cross_attn_fwd(dev(x), dev(g), dev(b), 1e-5, dev(k), dev(v), dev(lens))
+
+    def check(out):
+        want = oracle.prenorm_cross_attn(x.float().numpy(), g.numpy(), b.numpy(), 1e-5,
+                                         k.float().numpy(), v.float().numpy(), lens.numpy())
+        check_bf16(as_np(out), want, "Pre-LN forward after expiry")
+    return run, check
+
+
 def _tf32_fwd():
     q, k, v = (randn((2, 2, 300, 64), s) for s in (64, 65, 66))
     lens = torch.tensor([300, 123], dtype=torch.int32)
@@ -79,8 +99,8 @@ def _bf16_bwd():
     return run, check
 
 
-CASES = {"bf16 forward": (_bf16_fwd, 0), "3xTF32 forward": (_tf32_fwd, 1),
-         "bf16 backward": (_bf16_bwd, 2)}
+CASES = {"bf16 forward": (_bf16_fwd, 0), "Pre-LN forward": (_prenorm_fwd, 0),
+         "3xTF32 forward": (_tf32_fwd, 1), "bf16 backward": (_bf16_bwd, 2)}
 
 
 @pytest.mark.gpu
