@@ -65,9 +65,10 @@ def test_prenorm_c4_sampled_rows():
 def test_prenorm_chunks_of_heads_share_row_statistics(D, ctas):
     """A capped grid makes the kernel group several heads of the same 256 rows
     into one chunk (the default grid runs one head per chunk at this size),
-    whose row statistics the softmax warps form once, and walk many chunks per
-    CTA, with empty and ragged batches.  The result must not depend on the
-    grouping."""
+    whose row statistics are formed once (D = 64: by the CTA's prologue, with
+    two CTAs a cluster pair splitting them; D = 128: by the softmax warps at
+    the chunk start), and walk many chunks per CTA, with empty and ragged
+    batches.  The result must not depend on the grouping."""
     B, H, Lq, Lk = 3, 4, 300, 260
     lens = [260, 0, 131]
     x, g, b, k, v = _inputs(B, H, Lq, Lk, D, 31)
@@ -88,6 +89,44 @@ def test_prenorm_chunks_of_heads_share_row_statistics(D, ctas):
     want = oracle.prenorm_cross_attn(x.float().numpy(), g.numpy(), b.numpy(), 1e-5,
                                      k.float().numpy(), v.float().numpy(), lens)
     check_bf16(as_np(out), want, "chunks D=%d ctas=%d" % (D, ctas))
+
+
+@pytest.mark.gpu
+def test_prenorm_more_chunks_than_the_prologue_holds():
+    """One CTA walking 40 chunks: the prologue forms the statistics of the
+    first 32 (its shared-memory table), the softmax warps those of the rest
+    at their chunk starts.  Every row against the oracle."""
+    B, H, Lq, Lk, D = 1, 1, 40 * 256 - 70, 100, 64
+    x, g, b, k, v = _inputs(B, H, Lq, Lk, D, 35)
+    args = (dev(x), dev(g), dev(b), 1e-5, dev(k), dev(v), None)
+    ref = mha.prenorm_cross_attn_fwd(*args)
+    try:
+        mha.set_bf16_grid(1)
+        out = mha.prenorm_cross_attn_fwd(*args)
+        torch.cuda.synchronize()
+    finally:
+        mha.set_bf16_grid(0)
+    assert mha.device_status() == 0
+    assert torch.equal(out, ref)
+    want = oracle.prenorm_cross_attn(x.float().numpy(), g.numpy(), b.numpy(), 1e-5,
+                                     k.float().numpy(), v.float().numpy(), None)
+    check_bf16(as_np(out), want, "40 chunks on one CTA")
+
+
+@pytest.mark.gpu
+def test_prenorm_many_batches_keep_index_order():
+    """More batches than the kernel ranks by length (128): chunks then run in
+    batch order; lengths include zero and values past Lk."""
+    B, H, Lq, Lk, D = 130, 2, 20, 50, 64
+    lens = [(7 * i) % 61 for i in range(B)]
+    x, g, b, k, v = _inputs(B, H, Lq, Lk, D, 37)
+    out = mha.prenorm_cross_attn_fwd(dev(x), dev(g), dev(b), 1e-5, dev(k), dev(v),
+                                     dev(lens_tensor(lens)))
+    torch.cuda.synchronize()
+    want = oracle.prenorm_cross_attn(x.float().numpy(), g.numpy(), b.numpy(), 1e-5,
+                                     k.float().numpy(), v.float().numpy(), lens)
+    check_bf16(as_np(out), want, "130 batches")
+    assert mha.device_status() == 0
 
 
 @pytest.mark.gpu
