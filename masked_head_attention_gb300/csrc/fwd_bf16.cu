@@ -251,6 +251,13 @@ __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// 16-byte store into the shared memory of another CTA of the cluster.
+__device__ __forceinline__ void st_cluster_u32x4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Pre-LN, step 1: per-row statistics of x [rows, N] ("How to fuse cross-
 // attention and layer-norm into a single CUDA kernel?" (cms365.cn), answer
@@ -262,9 +269,10 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 // registers between the passes when the row fits in one segment (N <= 1024);
 // it keeps two partial sums (the even and the odd elements) on packed fp32x2
 // instructions, adds them, and the lane sums meet in an xor butterfly, after
-// which every lane holds the same bits.  Both users -- the attention kernel's
-// softmax warps and the standalone pass of the no-allocation entry point --
-// call this routine, so they produce identical statistics.  A null row
+// which every lane holds the same bits.  Every user -- the attention
+// kernel's prologue and softmax warps, and the standalone pass of the
+// no-allocation entry point -- calls this routine, so they produce identical
+// statistics.  A null row
 // pointer gives unused values.
 // ---------------------------------------------------------------------------
 // Lane sums of one 16-byte chunk (eight bf16) on packed fp32x2 instructions:
@@ -595,18 +603,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             ln_stats_warp<4>(xr, p.N, p.eps, lane, st);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
-                if (lane == r) {
-                    float2 *dst = &s_stats[want * 2 * kTileRows + rr + r];
-                    *dst = st[r];
-                    for (int k = 1; k < cs; ++k)
-                        st_cluster_f32x2(map_to_rank(dst, (uint32_t)((rank + k) % cs)), st[r]);
-                }
+                if (lane == r) s_stats[want * 2 * kTileRows + rr + r] = st[r];
         }
-        // The cluster barrier also orders the peers' stores before the reads.
-        if (cs > 1)
+        __syncthreads();
+        if (cs > 1) {
+            // This CTA's part of every chunk's table goes to the other CTAs of
+            // the cluster, 16 bytes per store from every thread; the cluster
+            // barrier orders those stores before the reads.
+            int nch = 0;
+            ItemIter cnt(p.cs);
+            while (nch < pre_chunks && cnt.next(p.n_chunks)) ++nch;
+            const int vecs = part * (int)sizeof(float2) / 16;   // per chunk
+            for (int v = threadIdx.x; v < nch * vecs; v += kThreads) {
+                const int chunk = v / vecs;
+                const uint4 *src =
+                    reinterpret_cast<const uint4 *>(&s_stats[chunk * 2 * kTileRows + rank * part]) +
+                    (v - chunk * vecs);
+                const uint4 val = *src;
+                for (int k = 1; k < cs; ++k)
+                    st_cluster_u32x4(map_to_rank(src, (uint32_t)((rank + k) % cs)), val);
+            }
             cluster_sync_all();
-        else
-            __syncthreads();
+        }
     }
 
     if (warp >= 8) {
