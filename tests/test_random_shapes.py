@@ -9,7 +9,7 @@ import torch
 
 import masked_head_attention_gb300 as mha
 import oracle
-from parity_util import as_np, check_bf16, check_f32, dev, lens_tensor, randn
+from parity_util import as_np, check_bf16, check_bf16_sum, check_f32, dev, lens_tensor, randn
 
 N_CASES = 40
 
@@ -62,4 +62,49 @@ def test_random_shape(i):
     assert np.array_equal(np.isfinite(got_lse), fin), what + ": rows with no visible key"
     if fin.any():
         assert np.max(np.abs(got_lse[fin] - want_lse[fin])) <= 1e-3, what + ": lse"
+    assert mha.device_status() == 0
+
+
+N_PRENORM_CASES = 24
+
+
+def _prenorm_case(i):
+    r = np.random.default_rng(3000 + i)
+    B = int(r.integers(1, 4))
+    H = int(r.choice([1, 2, 3, 4, 6, 8]))
+    D = int(r.choice([64, 128]))
+    Lq = int(r.choice([1, 7, 130, 256, 257, int(r.integers(1, 800))]))
+    Lk = int(r.choice([1, 64, 129, int(r.integers(1, 700))]))
+    lens = None
+    if r.random() < 0.6:
+        lens = [int(x) for x in r.integers(0, Lk + 30, size=B)]
+    shift = float(r.choice([0.0, 0.5, 4.0]))   # row means away from zero
+    std = float(r.choice([0.5, 1.0, 2.0]))
+    residual = bool(r.random() < 0.4)
+    return B, H, Lq, Lk, D, lens, shift, std, residual
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("i", range(N_PRENORM_CASES))
+def test_random_prenorm_shape(i):
+    """Pre-LN cross-attention (with and without the residual add) on seeded
+    random shapes: head counts that do and do not pair into clusters, both
+    head sizes, ragged and empty batches, rows with non-zero means."""
+    B, H, Lq, Lk, D, lens, shift, std, residual = _prenorm_case(i)
+    what = "prenorm case %d: B%d H%d Lq%d Lk%d D%d lens %s shift %g std %g residual %s" % (
+        i, B, H, Lq, Lk, D, lens, shift, std, residual)
+    N = H * D
+    x = (randn((B, Lq, N), 8000 + i, std) + shift).to(torch.bfloat16)
+    g = 1.0 + 0.1 * randn((N,), 8100 + i)
+    b = 0.1 * randn((N,), 8200 + i)
+    k = randn((B, H, Lk, D), 8300 + i, 1.0, torch.bfloat16)
+    v = randn((B, H, Lk, D), 8400 + i, 1.0, torch.bfloat16)
+    lt = lens_tensor(lens)
+    fn = mha.prenorm_cross_attn_residual_fwd if residual else mha.prenorm_cross_attn_fwd
+    out = fn(dev(x), dev(g), dev(b), 1e-5, dev(k), dev(v), dev(lt))
+    torch.cuda.synchronize()
+    ofn = oracle.prenorm_cross_attn_residual if residual else oracle.prenorm_cross_attn
+    want = ofn(x.float().numpy(), g.numpy(), b.numpy(), 1e-5, k.float().numpy(), v.float().numpy(),
+               lens)
+    (check_bf16_sum if residual else check_bf16)(as_np(out), want, what)
     assert mha.device_status() == 0
