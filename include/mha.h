@@ -217,9 +217,11 @@ MHA_API size_t mha_bwd_workspace_size(int B, int H, int Lq, int D, int dtype);
  * padding mask only (kv_lengths, or none when it is NULL).  One kernel runs
  * on `stream` and allocates nothing: it groups the heads of each block of
  * 256 query rows into chunks, forms each row's mean and 1/sqrt(var + eps)
- * from the full row of x once per chunk (inside the kernel, in fp32, two
- * passes), loads each head's slice of x with TMA and normalises it in
- * shared memory before the first QK^T product.
+ * from the full row of x inside the kernel (in fp32, two passes; at D = 64
+ * before any attention work, shared by the two CTAs of a thread-block
+ * cluster that take chunks of the same rows), loads each head's slice of x
+ * with TMA and normalises it in shared memory before the first QK^T
+ * product.
  *   x_q         [B,Lq,H*D] bf16 (query-side activations)
  *   gamma, beta fp32 [H*D]
  *   eps         finite, >= 0
