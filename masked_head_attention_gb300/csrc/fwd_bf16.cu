@@ -251,13 +251,6 @@ __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// 16-byte store into the shared memory of another CTA of the cluster.
-__device__ __forceinline__ void st_cluster_u32x4(uint32_t addr, uint4 v) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Pre-LN, step 1: per-row statistics of x [rows, N] ("How to fuse cross-
 // attention and layer-norm into a single CUDA kernel?" (cms365.cn), answer

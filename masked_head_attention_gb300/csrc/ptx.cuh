@@ -26,7 +26,7 @@ enum WaitSite : uint32_t {
     kSiteQFull = 0, kSiteKFull = 1, kSiteVFull = 2, kSiteKvEmpty = 3,
     kSiteSFull = 4, kSitePFull = 5, kSitePvDone = 6, kSiteQEmpty = 7,
     kSiteOFree = 8, kSiteDrain = 9, kSiteSelftest = 10, kSiteWg = 11,
-    kSiteStats = 12, kSiteTest = 13,   // kSiteStats: Pre-LN statistics prologue
+    kSiteStats = 12 /* no longer used */, kSiteTest = 13,
 };
 
 // Numeric flags, bits 16 and up of the same word ("softmax sum != 1 is an
@@ -221,8 +221,10 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float2 v) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+// 16-byte store into the shared memory of another CTA of the cluster.
+__device__ __forceinline__ void st_cluster_u32x4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
                  : "memory");
 }
 
