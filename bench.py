@@ -53,14 +53,21 @@ TF32X3_D = 64              # fp32 inputs with this head dimension run on the ten
 TF32_OVER_BF16 = 1.1 / 2.25
 
 
+# fp32 forward kernel choice (--f32-kernel): 0 automatic (3xTF32 for D = 64),
+# 1 the tiled CUDA-core kernel, 2 the short-key-range CUDA-core kernel where it
+# applies (else the tiled one).
+F32_KERNEL = 0
+
+
 def uses_tf32x3(w):
-    return w.kind == "mha" and w.dtype == "f32" and w.D == TF32X3_D
+    return w.kind == "mha" and w.dtype == "f32" and w.D == TF32X3_D and F32_KERNEL == 0
 
 
 def kernel_of(w):
     if uses_tf32x3(w):
         return "attn_fwd_tf32x3_kernel"
-    if w.kind == "mha" and w.dtype == "f32" and w.Lk * w.D <= SMALL_F32_MAX_KD:
+    if (w.kind == "mha" and w.dtype == "f32" and w.Lk * w.D <= SMALL_F32_MAX_KD
+            and F32_KERNEL != 1):
         return "mha_fwd_f32_small_kernel"
     if w.kind == "mha" and w.dtype == "bf16" and w.Lq <= DECODE_MAX_ROWS:
         return "attn_decode_bf16_kernel"
@@ -666,10 +673,15 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="run the workload with this batch size instead (profiling captures "
                          "of a smaller case of the same kernel); 0 = the workload's own")
+    ap.add_argument("--f32-kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="fp32 forward kernel: 0 automatic, 1 tiled CUDA-core kernel, 2 "
+                         "short-key-range CUDA-core kernel where it applies (profiling)")
     ap.add_argument("--settle-s", type=float, default=1.0,
                     help="untimed back-to-back steps before the timed region (clock settling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    global F32_KERNEL
+    F32_KERNEL = args.f32_kernel
     if args.batch > 0:
         import dataclasses
         w0 = synthetic.WORKLOADS[args.workload]
@@ -687,6 +699,8 @@ def main():
     mha.lib()   # fails loudly when the extension is missing
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if F32_KERNEL:
+        mha.set_f32_kernel(F32_KERNEL)
     props = torch.cuda.get_device_properties(device)
     n_sm = props.multi_processor_count
     l2 = getattr(props, "L2_cache_size", 0) or DEFAULT_L2
@@ -734,7 +748,8 @@ def main():
                            "nominal_tflops": round(world * nominal_flops(w) / ms_per_step / 1e9, 3),
                            "l2_policy": "%d rotating input sets of %.1f MB (> 2x L2 %.0f MB)" % (
                                len(wl.sets), wl.set_bytes / 1e6, l2 / 1e6),
-                           "parallelism": "replicas x%d (weak scaling, no collective)" % world},
+                           "parallelism": "replicas x%d (weak scaling, no collective)" % world,
+                           **({"f32_kernel": kernel_of(w)} if F32_KERNEL else {})},
                 "roofline": roof, "e2e": e2e, "gpu_launches": args.steps,
                 "clocks": clk.summary(), "device_status": status}
         del wl

@@ -143,3 +143,22 @@ def test_nvtx_range_is_harmless_without_a_gpu():
     with bench.nvtx_range("phase"):
         x = 1
     assert x == 1
+
+
+def test_forced_f32_kernel_changes_the_reported_kernel_and_roof(monkeypatch):
+    """--f32-kernel 1 / 2 (profiling the CUDA-core kernels) must make the
+    bench report those kernels and their FFMA roof, not the 3xTF32 one."""
+    c1 = synthetic.WORKLOADS["c1_causal_f32"]
+    c2 = synthetic.WORKLOADS["c2_padding_f32"]
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 7000.0, "_source": "test"}
+    monkeypatch.setattr(bench, "F32_KERNEL", 1)
+    assert bench.kernel_of(c2) == "mha_fwd_f32_kernel"
+    assert bench.kernel_of(c1) == "mha_fwd_f32_kernel"
+    assert not bench.uses_tf32x3(c2)
+    r = bench.roofline_for(c2, [512] * 16, 0.1, peaks, 152)
+    assert r["kernel"] == "mha_fwd_f32_kernel" and "tensor_issue_frac" not in r
+    monkeypatch.setattr(bench, "F32_KERNEL", 2)
+    assert bench.kernel_of(c1) == "mha_fwd_f32_small_kernel"   # Lk * D = 8192
+    assert bench.kernel_of(c2) == "mha_fwd_f32_kernel"         # Lk * D = 32768
+    monkeypatch.setattr(bench, "F32_KERNEL", 0)
+    assert bench.kernel_of(c1) == "attn_fwd_tf32x3_kernel"
