@@ -31,6 +31,21 @@ extern "C" {
 MHA_API void mha_set_bf16_grid(int ctas);
 
 /*
+ * mha_plan_prenorm -- the launch plan the Pre-LN forward (bf16) would use
+ * for these sizes on a grid of `grid` CTAs, from the host logic alone (no
+ * device needed).  out[0..5] = heads per chunk G, head groups per row block
+ * H / G, CTAs per thread-block cluster (2: the two CTAs share each block's
+ * row statistics), chunks whose statistics each CTA forms before its roles
+ * start (0: at the chunk starts, or none when stats_given: the statistics
+ * come from the no-allocation entry point's array), the grid after clamping
+ * to the chunk count, and the chunk count.  Returns MHA_OK,
+ * MHA_ERR_INVALID_ARG (non-positive sizes or grid, D not 64 or 128, null out)
+ * or MHA_ERR_TOO_LARGE.
+ */
+MHA_API int mha_plan_prenorm(int B, int H, int Lq, int Lk, int D, int grid, int stats_given,
+                             int64_t *out);
+
+/*
  * mha_set_f32_kernel -- fp32 kernel choice.  0 = automatic: for D = 64 the
  * tensor-core kernel (three TF32 MMAs per product: hi*hi + lo*hi + hi*lo of
  * the operands split as x = hi + lo, fp32 accumulation in TMEM); for D = 128

@@ -73,6 +73,8 @@ def lib():
         L.mha_selftest_umma.restype = i
         L.mha_set_bf16_grid.argtypes = [i]
         L.mha_set_bf16_grid.restype = None
+        L.mha_plan_prenorm.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int64)]
+        L.mha_plan_prenorm.restype = i
         L.mha_set_f32_kernel.argtypes = [i]
         L.mha_set_f32_kernel.restype = None
         L.mha_set_bf16_decode.argtypes = [i]
@@ -400,6 +402,16 @@ def selftest_umma(variant, kn, a, b, c, stream=None):
 
 def set_bf16_grid(ctas):
     lib().mha_set_bf16_grid(int(ctas))
+
+
+def plan_prenorm(B, H, Lq, Lk, D, grid, stats_given=False):
+    """Test hook: the Pre-LN forward's launch plan for these sizes on `grid`
+    CTAs (host logic; no device needed): dict with G (heads per chunk), n_hg,
+    cs (CTAs per cluster), pre_chunks, grid, n_chunks."""
+    out = (ctypes.c_int64 * 6)()
+    _check(lib().mha_plan_prenorm(int(B), int(H), int(Lq), int(Lk), int(D), int(grid),
+                                  1 if stats_given else 0, out), "mha_plan_prenorm")
+    return dict(zip(("G", "n_hg", "cs", "pre_chunks", "grid", "n_chunks"), (int(v) for v in out)))
 
 
 def set_bf16_decode(mode):

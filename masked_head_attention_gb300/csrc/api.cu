@@ -500,6 +500,20 @@ int mha_selftest_umma(int variant, int K_or_N, const void *a, const void *b, flo
 // Test and benchmark hooks (mha_testing.h); thread-local state.
 void mha_set_bf16_grid(int ctas) { mha::set_bf16_grid_override(ctas); }
 
+int mha_plan_prenorm(int B, int H, int Lq, int Lk, int D, int grid, int stats_given, int64_t *out) {
+    if (out == nullptr || B <= 0 || H <= 0 || Lq <= 0 || Lk < 0 || grid <= 0 || (D != 64 && D != 128))
+        return MHA_ERR_INVALID_ARG;
+    if ((int64_t)H * D > 65536 || (int64_t)B * H * ((Lq + 255) / 256) > 0x7fffffffll) return MHA_ERR_TOO_LARGE;
+    const mha::PrenormPlan pl = mha::plan_prenorm(B, H, Lq, Lk, D, grid, stats_given != 0);
+    out[0] = pl.G;
+    out[1] = pl.n_hg;
+    out[2] = pl.cs;
+    out[3] = pl.pre_chunks;
+    out[4] = pl.grid;
+    out[5] = pl.n_chunks;
+    return MHA_OK;
+}
+
 void mha_set_f32_kernel(int which) { mha::set_f32_kernel_override(which); }
 
 void mha_set_bf16_decode(int mode) { mha::set_decode_override(mode); }

@@ -1300,6 +1300,58 @@ static int prologue_chunks_max(int D) {
     return D == 64 ? Cfg<64>::kPreChunksMax : Cfg<128>::kPreChunksMax;
 }
 
+PrenormPlan plan_prenorm(int B, int H, int Lq, int Lk, int D, int grid, bool stats_given) {
+    PrenormPlan pl;
+    const long long n_items = (long long)B * H * ((Lq + 2 * kTileRows - 1) / (2 * kTileRows));
+    // Heads per chunk.  A chunk forms its rows' statistics once for its G
+    // items, and a CTA runs at most ceil(chunks / grid) chunks.  Where the
+    // prologue can hold the statistics of all of a CTA's chunks (D = 64),
+    // forming them costs about kPre N/Lk items' worth of work per chunk,
+    // shared by the kPair CTAs of a cluster when the head groups pair up; at
+    // the chunk starts inside the item loop about kLoop N/Lk (N features per
+    // row of x against Lk keys per row of attention; both factors measured on
+    // the Pre-LN workload); statistics read from the caller's array cost
+    // nothing.  Take the divisor of H that minimises
+    //     ceil(chunks / grid) * (G + factor * N / Lk).
+    // (Clusters of two CTAs all fit at once, one per SM; clusters of four
+    // left 8 of 152 SMs idle.)
+    constexpr double kPre = 1.0, kLoop = 2.2;
+    constexpr int kPair = 2;
+    const int pre_max = prologue_chunks_max(D);
+    const double ratio = (double)(H * D) / (double)(Lk > 0 ? Lk : 1);
+    double best = 0.0;
+    pl.G = 1;
+    for (int g = 1; g <= H; ++g) {
+        if (H % g != 0) continue;
+        const long long chunks = n_items / g;
+        const long long per_cta = (chunks + grid - 1) / grid;
+        const bool pre = !stats_given && per_cta <= pre_max;
+        const bool pair = pre && (H / g) % kPair == 0 && grid % kPair == 0;
+        const double factor = stats_given ? 0.0 : pre ? kPre / (pair ? kPair : 1) : kLoop;
+        const double cost = (double)per_cta * (g + factor * ratio);
+        if (g == 1 || cost < best) {
+            best = cost;
+            pl.G = g;
+        }
+    }
+    pl.n_hg = H / pl.G;
+    pl.n_chunks = n_items / pl.G;
+    pl.grid = grid < pl.n_chunks ? grid : (int)pl.n_chunks;
+    pl.cs = 1;
+    pl.pre_chunks = 0;
+    if (!stats_given) {
+        const int per_cta = (int)((pl.n_chunks + pl.grid - 1) / pl.grid);
+        pl.pre_chunks = per_cta < pre_max ? per_cta : pre_max;
+        // Two CTAs of a cluster take two head groups of the same blocks and
+        // form half of each block's row statistics each.
+        if (pl.pre_chunks == per_cta && pl.n_hg % 2 == 0 && pl.grid % 2 == 0) {
+            pl.cs = 2;
+            pl.pre_chunks = (int)((pl.n_chunks / 2 + pl.grid / 2 - 1) / (pl.grid / 2));
+        }
+    }
+    return pl;
+}
+
 cudaError_t status_ctl_fwd_bf16(int op, uint64_t value, uint32_t *bits) {
     return unit_status_ctl(op, value, bits);
 }
@@ -1396,38 +1448,14 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     p.G = 1;
     // Persistent grid: one CTA per SM (one fits per SM), unless overridden.
     int grid = g_grid_override > 0 ? g_grid_override : device_info().sms;
+    p.cs = 1;
     if (prenorm) {
-        // Heads per chunk.  A chunk forms its rows' statistics once for its G
-        // items, and a CTA runs at most ceil(chunks / grid) chunks.  Where the
-        // prologue can hold the statistics of all of a CTA's chunks (D = 64),
-        // forming them costs about kPre N/Lk items' worth of work per chunk,
-        // shared by the kPair CTAs of a cluster when the head groups pair up;
-        // at the chunk starts inside the item loop about kLoop N/Lk (N
-        // features per row of x against Lk keys per row of attention; both
-        // factors measured on the Pre-LN workload); statistics read from the
-        // caller's array cost nothing.  Take the divisor of H that minimises
-        //     ceil(chunks / grid) * (G + factor * N / Lk).
-        // (Clusters of two CTAs all fit at once, one per SM; clusters of four
-        // left 8 of 152 SMs idle.)
-        constexpr double kPre = 1.0, kLoop = 2.2;
-        constexpr int kPair = 2;
-        const int pre_max = prologue_chunks_max(c.D);
-        const double ratio = (double)(c.H * c.D) / (double)(c.Lk > 0 ? c.Lk : 1);
-        double best = 0.0;
-        for (int g = 1; g <= c.H; ++g) {
-            if (c.H % g != 0) continue;
-            const long long chunks = (long long)p.n_items / g;
-            const long long per_cta = (chunks + grid - 1) / grid;
-            const bool pre = ln_stats == nullptr && per_cta <= pre_max;
-            const bool pair = pre && (c.H / g) % kPair == 0 && grid % kPair == 0;
-            const double factor = ln_stats != nullptr ? 0.0 : pre ? kPre / (pair ? kPair : 1) : kLoop;
-            const double cost = (double)per_cta * (g + factor * ratio);
-            if (g == 1 || cost < best) {
-                best = cost;
-                p.G = g;
-            }
-        }
-        p.n_hg = c.H / p.G;
+        const PrenormPlan pl = plan_prenorm(c.B, c.H, c.Lq, c.Lk, c.D, grid, ln_stats != nullptr);
+        p.G = pl.G;
+        p.n_hg = pl.n_hg;
+        p.cs = pl.cs;
+        p.pre_chunks = pl.pre_chunks;
+        grid = pl.grid;
         p.x = reinterpret_cast<const __nv_bfloat16 *>(c.x);
         p.N = c.H * c.D;
         p.eps = c.eps;
@@ -1435,18 +1463,6 @@ cudaError_t launch_fwd_bf16(const Bf16Call &c, cudaStream_t stream, int *driver_
     }
     p.n_chunks = p.n_items / p.G;
     if (grid > p.n_chunks) grid = p.n_chunks;
-    p.cs = 1;
-    if (prenorm && ln_stats == nullptr) {
-        const int pre_max = prologue_chunks_max(c.D);
-        const int per_cta = (p.n_chunks + grid - 1) / grid;
-        p.pre_chunks = per_cta < pre_max ? per_cta : pre_max;
-        // Two CTAs of a cluster take two head groups of the same blocks and
-        // form half of each block's row statistics each.
-        if (p.pre_chunks == per_cta && p.n_hg % 2 == 0 && grid % 2 == 0) {
-            p.cs = 2;
-            p.pre_chunks = (p.n_chunks / 2 + grid / 2 - 1) / (grid / 2);
-        }
-    }
     {
         // (b, h) problems per scheduling group: their K and V together take
         // at most 1/kL2GroupDenom of L2.

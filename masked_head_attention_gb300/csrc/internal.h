@@ -172,6 +172,17 @@ constexpr int kStatusUnits = 4;
 
 // Launch-configuration overrides used by tests and benchmark sweeps (0 = default).
 void set_bf16_grid_override(int ctas);
+
+// Launch plan of the Pre-LN bf16 forward (host logic only): heads per chunk G,
+// head groups per row block n_hg = H / G, CTAs per cluster cs (2 when the
+// prologue's shared statistics pair up), chunks whose statistics the prologue
+// forms per CTA (0: formed at the chunk starts, or read from the caller's
+// array when stats_given), the grid and the chunk count.
+struct PrenormPlan {
+    int G, n_hg, cs, pre_chunks, grid;
+    long long n_chunks;
+};
+PrenormPlan plan_prenorm(int B, int H, int Lq, int Lk, int D, int grid, bool stats_given);
 void set_f32_kernel_override(int which);
 
 }  // namespace mha
