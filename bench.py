@@ -643,6 +643,10 @@ def measure_config(w, args, device, peaks, n_sm, l2):
                                           "tensor_issue_frac") if k in r},
            "hbm_gbs": round(algorithmic_bytes(w, wl.lens) / call_ms / 1e6, 1),
            "input_sets": len(wl.sets)}
+    if w.kind in ("prenorm", "prenorm_residual"):
+        # Heads per chunk of shared row statistics, cluster pairs, prologue
+        # chunks per CTA: the plan the launch used.
+        out["launch_plan"] = wl.mha.plan_prenorm(w.B, w.H, w.Lq, w.Lk, w.D, n_sm)
     if call_ms < 0.05:
         # Short calls are bound by the host's launch rate when issued one by
         # one from Python; a CUDA graph of back-to-back calls shows the GPU side.
